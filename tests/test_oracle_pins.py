@@ -1,0 +1,337 @@
+"""Pins of the float64 oracle to facts fixed by the pages and by mathematics.
+
+Each test checks the oracle against something other than itself: closed forms,
+a worked example, invariants, brute force on tiny inputs, or a textbook library
+routine (torch's CPU float64 scaled-dot-product attention).  The choice is such
+that a plausible slip (a dropped term, a sign, an index, a transposed operand,
+the wrong half of ``kv_b_proj``) fails at least one test.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import mla_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rng(seed):
+    return np.random.default_rng(seed)
+
+
+# ---------------------------------------------------------------- RoPE pins
+
+def test_rope_position_zero_is_the_deinterleave_permutation():
+    # At position 0 every angle is 0: the prefix leaves as [a0.., b0..], tail kept.
+    x = rng(0).standard_normal((2, 1, 3, 12)).astype(np.float32)
+    y = O.rope_partial_interleaved(x, 0, 8, 10000.0)
+    want = np.concatenate([x[..., 0:8:2], x[..., 1:8:2], x[..., 8:]], axis=-1)
+    assert np.array_equal(y, want.astype(np.float64))
+
+
+def test_rope_pair_zero_closed_form():
+    # invf_0 = theta^0 = 1, so pair 0 turns by exactly `position` radians.
+    assert O.rope_inverse_frequencies(64, 10000.0)[0] == np.float32(1.0)
+    x = rng(1).standard_normal((1, 5, 1, 64))
+    y = O.rope_partial_interleaved(x, 37, 64, 10000.0)
+    for t in range(5):
+        p = 37 + t
+        a, b = x[0, t, 0, 0], x[0, t, 0, 1]
+        assert y[0, t, 0, 0] == pytest.approx(a * math.cos(p) - b * math.sin(p), abs=1e-12)
+        assert y[0, t, 0, 32] == pytest.approx(b * math.cos(p) + a * math.sin(p), abs=1e-12)
+
+
+def test_rope_inverse_frequencies_closed_form():
+    d, theta = 64, 10000.0
+    invf = O.rope_inverse_frequencies(d, theta)
+    # theta^(-2j/d) at j = d/8 and j = d/4 is 10^-1 and 10^-2.
+    assert invf[8] == np.float32(0.1)
+    assert invf[16] == np.float32(0.01)
+    exact = np.array([theta ** (-2.0 * j / d) for j in range(d // 2)])
+    assert np.all(np.abs(invf - exact) <= 2.0 ** -22 * exact)   # f32 rounding only
+    assert np.all(np.diff(invf) < 0)
+
+
+def test_rope_worked_example():
+    # d = 4, theta = 1e4, position 1: pair angles (1, 0.01); width 6 keeps a tail of 2.
+    ex = json.load(open(os.path.join(GOLDEN, "rope_worked_example.json")))
+    x = np.array(ex["input"], dtype=np.float64).reshape(1, 1, 1, 6)
+    y = O.rope_partial_interleaved(x, ex["position"], ex["rotary_dims"], ex["theta"])[0, 0, 0]
+    a0, b0, a1, b1, t0, t1 = ex["input"]
+    c1, s1 = math.cos(1.0), math.sin(1.0)
+    th = float(np.float32(0.01))
+    c2, s2 = math.cos(th), math.sin(th)
+    want = [a0 * c1 - b0 * s1, a1 * c2 - b1 * s2, b0 * c1 + a0 * s1, b1 * c2 + a1 * s2, t0, t1]
+    assert np.allclose(y, want, rtol=0, atol=1e-12)
+    assert np.allclose(y, ex["expected"], rtol=0, atol=1e-12)
+
+
+def test_rope_preserves_pair_norms_and_relative_positions():
+    r = rng(2)
+    q = r.standard_normal((1, 1, 1, 64))
+    k = r.standard_normal((1, 1, 1, 64))
+    for p in (0, 5, 4095, 131071):
+        y = O.rope_partial_interleaved(q, p, 64, 10000.0)[0, 0, 0]
+        pairs = q[0, 0, 0].reshape(32, 2)
+        assert np.allclose(y[:32] ** 2 + y[32:] ** 2, (pairs ** 2).sum(-1), rtol=1e-12)
+    def dot(m, n):
+        return float(O.rope_partial_interleaved(q, m, 64, 10000.0)[0, 0, 0]
+                     @ O.rope_partial_interleaved(k, n, 64, 10000.0)[0, 0, 0])
+    # <R(q,m), R(k,n)> depends on m - n only (up to the f32 angle rounding).
+    for m, n, delta in ((7, 3, 100), (50, 49, 900), (1000, 0, 24)):
+        assert dot(m, n) == pytest.approx(dot(m + delta, n + delta), abs=1e-3)
+
+
+def test_rope_per_row_offsets_match_scalar_calls():
+    x = rng(3).standard_normal((3, 4, 2, 16))
+    offs = [0, 9, 1000]
+    y = O.rope_partial_interleaved(x, offs, 16, 10000.0)
+    for r, o in enumerate(offs):
+        assert np.array_equal(y[r:r + 1], O.rope_partial_interleaved(x[r:r + 1], o, 16, 10000.0))
+
+
+def test_rope_rejects_what_the_page_rejects():
+    x = np.zeros((1, 1, 1, 8))
+    for bad in (dict(rotary_dims=3), dict(rotary_dims=0), dict(rotary_dims=10)):
+        with pytest.raises(ValueError):
+            O.rope_partial_interleaved(x, 0, bad["rotary_dims"], 10000.0)
+    with pytest.raises(ValueError):
+        O.rope_partial_interleaved(x, -1, 8, 10000.0)
+    with pytest.raises(ValueError):
+        O.rope_partial_interleaved(x, 0, 8, 0.0)
+
+
+# ---------------------------------------------------------------- attention helpers
+
+def tiny(seed=0, B=2, S=1, T=9, H=3, rank=6, nope=4, rope=4, v=5):
+    r = rng(seed)
+    return dict(
+        q_nope=r.standard_normal((B * S, H, nope)),
+        q_rope=r.standard_normal((B * S, H, rope)),
+        latent=r.standard_normal((B, T, rank)),
+        rope=r.standard_normal((B, T, rope)),
+        kv_b_proj=r.standard_normal((H * (nope + v), rank)) / math.sqrt(rank),
+        dims=dict(heads=H, nope=nope, v=v, s_q=S),
+    )
+
+
+def run_rec(d, kv_start, kv_len, **kw):
+    out, lse = O.attend_reconstructed(d["q_nope"], d["q_rope"], d["latent"], d["rope"],
+                                      d["kv_b_proj"], kv_start, kv_len, **d["dims"], **kw)
+    return out, lse
+
+
+def run_abs(d, kv_start, kv_len, **kw):
+    return O.attend_absorbed(d["q_nope"], d["q_rope"], d["latent"], d["rope"],
+                             d["kv_b_proj"], kv_start, kv_len, **d["dims"], **kw)
+
+
+# ---------------------------------------------------------------- attention pins
+
+def test_brute_force_loops_tiny():
+    """Pure-Python loops (no numpy algebra) on a tiny causal, left-padded case."""
+    d = tiny(seed=4, B=2, S=2, T=6, H=2, rank=3, nope=2, rope=2, v=2)
+    kv_start, kv_len = [1, 0], [5, 6]
+    out, lse = run_rec(d, kv_start, kv_len)
+    H, nope, v = 2, 2, 2
+    W = d["kv_b_proj"]
+    for n in range(4):
+        b, i = divmod(n, 2)
+        last = kv_len[b] - 2 + i                       # last visible window key
+        for h in range(H):
+            scores, vals = [], []
+            for t in range(last + 1):
+                row = kv_start[b] + t
+                lat = d["latent"][b][row]
+                kn = [sum(W[h * (nope + v) + c][r] * lat[r] for r in range(3)) for c in range(nope)]
+                vv = [sum(W[h * (nope + v) + nope + c][r] * lat[r] for r in range(3)) for c in range(v)]
+                s = sum(d["q_nope"][n][h][c] * kn[c] for c in range(nope))
+                s += sum(d["q_rope"][n][h][c] * d["rope"][b][row][c] for c in range(2))
+                scores.append(s / math.sqrt(nope + 2))
+                vals.append(vv)
+            mx = max(scores)
+            e = [math.exp(s - mx) for s in scores]
+            z = sum(e)
+            want = [sum(e[t] * vals[t][c] for t in range(len(e))) / z for c in range(v)]
+            assert np.allclose(out[n, h], want, rtol=1e-12, atol=1e-14)
+            assert lse[n, h] == pytest.approx(mx + math.log(z), rel=1e-12)
+
+
+def test_reconstructed_matches_torch_sdpa_float64():
+    """Textbook scaled-dot-product attention (torch CPU, float64) with an explicit mask."""
+    d = tiny(seed=5, B=2, S=3, T=11, H=4, rank=8, nope=6, rope=4, v=5)
+    kv_start, kv_len = [2, 0], [9, 11]
+    out, _ = run_rec(d, kv_start, kv_len)
+    H, nope, v, S = 4, 6, 5, 3
+    W = torch.tensor(d["kv_b_proj"])
+    for b in range(2):
+        lat = torch.tensor(d["latent"][b])
+        kv = torch.einsum("tr,or->to", lat, W).reshape(-1, H, nope + v)
+        k = torch.cat([kv[..., :nope], torch.tensor(d["rope"][b])[:, None, :].expand(-1, H, -1)], -1)
+        val = kv[..., nope:]
+        q = torch.cat([torch.tensor(d["q_nope"][b * S:(b + 1) * S]),
+                       torch.tensor(d["q_rope"][b * S:(b + 1) * S])], -1)        # [S, H, 10]
+        T = lat.shape[0]
+        mask = torch.zeros(S, T, dtype=torch.bool)
+        for i in range(S):
+            lo, hi = kv_start[b], kv_start[b] + kv_len[b] - S + i
+            mask[i, lo:hi + 1] = True
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q.transpose(0, 1), k.transpose(0, 1), val.transpose(0, 1), attn_mask=mask)
+        assert np.allclose(out[b * S:(b + 1) * S], ref.transpose(0, 1).numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_absorbed_equals_reconstructed():
+    """The page's two forms compute one function (absorption is exact algebra)."""
+    d = tiny(seed=6, B=3, S=2, T=13, H=3, rank=16, nope=8, rope=4, v=8)
+    kv_start, kv_len = [0, 3, 1], [13, 10, 7]
+    rec, lse_r = run_rec(d, kv_start, kv_len)
+    out, ctx, lse_a, _ = run_abs(d, kv_start, kv_len)
+    assert np.allclose(out, rec, rtol=1e-12, atol=1e-13)
+    assert np.allclose(lse_a, lse_r, rtol=1e-12)
+    # and with a selection
+    sel = np.array([[0, 2, 5], [1, 1, 4], [0, 8, 3], [8, 2, 0], [3, 5, 1], [0, 6, 2]], np.int64)
+    cnt = [3, 2, 3, 2, 1, 3]
+    rec, _ = run_rec(d, kv_start, kv_len, sel=sel, sel_count=cnt)
+    out, _, _, _ = run_abs(d, kv_start, kv_len, sel=sel, sel_count=cnt)
+    assert np.allclose(out, rec, rtol=1e-12, atol=1e-13)
+
+
+def test_one_visible_key_returns_its_value():
+    d = tiny(seed=7)
+    sel = np.array([[4], [2]])
+    out, lse = run_rec(d, [0, 0], [9, 9], sel=sel, sel_count=[1, 1])
+    H, nope, v = 3, 4, 5
+    for b, t in ((0, 4), (1, 2)):
+        for h in range(H):
+            _, w_uv = O.head_weights(d["kv_b_proj"], h, nope, v)
+            assert np.allclose(out[b, h], w_uv @ d["latent"][b][t], rtol=1e-12)
+            w_uk, _ = O.head_weights(d["kv_b_proj"], h, nope, v)
+            s = (d["q_nope"][b, h] @ (w_uk @ d["latent"][b][t]) + d["q_rope"][b, h] @ d["rope"][b][t]) / math.sqrt(8)
+            assert lse[b, h] == pytest.approx(s, rel=1e-12)
+
+
+def test_zero_query_averages_values():
+    d = tiny(seed=8)
+    d["q_nope"][:] = 0.0
+    d["q_rope"][:] = 0.0
+    out, lse = run_rec(d, [0, 2], [9, 7])
+    for b, (s, n) in enumerate(((0, 9), (2, 7))):
+        for h in range(3):
+            _, w_uv = O.head_weights(d["kv_b_proj"], h, 4, 5)
+            assert np.allclose(out[b, h], (w_uv @ d["latent"][b][s:s + n].T).mean(-1), rtol=1e-12)
+            assert lse[b, h] == pytest.approx(math.log(n), rel=1e-12)
+
+
+def test_value_and_key_halves_of_kv_b_proj():
+    d = tiny(seed=9)
+    H, nope, v = 3, 4, 5
+    w = d["kv_b_proj"].copy()
+    for h in range(H):                       # zero every W_UV_h: output must vanish
+        w[h * (nope + v) + nope:(h + 1) * (nope + v)] = 0.0
+    out, _ = O.attend_reconstructed(d["q_nope"], d["q_rope"], d["latent"], d["rope"], w,
+                                    [0, 0], [9, 9], **d["dims"])
+    assert np.all(out == 0.0)
+    w = d["kv_b_proj"].copy()
+    for h in range(H):                       # zero every W_UK_h: scores are the rope term only
+        w[h * (nope + v):h * (nope + v) + nope] = 0.0
+    out, _ = O.attend_reconstructed(d["q_nope"], d["q_rope"], d["latent"], d["rope"], w,
+                                    [0, 0], [9, 9], **d["dims"])
+    for b in range(2):
+        for h in range(H):
+            s = d["rope"][b] @ d["q_rope"][b, h] / math.sqrt(8)
+            p = np.exp(s - s.max()); p /= p.sum()
+            _, w_uv = O.head_weights(w, h, nope, v)
+            assert np.allclose(out[b, h], p @ (d["latent"][b] @ w_uv.T), rtol=1e-12)
+
+
+def test_selection_semantics():
+    d = tiny(seed=10, T=12)
+    kv_start, kv_len = [0, 2], [12, 10]
+    dense, _ = run_rec(d, kv_start, kv_len)
+    all_sel = np.array([np.arange(12), np.r_[np.arange(10), 0, 0]])
+    out, _ = run_rec(d, kv_start, kv_len, sel=all_sel, sel_count=[12, 10])
+    assert np.allclose(out, dense, rtol=1e-12)             # all positions == dense
+    perm = np.array([rng(11).permutation(12), np.r_[rng(12).permutation(10), 0, 0]])
+    out_p, _ = run_rec(d, kv_start, kv_len, sel=perm, sel_count=[12, 10])
+    assert np.allclose(out_p, dense, rtol=1e-12)           # order does not matter
+    # a unique subset == dense attention over a cache that holds only those rows
+    sub = np.array([[1, 4, 7, 11], [0, 3, 9, 0]])
+    out_s, _ = run_rec(d, kv_start, kv_len, sel=sub, sel_count=[4, 3])
+    for b, rows in ((0, [1, 4, 7, 11]), (1, [2 + 0, 2 + 3, 2 + 9])):
+        d2 = dict(d, latent=d["latent"][b:b + 1, rows], rope=d["rope"][b:b + 1, rows],
+                  q_nope=d["q_nope"][b:b + 1], q_rope=d["q_rope"][b:b + 1])
+        ref, _ = run_rec(d2, [0], [len(rows)])
+        assert np.allclose(out_s[b], ref[0], rtol=1e-12)
+    # a duplicated position counts twice (multiset / gather semantics)
+    dup = np.array([[5, 5, 6], [0, 0, 0]])
+    out_d, _ = run_rec(d, kv_start, kv_len, sel=dup, sel_count=[3, -1])
+    d3 = dict(d, latent=d["latent"][0:1, [5, 5, 6]], rope=d["rope"][0:1, [5, 5, 6]],
+              q_nope=d["q_nope"][0:1], q_rope=d["q_rope"][0:1])
+    ref, _ = run_rec(d3, [0], [3])
+    assert np.allclose(out_d[0], ref[0], rtol=1e-12)
+    assert np.allclose(out_d[1], dense[1], rtol=1e-12)     # count -1 == dense row
+
+
+def test_selection_errors_and_empty_rows():
+    d = tiny(seed=13)
+    with pytest.raises(ValueError):
+        run_rec(d, [0, 0], [9, 9], sel=np.array([[0], [0]]), sel_count=[0, 1])
+    with pytest.raises(ValueError):
+        run_rec(d, [0, 0], [9, 9], sel=np.array([[9], [0]]), sel_count=[1, 1])
+    out, lse = run_rec(d, [0, 0], [0, 9])
+    assert np.all(out[0] == 0.0) and np.all(lse[0] == -np.inf)
+
+
+def test_verify_token_equals_single_token_decode():
+    """Token i of a causal S_q-token block sees the prefix a serial decode sees."""
+    S = 4
+    d = tiny(seed=14, B=2, S=S, T=16)
+    kv_start, kv_len = [0, 3], [16, 13]
+    out, _ = run_rec(d, kv_start, kv_len)
+    for b in range(2):
+        for i in range(S):
+            n = b * S + i
+            d1 = dict(d, q_nope=d["q_nope"][n:n + 1], q_rope=d["q_rope"][n:n + 1],
+                      latent=d["latent"][b:b + 1], rope=d["rope"][b:b + 1],
+                      dims=dict(d["dims"], s_q=1))
+            ref, _ = run_rec(d1, [kv_start[b]], [kv_len[b] - S + i + 1])
+            assert np.allclose(out[n], ref[0], rtol=1e-12)
+
+
+def test_left_padding_content_is_ignored():
+    d = tiny(seed=15)
+    out, _ = run_rec(d, [3, 0], [6, 9])
+    d["latent"][0, :3] = 1e6
+    d["rope"][0, :3] = -1e6
+    out2, _ = run_rec(d, [3, 0], [6, 9])
+    assert np.array_equal(out, out2)
+
+
+def test_absorb_and_project_match_einsum():
+    d = tiny(seed=16, H=3, rank=6, nope=4, v=5)
+    q_lat = O.absorb_q(d["q_nope"], d["kv_b_proj"], 3, 4, 5)
+    W = torch.tensor(d["kv_b_proj"]).reshape(3, 9, 6)
+    ref = torch.einsum("nhk,hkr->nhr", torch.tensor(d["q_nope"]), W[:, :4])
+    assert np.allclose(q_lat, ref.numpy(), rtol=1e-12)
+    ctx = rng(17).standard_normal((2, 3, 6))
+    out = O.project_v(ctx, d["kv_b_proj"], 3, 4, 5)
+    ref = torch.einsum("nhr,hvr->nhv", torch.tensor(ctx), W[:, 4:]).reshape(2, 15)
+    assert np.allclose(out, ref.numpy(), rtol=1e-12)
+
+
+def test_gather_selected_is_indexing():
+    r = rng(18)
+    lat = r.integers(-30000, 30000, size=(2, 10, 6)).astype(np.int16)
+    rp = r.integers(-30000, 30000, size=(2, 10, 2)).astype(np.int16)
+    sel = np.array([[3, 1, 0], [8, 4, 4]])
+    g = O.gather_selected(lat, rp, [0, 1], [10, 9], 1, sel, [2, 3], 3)
+    assert np.array_equal(g[0, 0], np.r_[lat[0, 3], rp[0, 3]])
+    assert np.array_equal(g[0, 1], np.r_[lat[0, 1], rp[0, 1]])
+    assert np.all(g[0, 2] == 0)
+    assert np.array_equal(g[1, 0], np.r_[lat[1, 1 + 8], rp[1, 9]])
+    assert np.array_equal(g[1, 2], np.r_[lat[1, 5], rp[1, 5]])
