@@ -1,0 +1,206 @@
+/*
+ * mla.h -- C ABI of libmla: decode of multi-head latent attention (MLA) over a
+ * compressed latent||rope KV cache, on NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow the page "mlx-bun 0.0.11 -> 0.0.13,
+ * package/src/model/glm52-mla.ts" (the MLA page):
+ *   - partialInterleavedRopeMlx         -> mla_rope_partial_interleaved
+ *   - Glm52Mla.attendAbsorbed, q_nope @ Wk      -> mla_absorb_q
+ *   - Glm52Mla.attendAbsorbed, scores, softmax, p @ latent, with the per-row
+ *     windows of Glm52Mla.forward and the selected-position gather
+ *                                        -> mla_decode_attend
+ *   - Glm52Mla.attendAbsorbed, latentContext @ Wv^T, heads concatenated
+ *                                        -> mla_project_v
+ * and the causal verify window of "mlx-bun 0.4.0 -> 1.0.0, glm52.ts",
+ * Glm52DecoderLayer.attend (token i of a block sees the prefix up to itself).
+ *
+ * Conventions shared by every entry point
+ *   - Ownership: the caller allocates and owns every buffer (device memory
+ *     unless stated).  The library never allocates device memory, frees or
+ *     synchronises; scratch memory is a caller-provided workspace.
+ *   - Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).  Nothing is launched when a call returns an
+ *     error, and outputs are then left untouched.
+ *   - Errors: every function returns an mla_status.  Host-side checks of
+ *     scalars, pointers, strides and alignment run before any launch; on
+ *     failure a detail string is kept per thread (mla_last_error_detail).
+ *     A failed launch returns MLA_ERR_CUDA.  Values that only exist on the
+ *     device (lengths, selections) are checked by the kernels, which OR the
+ *     MLA_DEVICE_* bits into *device_status (if non-NULL) and skip the bad
+ *     entry instead of dereferencing it.
+ *   - Layout: strides are in elements; the feature (last) axis is always
+ *     contiguous.  dtype values are mla_dtype.
+ *   - Threads: calls are thread-safe; distinct streams may run concurrently
+ *     as long as their workspaces do not overlap.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (same type, declared without the CUDA headers). */
+typedef struct CUstream_st* mla_stream_t;
+
+typedef enum mla_status {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARGUMENT = 1, /* bad scalar, NULL pointer, bad stride or size */
+  MLA_ERR_UNSUPPORTED = 2,      /* valid request that no kernel here serves     */
+  MLA_ERR_CUDA = 3,             /* a CUDA runtime / launch error                */
+  MLA_ERR_INDEX_OUT_OF_RANGE = 4,
+  MLA_ERR_DEVICE_TIMEOUT = 5
+} mla_status;
+
+typedef enum mla_dtype { MLA_DTYPE_F32 = 0, MLA_DTYPE_BF16 = 1 } mla_dtype;
+
+/* Bits the kernels OR into *device_status. */
+#define MLA_DEVICE_BAD_SELECTION_COUNT (1 << 1) /* a count of 0, < -1 or > k_max   */
+#define MLA_DEVICE_INDEX_OUT_OF_RANGE (1 << 4)  /* a position outside its window    */
+#define MLA_DEVICE_TIMEOUT (1 << 5)             /* a bounded device wait gave up    */
+
+/* Static, never NULL. */
+const char* mla_status_string(int status);
+/* Thread-local detail of the last failed call on this thread ("" if none). */
+const char* mla_last_error_detail(void);
+/* ABI version, (major << 16) | minor. */
+int mla_version(void);
+
+/*
+ * Partial interleaved RoPE (MLA page, partialInterleavedRopeMlx).
+ *
+ * Logical tensor [rows, tokens, inner, width]; element (r, t, i, f) sits at
+ * base + r*strides[0] + t*strides[1] + i*strides[2] + f.  The first
+ * `rotary_dims` features enter pair-interleaved [a0,b0,a1,b1,...] and leave
+ * as split halves [r0..r_{h-1}, i0..i_{h-1}] with r_j = a_j cos - b_j sin and
+ * i_j = b_j cos + a_j sin; features >= rotary_dims are copied.  Position of
+ * token t of row r is p = offset_r + t with offset_r = row_offsets[r] (device
+ * int32 [rows], values must be >= 0) or `position_offset` when row_offsets is
+ * NULL.  Angle of pair j: f32(p * invf_j), invf_j = f32(pow(f32(theta),
+ * f32(-2j / rotary_dims))) -- the page's f32 roundings -- then sincos in f32.
+ * Math is f32; `in` and `out` share `dtype`.  in == out with equal strides
+ * (in place) is allowed; other overlaps are not.
+ * Errors: INVALID_ARGUMENT for NULL pointers, non-positive sizes, odd / zero /
+ * too large rotary_dims (> width or > 256), theta <= 0 or not finite, a
+ * negative position_offset.
+ */
+int mla_rope_partial_interleaved(const void* in, void* out, int dtype, int64_t rows,
+                                 int64_t tokens, int64_t inner, int64_t width,
+                                 const int64_t* in_strides /* host [3] */,
+                                 const int64_t* out_strides /* host [3] */,
+                                 int32_t rotary_dims, float theta,
+                                 const int32_t* row_offsets, int64_t position_offset,
+                                 mla_stream_t stream);
+
+/*
+ * Query absorption (MLA page, attendAbsorbed: "q_nope @ Wk produces latent-space q").
+ *
+ * q_out[n, h, 0:rank] = q_nope[n, h, 0:nope] @ W_UK_h, where W_UK_h is rows
+ * [h*(nope+v_dim), h*(nope+v_dim)+nope) of kv_b_proj ([heads*(nope+v_dim),
+ * rank], row-major, the linear layer's weight).  q_nope[n, h, k] sits at
+ * q_nope + n*q_nope_row_stride + h*q_nope_head_stride + k; q_out likewise.
+ * Only columns [0, rank) of each q_out head row are written, so q_out may be
+ * the packed [n_q, H, rank+rope] query that mla_decode_attend reads.
+ * fp32 accumulation; all three tensors have `dtype`.
+ * bf16 with nope = 128, rank = 512, n_q <= 256 and 16-byte aligned pointers
+ * and strides runs on the tensor cores (tcgen05); everything else on the CUDA
+ * cores.
+ */
+int mla_absorb_q(const void* q_nope, int64_t q_nope_row_stride, int64_t q_nope_head_stride,
+                 const void* kv_b_proj, void* q_out, int64_t q_out_row_stride,
+                 int64_t q_out_head_stride, int dtype, int32_t n_q, int32_t heads, int32_t nope,
+                 int32_t v_dim, int32_t rank, mla_stream_t stream);
+
+/*
+ * Latent-space decode attention (MLA page, attendAbsorbed: combined scores,
+ * scale, softmax, p @ latent; with Glm52Mla.forward's per-row windows and
+ * selected positions, and the verify window of Glm52DecoderLayer.attend).
+ *
+ * Query rows n = b*s_q + i (batch row b, token i < s_q).  q[n, h, 0:rank] is
+ * the absorbed query and q[n, h, rank:rank+rope_dim] the rotated q_rope
+ * (mla_absorb_q and mla_rope_partial_interleaved write exactly this).
+ * Cache: row t of batch row b is latent[b*latent_batch_stride +
+ * (kv_start[b]+t)*latent_row_stride + 0:rank] and rope[...] likewise, for
+ * t < kv_len[b]; kv_start == NULL means 0.  Rows may be packed (batch stride
+ * 0, kv_start = prefix sums) or padded (kv_start = the page's left pad);
+ * kv_start[b] + kv_len[b] <= t_max is the caller's promise.  Token i of row
+ * b sees window keys t <= kv_len[b] - s_q + i (causal among the s_q tokens).
+ * Selection: if selected_positions != NULL, row n attends to the window keys
+ * selected_positions[n*k_max + 0 .. count-1] (a multiset, any order), with
+ * count = selected_counts[n]; count == -1 means dense.  A count of 0, < -1
+ * or > k_max sets MLA_DEVICE_BAD_SELECTION_COUNT and the row attends to
+ * nothing; a position outside the token's visible window sets
+ * MLA_DEVICE_INDEX_OUT_OF_RANGE and is skipped.
+ * s = (q_lat . latent_t + q_rope . rope_t) * softmax_scale (the page's scale
+ * is 1/sqrt(qk_nope + qk_rope)); p = softmax(s); ctx = sum_t p_t latent_t.
+ * Outputs: ctx_out[n*ctx_row_stride + h*ctx_head_stride + 0:rank] in
+ * out_dtype, and lse_out[n*heads + h] = log(sum_t exp(s_t)) (f32, may be
+ * NULL).  A row with no visible key gets ctx = 0 and lse = -inf.
+ * q, latent and rope have `dtype`.  workspace must hold
+ * mla_decode_workspace_size(...) bytes (256-byte aligned) and may be NULL
+ * when that size is 0.
+ * bf16 with heads = 128, rank = 512, rope_dim = 64 runs the tensor-core
+ * flash-decode kernel (tcgen05 + TMA, split-K over SM pairs); other shapes
+ * and f32 run a CUDA-core kernel.  mla_decode_kernel_kind tells which.
+ */
+int mla_decode_attend(const void* q, int64_t q_row_stride, int64_t q_head_stride,
+                      const void* latent, int64_t latent_row_stride, int64_t latent_batch_stride,
+                      const void* rope, int64_t rope_row_stride, int64_t rope_batch_stride,
+                      int dtype, const int32_t* kv_start, const int32_t* kv_len, int32_t batch,
+                      int32_t s_q, int32_t heads, int32_t rank, int32_t rope_dim, int64_t t_max,
+                      const int32_t* selected_positions, const int32_t* selected_counts,
+                      int32_t k_max, float softmax_scale, void* ctx_out, int64_t ctx_row_stride,
+                      int64_t ctx_head_stride, int out_dtype, float* lse_out, void* workspace,
+                      size_t workspace_bytes, int32_t* device_status, mla_stream_t stream);
+
+/* Workspace bytes mla_decode_attend needs for these sizes on the current
+ * device (0 on an invalid request).  `selected` is non-zero when a selection
+ * will be passed. */
+size_t mla_decode_workspace_size(int32_t batch, int32_t s_q, int32_t heads, int32_t rank,
+                                 int32_t rope_dim, int64_t t_max, int32_t k_max, int selected,
+                                 int dtype);
+
+/* 1 if mla_decode_attend runs the tensor-core kernel for these sizes, 0 if the
+ * CUDA-core kernel, -1 if the request is invalid. */
+int mla_decode_kernel_kind(int32_t heads, int32_t rank, int32_t rope_dim, int dtype, int out_dtype);
+
+/*
+ * Value projection (MLA page, attendAbsorbed: "the latent context multiplies
+ * Wv^T", heads concatenated along the feature axis).
+ *
+ * out[n*out_row_stride + h*v_dim + j] = ctx[n, h, 0:rank] . W_UV_h[j, 0:rank],
+ * W_UV_h = rows [h*(nope+v_dim)+nope, (h+1)*(nope+v_dim)) of kv_b_proj.
+ * ctx[n, h, c] sits at ctx + n*ctx_row_stride + h*ctx_head_stride + c.  The
+ * output stops before o_proj.  fp32 accumulation.  ctx and kv_b_proj have
+ * `dtype`; out has out_dtype.  bf16 inputs with rank = 512, v_dim = 128,
+ * n_q <= 256 and 16-byte aligned pointers/strides run on the tensor cores.
+ */
+int mla_project_v(const void* ctx, int64_t ctx_row_stride, int64_t ctx_head_stride,
+                  const void* kv_b_proj, int dtype, void* out, int64_t out_row_stride,
+                  int out_dtype, int32_t n_q, int32_t heads, int32_t nope, int32_t v_dim,
+                  int32_t rank, mla_stream_t stream);
+
+/*
+ * Test hook: the selected-position gather of attendAbsorbed (takeAxis on
+ * latent and rope), bit-exact.  out[n, j, 0:rank+rope_dim] = latent || rope of
+ * window key selected_positions[n*k_max + j] of query row n, for j < count;
+ * the remaining slots, and slots whose position is outside the token's
+ * visible window (flagged like mla_decode_attend), are zero.  A count of -1
+ * gathers the visible window keys 0, 1, ... (at most k_max).
+ */
+int mla_gather_selected(const void* latent, int64_t latent_row_stride,
+                        int64_t latent_batch_stride, const void* rope, int64_t rope_row_stride,
+                        int64_t rope_batch_stride, int dtype, const int32_t* kv_start,
+                        const int32_t* kv_len, int32_t batch, int32_t s_q, int32_t rank,
+                        int32_t rope_dim, int64_t t_max, const int32_t* selected_positions,
+                        const int32_t* selected_counts, int32_t k_max, void* out,
+                        int32_t* device_status, mla_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

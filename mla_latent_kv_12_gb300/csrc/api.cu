@@ -1,0 +1,317 @@
+// Host side of the C ABI: argument validation, kernel selection, launches.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "mla_internal.h"
+
+namespace mla {
+
+namespace {
+thread_local char g_detail[512] = "";
+
+bool valid_dtype(int d) { return d == MLA_DTYPE_F32 || d == MLA_DTYPE_BF16; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int fail(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_detail, sizeof(g_detail), fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+int cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return MLA_OK;
+  return fail(MLA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define MLA_CHECK(cond, ...) \
+  do {                       \
+    if (!(cond)) return fail(MLA_ERR_INVALID_ARGUMENT, __VA_ARGS__); \
+  } while (0)
+
+}  // namespace
+
+void set_error_detail(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_detail, sizeof(g_detail), fmt, ap);
+  va_end(ap);
+}
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 148;
+  }
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+// Tensor-core path availability for the decode step.
+static bool tc_decode_shape(int32_t heads, int32_t rank, int32_t rope_dim, int dtype) {
+  return dtype == MLA_DTYPE_BF16 && heads == 128 && rank == 512 && rope_dim == 64;
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+const char* mla_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported";
+    case MLA_ERR_CUDA: return "CUDA error";
+    case MLA_ERR_INDEX_OUT_OF_RANGE: return "index out of range";
+    case MLA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+const char* mla_last_error_detail(void) { return g_detail; }
+
+int mla_version(void) { return (1 << 16) | 0; }
+
+int mla_rope_partial_interleaved(const void* in, void* out, int dtype, int64_t rows, int64_t tokens,
+                                 int64_t inner, int64_t width, const int64_t* in_strides,
+                                 const int64_t* out_strides, int32_t rotary_dims, float theta,
+                                 const int32_t* row_offsets, int64_t position_offset,
+                                 mla_stream_t stream) {
+  g_detail[0] = 0;
+  MLA_CHECK(in && out && in_strides && out_strides, "rope: NULL pointer");
+  MLA_CHECK(valid_dtype(dtype), "rope: bad dtype %d", dtype);
+  MLA_CHECK(rows > 0 && tokens > 0 && inner > 0 && width > 0, "rope: sizes must be positive");
+  MLA_CHECK(rotary_dims > 0 && (rotary_dims & 1) == 0 && rotary_dims <= width &&
+                rotary_dims <= kMaxRotaryDims,
+            "rope: rotary_dims %d must be positive, even, <= width %lld and <= %d", rotary_dims,
+            (long long)width, kMaxRotaryDims);
+  MLA_CHECK(width - rotary_dims <= 256, "rope: the kept tail may hold at most 256 features");
+  MLA_CHECK(isfinite(theta) && theta > 0.f, "rope: theta must be positive and finite");
+  MLA_CHECK(row_offsets || position_offset >= 0, "rope: position offset must be non-negative");
+  for (int k = 0; k < 3; ++k)
+    MLA_CHECK(in_strides[k] >= 0 && out_strides[k] >= 0, "rope: strides must be non-negative");
+  RopeParams p;
+  memset(&p, 0, sizeof(p));
+  p.in = in;
+  p.out = out;
+  p.rows = rows;
+  p.tokens = tokens;
+  p.inner = inner;
+  p.width = width;
+  for (int k = 0; k < 3; ++k) {
+    p.in_stride[k] = in_strides[k];
+    p.out_stride[k] = out_strides[k];
+  }
+  p.rotary_dims = rotary_dims;
+  p.row_offsets = row_offsets;
+  p.position_offset = position_offset;
+  // The page's f32 roundings: exponent f32(f32(-2j)/d), invf f32(pow(f32 theta, exponent)).
+  const double theta32 = (double)(float)theta;
+  for (int j = 0; j < rotary_dims / 2; ++j) {
+    const float exponent = (float)((double)(float)(-2.0 * j) / (double)rotary_dims);
+    p.inv_freq[j] = (float)pow(theta32, (double)exponent);
+  }
+  return cuda_status(launch_rope(p, dtype, (cudaStream_t)stream), "rope launch");
+}
+
+int mla_absorb_q(const void* q_nope, int64_t q_nope_row_stride, int64_t q_nope_head_stride,
+                 const void* kv_b_proj, void* q_out, int64_t q_out_row_stride,
+                 int64_t q_out_head_stride, int dtype, int32_t n_q, int32_t heads, int32_t nope,
+                 int32_t v_dim, int32_t rank, mla_stream_t stream) {
+  g_detail[0] = 0;
+  MLA_CHECK(q_nope && kv_b_proj && q_out, "absorb: NULL pointer");
+  MLA_CHECK(valid_dtype(dtype), "absorb: bad dtype %d", dtype);
+  MLA_CHECK(n_q > 0 && heads > 0 && nope > 0 && v_dim > 0 && rank > 0, "absorb: sizes must be positive");
+  MLA_CHECK(nope <= 256, "absorb: nope %d > 256", nope);
+  MLA_CHECK(q_nope_head_stride >= nope && q_nope_row_stride >= 0 && q_out_head_stride >= rank &&
+                q_out_row_stride >= 0,
+            "absorb: strides too small for the head widths");
+  AbsorbParams p{q_nope, q_nope_row_stride, q_nope_head_stride, kv_b_proj, q_out,
+                 q_out_row_stride, q_out_head_stride, n_q, heads, nope, v_dim, rank};
+  const bool tc = dtype == MLA_DTYPE_BF16 && nope == 128 && rank % 128 == 0 && rank <= 4096 &&
+                  n_q <= 256 && aligned16(q_nope) && aligned16(kv_b_proj) &&
+                  q_nope_head_stride % 8 == 0 && q_nope_row_stride % 8 == 0;
+  if (tc) return cuda_status(launch_tc_absorb(p, (cudaStream_t)stream), "absorb (tensor core) launch");
+  return cuda_status(launch_simt_absorb(p, dtype, (cudaStream_t)stream), "absorb launch");
+}
+
+int mla_decode_kernel_kind(int32_t heads, int32_t rank, int32_t rope_dim, int dtype, int out_dtype) {
+  if (heads <= 0 || rank <= 0 || rope_dim < 0 || !valid_dtype(dtype) || !valid_dtype(out_dtype)) return -1;
+  return tc_decode_shape(heads, rank, rope_dim, dtype) ? 1 : 0;
+}
+
+static int decode_geometry(DecodeGeometry& g, const void* q, int64_t q_row_stride,
+                           int64_t q_head_stride, const void* latent, int64_t latent_row_stride,
+                           int64_t latent_batch_stride, const void* rope, int64_t rope_row_stride,
+                           int64_t rope_batch_stride, int dtype, const int32_t* kv_start,
+                           const int32_t* kv_len, int32_t batch, int32_t s_q, int32_t heads,
+                           int32_t rank, int32_t rope_dim, int64_t t_max,
+                           const int32_t* selected_positions, const int32_t* selected_counts,
+                           int32_t k_max, float softmax_scale, void* ctx_out,
+                           int64_t ctx_row_stride, int64_t ctx_head_stride, float* lse_out,
+                           int32_t* device_status, bool need_q) {
+  MLA_CHECK(valid_dtype(dtype), "decode: bad dtype %d", dtype);
+  MLA_CHECK(batch > 0 && s_q > 0 && heads > 0 && rank > 0 && rope_dim >= 0 && t_max > 0,
+            "decode: sizes must be positive");
+  MLA_CHECK((int64_t)batch * s_q <= (1 << 24), "decode: too many query rows");
+  MLA_CHECK(t_max < (1LL << 31), "decode: t_max must fit int32");
+  MLA_CHECK(rank <= 1024 && rope_dim <= 256, "decode: rank <= 1024 and rope <= 256 are served");
+  MLA_CHECK(latent && kv_len && (rope || rope_dim == 0), "decode: NULL cache pointer");
+  MLA_CHECK(!need_q || (q && ctx_out), "decode: NULL q or ctx_out");
+  MLA_CHECK(latent_row_stride >= rank && latent_batch_stride >= 0 &&
+                (rope_dim == 0 || rope_row_stride >= rope_dim) && rope_batch_stride >= 0,
+            "decode: cache strides too small");
+  if (need_q)
+    MLA_CHECK(q_head_stride >= rank + rope_dim && q_row_stride >= 0 && ctx_head_stride >= rank &&
+                  ctx_row_stride >= 0,
+              "decode: q / ctx strides too small");
+  MLA_CHECK(!need_q || (isfinite(softmax_scale) && softmax_scale > 0.f),
+            "decode: softmax_scale must be positive");
+  if (selected_positions) {
+    MLA_CHECK(selected_counts && k_max > 0, "decode: a selection needs counts and k_max > 0");
+  }
+  memset(&g, 0, sizeof(g));
+  g.q = q;
+  g.q_row_stride = q_row_stride;
+  g.q_head_stride = q_head_stride;
+  g.latent = latent;
+  g.latent_row_stride = latent_row_stride;
+  g.latent_batch_stride = latent_batch_stride;
+  g.rope = rope;
+  g.rope_row_stride = rope_row_stride;
+  g.rope_batch_stride = rope_batch_stride;
+  g.kv_start = kv_start;
+  g.kv_len = kv_len;
+  g.batch = batch;
+  g.s_q = s_q;
+  g.heads = heads;
+  g.rank = rank;
+  g.rope_dim = rope_dim;
+  g.t_max = t_max;
+  g.sel = selected_positions;
+  g.sel_count = selected_positions ? selected_counts : nullptr;
+  g.k_max = selected_positions ? k_max : 0;
+  g.scale_log2 = softmax_scale * 1.4426950408889634f;
+  g.ctx_out = ctx_out;
+  g.ctx_row_stride = ctx_row_stride;
+  g.ctx_head_stride = ctx_head_stride;
+  g.lse_out = lse_out;
+  g.device_status = device_status;
+  return MLA_OK;
+}
+
+size_t mla_decode_workspace_size(int32_t batch, int32_t s_q, int32_t heads, int32_t rank,
+                                 int32_t rope_dim, int64_t t_max, int32_t k_max, int selected,
+                                 int dtype) {
+  if (batch <= 0 || s_q <= 0 || heads <= 0 || rank <= 0 || rope_dim < 0 || t_max <= 0 ||
+      !valid_dtype(dtype) || (selected && k_max <= 0))
+    return 0;
+  DecodeGeometry g;
+  memset(&g, 0, sizeof(g));
+  g.batch = batch;
+  g.s_q = s_q;
+  g.heads = heads;
+  g.rank = rank;
+  g.rope_dim = rope_dim;
+  g.t_max = t_max;
+  g.k_max = selected ? k_max : 0;
+  g.sel = selected ? reinterpret_cast<const int32_t*>(16) : nullptr;
+  size_t need = tc_decode_shape(heads, rank, rope_dim, dtype)
+                    ? tc_decode_workspace(batch * s_q, heads, rank)
+                    : simt_decode_workspace(g, nullptr);
+  return (need + 255) & ~(size_t)255;
+}
+
+int mla_decode_attend(const void* q, int64_t q_row_stride, int64_t q_head_stride,
+                      const void* latent, int64_t latent_row_stride, int64_t latent_batch_stride,
+                      const void* rope, int64_t rope_row_stride, int64_t rope_batch_stride,
+                      int dtype, const int32_t* kv_start, const int32_t* kv_len, int32_t batch,
+                      int32_t s_q, int32_t heads, int32_t rank, int32_t rope_dim, int64_t t_max,
+                      const int32_t* selected_positions, const int32_t* selected_counts,
+                      int32_t k_max, float softmax_scale, void* ctx_out, int64_t ctx_row_stride,
+                      int64_t ctx_head_stride, int out_dtype, float* lse_out, void* workspace,
+                      size_t workspace_bytes, int32_t* device_status, mla_stream_t stream) {
+  g_detail[0] = 0;
+  DecodeGeometry g;
+  int st = decode_geometry(g, q, q_row_stride, q_head_stride, latent, latent_row_stride,
+                           latent_batch_stride, rope, rope_row_stride, rope_batch_stride, dtype,
+                           kv_start, kv_len, batch, s_q, heads, rank, rope_dim, t_max,
+                           selected_positions, selected_counts, k_max, softmax_scale, ctx_out,
+                           ctx_row_stride, ctx_head_stride, lse_out, device_status, true);
+  if (st != MLA_OK) return st;
+  MLA_CHECK(valid_dtype(out_dtype), "decode: bad out_dtype %d", out_dtype);
+  const size_t need = mla_decode_workspace_size(batch, s_q, heads, rank, rope_dim, t_max, k_max,
+                                                selected_positions != nullptr, dtype);
+  MLA_CHECK(workspace_bytes >= need && (need == 0 || workspace),
+            "decode: workspace of %zu bytes < %zu needed", workspace_bytes, need);
+  MLA_CHECK((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0,
+            "decode: workspace must be 256-byte aligned");
+  if (tc_decode_shape(heads, rank, rope_dim, dtype)) {
+    // The tensor-core kernel moves 16-byte vectors and TMA boxes: every base
+    // pointer 16-byte aligned, every stride a multiple of 16 bytes.
+    const int64_t ovec = out_dtype == MLA_DTYPE_F32 ? 4 : 8;
+    MLA_CHECK(aligned16(q) && aligned16(latent) && aligned16(rope) && aligned16(ctx_out),
+              "decode: q, latent, rope and ctx_out must be 16-byte aligned");
+    MLA_CHECK(q_row_stride % 8 == 0 && q_head_stride % 8 == 0 && latent_row_stride % 8 == 0 &&
+                  latent_batch_stride % 8 == 0 && rope_row_stride % 8 == 0 &&
+                  rope_batch_stride % 8 == 0 && ctx_row_stride % ovec == 0 && ctx_head_stride % ovec == 0,
+              "decode: strides must be multiples of 16 bytes");
+    MLA_CHECK((int64_t)batch * s_q <= (1 << 20), "decode: at most 2^20 query rows");
+    return cuda_status(launch_tc_decode(g, out_dtype, workspace, workspace_bytes, (cudaStream_t)stream),
+                       "decode (tensor core) launch");
+  }
+  return cuda_status(launch_simt_decode(g, dtype, out_dtype, workspace, workspace_bytes,
+                                        (cudaStream_t)stream),
+                     "decode launch");
+}
+
+int mla_project_v(const void* ctx, int64_t ctx_row_stride, int64_t ctx_head_stride,
+                  const void* kv_b_proj, int dtype, void* out, int64_t out_row_stride,
+                  int out_dtype, int32_t n_q, int32_t heads, int32_t nope, int32_t v_dim,
+                  int32_t rank, mla_stream_t stream) {
+  g_detail[0] = 0;
+  MLA_CHECK(ctx && kv_b_proj && out, "project_v: NULL pointer");
+  MLA_CHECK(valid_dtype(dtype) && valid_dtype(out_dtype), "project_v: bad dtype");
+  MLA_CHECK(n_q > 0 && heads > 0 && nope > 0 && v_dim > 0 && rank > 0, "project_v: sizes must be positive");
+  MLA_CHECK(rank <= 1024, "project_v: rank %d > 1024", rank);
+  MLA_CHECK(ctx_head_stride >= rank && ctx_row_stride >= 0 && out_row_stride >= (int64_t)heads * v_dim,
+            "project_v: strides too small");
+  ProjectParams p{ctx, ctx_row_stride, ctx_head_stride, kv_b_proj, out, out_row_stride,
+                  n_q, heads, nope, v_dim, rank};
+  const bool tc = dtype == MLA_DTYPE_BF16 && rank == 512 && v_dim == 128 && n_q <= 64 &&
+                  aligned16(ctx) && aligned16(kv_b_proj) && ctx_head_stride % 8 == 0 &&
+                  ctx_row_stride % 8 == 0;
+  if (tc) return cuda_status(launch_tc_project(p, out_dtype, (cudaStream_t)stream), "project_v (tensor core) launch");
+  return cuda_status(launch_simt_project(p, dtype, out_dtype, (cudaStream_t)stream), "project_v launch");
+}
+
+int mla_gather_selected(const void* latent, int64_t latent_row_stride, int64_t latent_batch_stride,
+                        const void* rope, int64_t rope_row_stride, int64_t rope_batch_stride,
+                        int dtype, const int32_t* kv_start, const int32_t* kv_len, int32_t batch,
+                        int32_t s_q, int32_t rank, int32_t rope_dim, int64_t t_max,
+                        const int32_t* selected_positions, const int32_t* selected_counts,
+                        int32_t k_max, void* out, int32_t* device_status, mla_stream_t stream) {
+  g_detail[0] = 0;
+  MLA_CHECK(out && selected_counts && k_max > 0, "gather: NULL output, counts, or k_max <= 0");
+  DecodeGeometry g;
+  int st = decode_geometry(g, nullptr, 0, 0, latent, latent_row_stride, latent_batch_stride, rope,
+                           rope_row_stride, rope_batch_stride, dtype, kv_start, kv_len, batch, s_q,
+                           1, rank, rope_dim, t_max, selected_positions, selected_counts, k_max, 1.f,
+                           nullptr, 0, 0, nullptr, device_status, false);
+  if (st != MLA_OK) return st;
+  g.sel_count = selected_counts;
+  g.k_max = k_max;
+  return cuda_status(launch_gather(g, dtype, out, (cudaStream_t)stream), "gather launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,89 @@
+// Internal declarations shared by the host API and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+// Per-thread detail of the last error (set by the host API).
+void set_error_detail(const char* fmt, ...);
+
+constexpr int kMaxRotaryDims = 256;
+
+struct RopeParams {
+  const void* in;
+  void* out;
+  int64_t rows, tokens, inner, width;
+  int64_t in_stride[3];
+  int64_t out_stride[3];
+  int32_t rotary_dims;
+  const int32_t* row_offsets;
+  int64_t position_offset;
+  float inv_freq[kMaxRotaryDims / 2];
+};
+cudaError_t launch_rope(const RopeParams& p, int dtype, cudaStream_t stream);
+
+// Geometry of a decode call (all strides in elements).
+struct DecodeGeometry {
+  const void* q;
+  int64_t q_row_stride, q_head_stride;
+  const void* latent;
+  int64_t latent_row_stride, latent_batch_stride;
+  const void* rope;
+  int64_t rope_row_stride, rope_batch_stride;
+  const int32_t* kv_start;
+  const int32_t* kv_len;
+  int32_t batch, s_q, heads, rank, rope_dim;
+  int64_t t_max;
+  const int32_t* sel;
+  const int32_t* sel_count;
+  int32_t k_max;
+  float scale_log2;  // softmax_scale * log2(e)
+  void* ctx_out;
+  int64_t ctx_row_stride, ctx_head_stride;
+  float* lse_out;
+  int32_t* device_status;
+};
+
+// CUDA-core decode (any shape, f32 or bf16 inputs).
+size_t simt_decode_workspace(const DecodeGeometry& g, int* splits_out);
+cudaError_t launch_simt_decode(const DecodeGeometry& g, int dtype, int out_dtype, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream);
+
+// Tensor-core decode (bf16, heads 128, rank 512, rope 64).
+size_t tc_decode_workspace(int32_t n_q, int32_t heads, int32_t rank);
+cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+
+struct AbsorbParams {
+  const void* q_nope;
+  int64_t q_row_stride, q_head_stride;
+  const void* w;
+  void* out;
+  int64_t out_row_stride, out_head_stride;
+  int32_t n_q, heads, nope, v_dim, rank;
+};
+cudaError_t launch_simt_absorb(const AbsorbParams& p, int dtype, cudaStream_t stream);
+cudaError_t launch_tc_absorb(const AbsorbParams& p, cudaStream_t stream);
+
+struct ProjectParams {
+  const void* ctx;
+  int64_t ctx_row_stride, ctx_head_stride;
+  const void* w;
+  void* out;
+  int64_t out_row_stride;
+  int32_t n_q, heads, nope, v_dim, rank;
+};
+cudaError_t launch_simt_project(const ProjectParams& p, int dtype, int out_dtype,
+                                cudaStream_t stream);
+cudaError_t launch_tc_project(const ProjectParams& p, int out_dtype, cudaStream_t stream);
+
+cudaError_t launch_gather(const DecodeGeometry& g, int dtype, void* out, cudaStream_t stream);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace mla

@@ -1,0 +1,750 @@
+// Tensor-core flash-decode over the latent||rope cache ("glm52-mla.ts",
+// Glm52Mla.attendAbsorbed: s = q_lat.latent + q_rope.rope, scaled, softmax,
+// ctx = p @ latent; with the per-row windows / selections of Glm52Mla.forward
+// and the causal verify window of Glm52DecoderLayer.attend).
+//
+// Design (bf16, H = 128 heads, rank 512, rope 64):
+//  * All 128 heads of one query row form the M = 128 side of every tcgen05 MMA;
+//    keys come in tiles of 64 (the N side of the score MMA, the K side of P.V).
+//  * A cluster of two CTAs (an SM pair) owns one stream of work.  The f32
+//    context accumulator [128 x 512] would fill a whole SM's TMEM, so the pair
+//    splits the feature axis: CTA 0 reads latent dims [0,256), CTA 1 reads
+//    latent dims [256,512) plus the 64 rope dims.  Each computes a partial
+//    score S_r = Q[:, dims_r] . C[:, dims_r]^T, the pair swaps partials through
+//    distributed shared memory and both form S = S_0 + S_1 (commutative, so
+//    bit-identical), run the same online softmax, and each accumulates
+//    O[:, own 256 latent dims] += P . latent[:, own dims].  Every cache byte is
+//    read from HBM once and no MMA work is repeated.
+//  * Q (the CTA's dims) and P live in TMEM as the MMA A operand; cache tiles
+//    are TMA-loaded (128-byte swizzle) into a 4-stage ring; one tile serves the
+//    score MMA (K-major B) and the P.V MMA (MN-major B) through two descriptors.
+//  * Warp roles: warp 0 loads (TMA, or cp.async row gathers for selected
+//    positions), warp 1 issues MMAs, warps 2..5 (one thread per head) run the
+//    exchange, online softmax (log2 domain, lazy rescale), and the epilogue.
+//  * Split-K: a planner kernel counts each query row's tiles; the flattened
+//    tile sequence is cut into equal ranges, one per cluster.  A row wholly
+//    inside one range is finished in place; otherwise each piece writes an
+//    f32 partial (O, m, l) and a combine kernel merges them.
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "mla_internal.h"
+#include "tc_common.cuh"
+#include "tc_host.h"
+
+namespace mla {
+namespace {
+
+using namespace tc;
+
+constexpr int BN = 64;                    // keys per tile
+constexpr int STAGES = 4;
+constexpr int NCH_MAX = 5;                // 64-dim chunks per CTA (CTA 0: 4, CTA 1: 5)
+constexpr int CHUNK_BYTES = BN * 128;     // one [64 keys x 64 dims] bf16 box
+constexpr int STAGE_BYTES = NCH_MAX * CHUNK_BYTES;
+constexpr int X_BYTES = 128 * BN * 4;     // exchanged f32 partial scores
+constexpr int HEADS = 128, RANK = 512, ROPE = 64, DV = 256;  // DV: latent dims per CTA
+constexpr int THREADS = 192;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + X_BYTES;
+constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 416, TM_P = 480;  // TMEM columns
+constexpr long long kWaitLimit = 1LL << 32;  // clock cycles (~2 s)
+constexpr float kRescaleThreshold = 8.0f;    // log2 units
+
+struct TcDecodeArgs {
+  const __nv_bfloat16* q;
+  int64_t q_row_stride, q_head_stride;
+  const __nv_bfloat16* latent;
+  int64_t latent_row_stride, latent_batch_stride;
+  const __nv_bfloat16* rope;
+  int64_t rope_row_stride, rope_batch_stride;
+  const int32_t* kv_start;
+  const int32_t* kv_len;
+  int32_t s_q, n_q;
+  const int32_t* sel;
+  const int32_t* sel_count;
+  int32_t k_max;
+  float scale_log2;
+  void* ctx;
+  int64_t ctx_row_stride, ctx_head_stride;
+  int32_t out_f32;
+  float* lse;
+  int32_t* status;
+  int32_t* prefix;     // [n_q + 1] tile prefix (planner)
+  int32_t* keys;       // [n_q] visible entries per row (planner)
+  float* ws_o;         // [slots][H][512] partial O
+  float* ws_ml;        // [slots][H][2] partial (m, l), log2 domain
+  int32_t num_clusters;
+  int32_t batch_in_map;  // 1: use batch coordinate b in the tensor maps
+};
+
+// ------------------------------------------------------------------ helpers
+
+__device__ __forceinline__ int row_limit(const TcDecodeArgs& a, int n) {
+  const int b = n / a.s_q, i = n % a.s_q;
+  const int len = a.kv_len[b];
+  int lim = len - a.s_q + i + 1;
+  lim = lim < 0 ? 0 : (lim > len ? len : lim);
+  return lim;
+}
+
+// Iterates this cluster's range of the flattened tile sequence row by row.
+struct WorkIter {
+  const int32_t* prefix;
+  int n_q, n, t, t_begin, t_end;
+  __device__ void init(const int32_t* p, int nq, int cluster, int nclusters) {
+    prefix = p;
+    n_q = nq;
+    const int total = p[nq];
+    const int per = (total + nclusters - 1) / nclusters;
+    t_begin = min(total, cluster * per);
+    t_end = min(total, t_begin + per);
+    // first row with prefix[n+1] > t_begin
+    int lo = 0, hi = nq - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (p[mid + 1] > t_begin) hi = mid; else lo = mid + 1;
+    }
+    n = lo;
+    t = t_begin;
+  }
+  // Next segment: row n, row-local tiles [t0, t1); `whole` if the row lies
+  // entirely inside this cluster's range.
+  __device__ bool next(int& row, int& t0, int& t1, bool& whole) {
+    if (t >= t_end) return false;
+    while (prefix[n + 1] <= t) ++n;
+    const int rs = prefix[n], re = prefix[n + 1];
+    const int e = min(t_end, re);
+    row = n;
+    t0 = t - rs;
+    t1 = e - rs;
+    whole = rs >= t_begin && re <= t_end;
+    t = e;
+    return true;
+  }
+};
+
+// ------------------------------------------------------------------ planner
+// One block: per query row the number of visible entries and tiles, and the
+// exclusive prefix of tiles.  Bad selection counts are flagged and give 0.
+__global__ void __launch_bounds__(1024) tc_plan_kernel(const __grid_constant__ TcDecodeArgs a) {
+  __shared__ int warp_sums[32];
+  __shared__ int carry_s;
+  if (threadIdx.x == 0) carry_s = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int base = 0; base < a.n_q; base += 1024) {
+    const int n = base + threadIdx.x;
+    int keys = 0;
+    if (n < a.n_q) {
+      keys = row_limit(a, n);
+      if (a.sel) {
+        const int c = a.sel_count[n];
+        if (c != -1) {
+          if (c <= 0 || c > a.k_max) {
+            keys = 0;
+            if (a.status) atomicOr(a.status, MLA_DEVICE_BAD_SELECTION_COUNT);
+          } else {
+            keys = c;
+          }
+        }
+      }
+      a.keys[n] = keys;
+    }
+    const int tiles = (keys + BN - 1) / BN;
+    int v = tiles;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += u;
+    }
+    if (lane == 31) warp_sums[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_sums[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += u;
+      }
+      warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const int excl = carry_s + (warp ? warp_sums[warp - 1] : 0) + v - tiles;
+    if (n < a.n_q) a.prefix[n] = excl;
+    __syncthreads();
+    if (threadIdx.x == 1023) carry_s = excl + tiles;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) a.prefix[a.n_q] = carry_s;
+}
+
+// ------------------------------------------------------------------ decode
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    tc_decode_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__ CUtensorMap rope_map,
+                     const __grid_constant__ TcDecodeArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  float* xbuf = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES);  // [16][128][4] written by the peer
+
+  __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t s_full, s_free, p_full, pv_done, q_full, o_free, x_full, x_free, mma_drain;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ volatile int abort_s;
+  auto aborted = [&]() -> bool { return __any_sync(0xffffffffu, abort_s != 0); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t peer = rank ^ 1u;
+  const int nch = 4 + (int)rank;            // 64-dim chunks this CTA scores
+  const int dim_base = 256 * (int)rank;     // first latent dim of this CTA
+  const int cluster = blockIdx.x >> 1;
+  const bool gather = a.sel != nullptr;
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&lat_map);
+    tma_prefetch_desc(&rope_map);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], gather ? 32 : 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(&s_full, 1);
+    mbar_init(&s_free, 128);
+    mbar_init(&p_full, 128);
+    mbar_init(&pv_done, 1);
+    mbar_init(&q_full, 128);
+    mbar_init(&o_free, 128);
+    mbar_init(&x_full, 128);
+    mbar_init(&x_free, 128);
+    mbar_init(&mma_drain, 1);
+    abort_s = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_s, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // peer barriers initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+
+  WorkIter it;
+  it.init(a.prefix, a.n_q, cluster, a.num_clusters);
+
+  auto fail = [&]() {
+    abort_s = 1;
+    if (a.status) atomicOr(a.status, MLA_DEVICE_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    // ============================================================ producer
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued_phase[STAGES];
+    bool issued[STAGES];
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) issued[s] = false, issued_phase[s] = 0;
+    int n, t0, t1;
+    bool whole;
+    while (!aborted() && it.next(n, t0, t1, whole)) {
+      const int b = n / a.s_q;
+      const int start = a.kv_start ? a.kv_start[b] : 0;
+      const int limit = row_limit(a, n);
+      const int keys = a.keys[n];
+      const int zb = a.batch_in_map ? b : 0;
+      const int32_t* list = (gather && a.sel_count[n] != -1) ? a.sel + (int64_t)n * a.k_max : nullptr;
+      for (int t = t0; t < t1 && !aborted(); ++t) {
+        if (!mbar_wait_warp(&empty_bar[stage], phase ^ 1u, kWaitLimit)) { fail(); break; }
+        if (!gather) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&full_bar[stage], nch * CHUNK_BYTES);
+            uint8_t* dst = stages + stage * STAGE_BYTES;
+            const int y = start + t * BN;
+            for (int c = 0; c < 4; ++c)
+              tma_load_3d(dst + c * CHUNK_BYTES, &lat_map, &full_bar[stage], dim_base + 64 * c, y, zb);
+            if (rank == 1) tma_load_3d(dst + 4 * CHUNK_BYTES, &rope_map, &full_bar[stage], 0, y, zb);
+          }
+        } else {
+          // Row gather: lane L owns keys L and L+32 of the tile.
+          const int e0 = t * BN + lane, e1 = e0 + 32;
+          int p0 = e0, p1 = e1;
+          bool v0 = e0 < keys, v1 = e1 < keys;
+          if (list) {
+            p0 = v0 ? list[e0] : 0;
+            p1 = v1 ? list[e1] : 0;
+            const bool b0 = v0 && (p0 < 0 || p0 >= limit), b1 = v1 && (p1 < 0 || p1 >= limit);
+            if ((b0 || b1) && a.status && rank == 0) atomicOr(a.status, MLA_DEVICE_INDEX_OUT_OF_RANGE);
+            v0 = v0 && !b0;
+            v1 = v1 && !b1;
+          }
+          const uint32_t dst0 = smem_u32(stages + stage * STAGE_BYTES);
+          const int64_t lat_b = (int64_t)b * a.latent_batch_stride, rope_b = (int64_t)b * a.rope_batch_stride;
+          for (int r = 0; r < BN; ++r) {
+            const int src_lane = r & 31;
+            const int pr = __shfl_sync(0xffffffffu, r < 32 ? p0 : p1, src_lane);
+            const bool vr = __shfl_sync(0xffffffffu, r < 32 ? v0 : v1, src_lane);
+            const int64_t row = (int64_t)start + (vr ? pr : 0);
+            const __nv_bfloat16* lrow = a.latent + lat_b + row * a.latent_row_stride + dim_base;
+            const __nv_bfloat16* rrow = a.rope + rope_b + row * a.rope_row_stride;
+            for (int u = lane; u < nch * 8; u += 32) {
+              const int c = u >> 3, uu = u & 7;
+              const __nv_bfloat16* src = (c < 4) ? lrow + c * 64 + uu * 8 : rrow + uu * 8;
+              const uint32_t dst = dst0 + c * CHUNK_BYTES + r * 128 + ((uu ^ (r & 7)) << 4);
+              cp_async_16(dst, src, vr ? 16u : 0u);
+            }
+          }
+          cp_async_arrive_noinc(&full_bar[stage]);
+        }
+        issued[stage] = true;
+        issued_phase[stage] = phase;
+        if (++stage == STAGES) stage = 0, phase ^= 1u;
+      }
+    }
+    // Drain: every issued fill must land before this CTA may exit.
+    for (int s = 0; s < STAGES; ++s)
+      if (issued[s]) mbar_wait(&full_bar[s], issued_phase[s], kWaitLimit);
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    const uint32_t idesc_s = idesc_bf16_f32(128, BN, 0, 0);
+    const uint32_t idesc_pv = idesc_bf16_f32(128, DV, 0, 1);
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t tile = 0;      // global tile counter (S / P / PV phases)
+    uint32_t seg = 0;       // segment counter (q_full / o_free phases)
+    int n, t0, t1;
+    bool whole;
+    bool pending = false;   // a tile whose P.V is not yet issued
+    int pend_stage = 0;
+    bool pend_first = false;
+    auto issue_pv = [&](int st, bool first, uint32_t j) -> bool {
+      if (!mbar_wait_warp(&p_full, j & 1u, kWaitLimit)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t base = smem_u32(stages + st * STAGE_BYTES);
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint64_t bd = smem_desc(base + k * 2048, CHUNK_BYTES, 1024, kSwizzle128B);
+          mma_ts(tmem + TM_O, tmem + TM_P + k * 8, bd, idesc_pv, (first && k == 0) ? 0u : 1u);
+        }
+        mma_commit(&empty_bar[st]);
+        mma_commit(&pv_done);
+      }
+      __syncwarp();
+      return true;
+    };
+    while (!aborted() && it.next(n, t0, t1, whole)) {
+      const int keys = a.keys[n];
+      if (!mbar_wait_warp(&q_full, seg & 1u, kWaitLimit)) { fail(); break; }
+      bool first_tile = true;
+      for (int t = t0; t < t1; ++t) {
+        if (!mbar_wait_warp(&full_bar[stage], phase, kWaitLimit)) { fail(); break; }
+        if (!gather && t == (keys - 1) / BN && (keys % BN) != 0) {
+          // Tail tile: clear the rows past the window so that P = 0 never meets
+          // a non-finite value left in the caller's buffer.
+          const int valid = keys % BN;
+          uint8_t* st = stages + stage * STAGE_BYTES;
+          for (int u = lane; u < (BN - valid) * 4 * 8; u += 32) {
+            const int c = u / ((BN - valid) * 8), rem = u % ((BN - valid) * 8);
+            const int r = valid + rem / 8, uu = rem % 8;
+            *reinterpret_cast<uint4*>(st + c * CHUNK_BYTES + r * 128 + uu * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (gather) fence_proxy_async_smem();
+        if (tile > 0 && !mbar_wait_warp(&s_free, (tile - 1) & 1u, kWaitLimit)) { fail(); break; }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t base = smem_u32(stages + stage * STAGE_BYTES);
+          for (int c = 0; c < nch; ++c) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t bd = smem_desc(base + c * CHUNK_BYTES + k * 32, 16, 1024, kSwizzle128B);
+              mma_ts(tmem + TM_S, tmem + TM_Q + c * 32 + k * 8, bd, idesc_s, (c | k) != 0);
+            }
+          }
+          mma_commit(&s_full);
+        }
+        __syncwarp();
+        if (pending) {
+          if (pend_first && seg > 0 && !mbar_wait_warp(&o_free, (seg - 1) & 1u, kWaitLimit)) { fail(); break; }
+          if (!issue_pv(pend_stage, pend_first, tile - 1)) { fail(); break; }
+        }
+        pending = true;
+        pend_stage = stage;
+        pend_first = first_tile;
+        first_tile = false;
+        ++tile;
+        if (++stage == STAGES) stage = 0, phase ^= 1u;
+      }
+      if (aborted()) break;
+      // the segment's last P.V
+      if (pending) {
+        if (pend_first && seg > 0 && !mbar_wait_warp(&o_free, (seg - 1) & 1u, kWaitLimit)) { fail(); break; }
+        if (!issue_pv(pend_stage, pend_first, tile - 1)) { fail(); break; }
+        pending = false;
+      }
+      ++seg;
+    }
+    // All MMAs of this CTA complete before TMEM is released.
+    if (lane == 0) mma_commit(&mma_drain);
+    __syncwarp();
+    mbar_wait_warp(&mma_drain, 0, kWaitLimit);
+  } else {
+    // ============================================================ softmax / exchange / epilogue
+    const int quarter = warp & 3;
+    const int h = 32 * quarter + lane;                    // head = TMEM lane
+    const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
+    const uint32_t x_full_peer = mapa(smem_u32(&x_full), peer);
+    const uint32_t x_free_peer = mapa(smem_u32(&x_free), peer);
+    const uint32_t xbuf_peer = mapa(smem_u32(xbuf), peer);
+    uint32_t tile = 0, seg = 0;
+    uint32_t pv_seen = 0;   // P.V completions waited for
+    int n, t0, t1;
+    bool whole;
+    while (!aborted() && it.next(n, t0, t1, whole)) {
+      const int keys = a.keys[n];
+      const int b = n / a.s_q;
+      const int limit = row_limit(a, n);
+      const int32_t* list = (gather && a.sel_count[n] != -1) ? a.sel + (int64_t)n * a.k_max : nullptr;
+      // ---- Q row of this head (this CTA's dims) into TMEM
+      {
+        const __nv_bfloat16* qrow = a.q + (int64_t)n * a.q_row_stride + (int64_t)h * a.q_head_stride;
+        for (int c = 0; c < nch; ++c) {
+          const uint4* src = reinterpret_cast<const uint4*>(qrow + (c < 4 ? dim_base + 64 * c : RANK));
+          uint32_t r[32];
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            const uint4 x = __ldg(src + v);
+            r[4 * v] = x.x, r[4 * v + 1] = x.y, r[4 * v + 2] = x.z, r[4 * v + 3] = x.w;
+          }
+          tmem_st32(tmem + TM_Q + c * 32 + lane_off, r);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&q_full);
+      }
+      float m_used = -CUDART_INF_F, l = 0.f;
+      bool first_tile = true;
+      for (int t = t0; t < t1; ++t) {
+        // ---- validity of this tile's 64 entries (lane L: entries L, L+32)
+        uint64_t valid;
+        {
+          const int e0 = t * BN + lane, e1 = e0 + 32;
+          bool v0 = e0 < keys, v1 = e1 < keys;
+          if (list) {
+            if (v0) { const int p = list[e0]; v0 = p >= 0 && p < limit; }
+            if (v1) { const int p = list[e1]; v1 = p >= 0 && p < limit; }
+          }
+          valid = (uint64_t)__ballot_sync(0xffffffffu, v0) | ((uint64_t)__ballot_sync(0xffffffffu, v1) << 32);
+        }
+        // ---- own partial scores
+        if (!mbar_wait_warp(&s_full, tile & 1u, kWaitLimit)) { fail(); break; }
+        tc_fence_after();
+        uint32_t sa[32], sb[32];
+        tmem_ld32(tmem + TM_S + lane_off, sa);
+        tmem_ld32(tmem + TM_S + 32 + lane_off, sb);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&s_free);
+        // ---- exchange with the peer CTA
+        if (tile > 0 && !mbar_wait_cluster_warp(&x_free, (tile - 1) & 1u, kWaitLimit)) { fail(); break; }
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const uint32_t* src = c < 8 ? &sa[4 * c] : &sb[4 * (c - 8)];
+          const uint32_t dst = xbuf_peer + (uint32_t)((c * 128 + h) * 16);
+          asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(src[0]), "r"(src[1]),
+                       "r"(src[2]), "r"(src[3])
+                       : "memory");
+        }
+        mbar_arrive_remote(x_full_peer);
+        if (!mbar_wait_cluster_warp(&x_full, tile & 1u, kWaitLimit)) { fail(); break; }
+        float s[BN];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float4 x = *reinterpret_cast<const float4*>(xbuf + (c * 128 + h) * 4);
+          const uint32_t* own = c < 8 ? &sa[4 * c] : &sb[4 * (c - 8)];
+          s[4 * c + 0] = __uint_as_float(own[0]) + x.x;
+          s[4 * c + 1] = __uint_as_float(own[1]) + x.y;
+          s[4 * c + 2] = __uint_as_float(own[2]) + x.z;
+          s[4 * c + 3] = __uint_as_float(own[3]) + x.w;
+        }
+        mbar_arrive_remote(x_free_peer);
+        // ---- online softmax (log2 domain) with lazy rescaling
+        float mx = -CUDART_INF_F;
+#pragma unroll
+        for (int k = 0; k < BN; ++k) {
+          s[k] = ((valid >> k) & 1ull) ? s[k] * a.scale_log2 : -CUDART_INF_F;
+          mx = fmaxf(mx, s[k]);
+        }
+        float alpha = 1.f;
+        bool rescale = false;
+        if (mx > m_used + kRescaleThreshold || m_used == -CUDART_INF_F) {
+          const float m_new = fmaxf(m_used, mx);
+          if (m_new != m_used) {
+            alpha = (m_used == -CUDART_INF_F) ? 0.f : exp2f(m_used - m_new);
+            rescale = !first_tile && m_used != -CUDART_INF_F;
+            m_used = m_new;
+          }
+        }
+        uint32_t pk[32];
+        float psum = 0.f;
+#pragma unroll
+        for (int k = 0; k < BN; k += 2) {
+          const float p0 = (s[k] == -CUDART_INF_F) ? 0.f : exp2f(s[k] - m_used);
+          const float p1 = (s[k + 1] == -CUDART_INF_F) ? 0.f : exp2f(s[k + 1] - m_used);
+          const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+          psum += __low2float(pb) + __high2float(pb);
+          pk[k >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
+        }
+        l = l * alpha + psum;
+        // ---- P into TMEM once the previous P.V has consumed it (and O is stable)
+        while (pv_seen < tile) {
+          if (!mbar_wait_warp(&pv_done, pv_seen & 1u, kWaitLimit)) { fail(); break; }
+          ++pv_seen;
+        }
+        if (aborted()) break;
+        tc_fence_after();
+        if (rescale) {
+          for (int c = 0; c < DV / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tmem + TM_O + c * 32 + lane_off, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+            tmem_st32(tmem + TM_O + c * 32 + lane_off, o);
+          }
+        }
+        tmem_st32(tmem + TM_P + lane_off, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&p_full);
+        first_tile = false;
+        ++tile;
+      }
+      if (aborted()) break;
+      // ---- epilogue: wait for the segment's last P.V
+      while (pv_seen < tile) {
+        if (!mbar_wait_warp(&pv_done, pv_seen & 1u, kWaitLimit)) { fail(); break; }
+        ++pv_seen;
+      }
+      if (aborted()) break;
+      tc_fence_after();
+      const int64_t slot = (int64_t)n + cluster;
+      if (whole) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const int64_t off = (int64_t)n * a.ctx_row_stride + (int64_t)h * a.ctx_head_stride + dim_base;
+        for (int c = 0; c < DV / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tmem + TM_O + c * 32 + lane_off, o);
+          tmem_wait_ld();
+          if (a.out_f32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.ctx) + off + c * 32);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                                   __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.ctx) + off + c * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * v]) * inv, __uint_as_float(o[8 * v + 1]) * inv),
+                                  pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv),
+                                  pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv),
+                                  pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv));
+          }
+        }
+        if (rank == 0 && a.lse)
+          a.lse[(int64_t)n * HEADS + h] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+      } else {
+        float4* dst = reinterpret_cast<float4*>(a.ws_o + (slot * HEADS + h) * RANK + dim_base);
+        for (int c = 0; c < DV / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tmem + TM_O + c * 32 + lane_off, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[c * 8 + v] = make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
+                                         __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
+        }
+        if (rank == 0) {
+          a.ws_ml[(slot * HEADS + h) * 2] = l > 0.f ? m_used : -CUDART_INF_F;
+          a.ws_ml[(slot * HEADS + h) * 2 + 1] = l;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&o_free);
+      ++seg;
+      (void)b;
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // the peer no longer writes into this CTA's shared memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------ combine
+// grid (n_q, H/4); 128 threads = 4 heads x 32 lanes x 16 dims.
+__global__ void __launch_bounds__(128) tc_combine_kernel(const __grid_constant__ TcDecodeArgs a) {
+  const int n = blockIdx.x;
+  const int h = blockIdx.y * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int total = a.prefix[a.n_q];
+  const int per = (total + a.num_clusters - 1) / a.num_clusters;
+  const int rs = a.prefix[n], re = a.prefix[n + 1];
+  const int64_t orow = (int64_t)n * a.ctx_row_stride + (int64_t)h * a.ctx_head_stride;
+  if (re == rs) {   // nothing visible: ctx = 0, lse = -inf
+    for (int d = lane; d < RANK; d += 32) {
+      if (a.out_f32) static_cast<float*>(a.ctx)[orow + d] = 0.f;
+      else static_cast<__nv_bfloat16*>(a.ctx)[orow + d] = __float2bfloat16_rn(0.f);
+    }
+    if (lane == 0 && a.lse) a.lse[(int64_t)n * HEADS + h] = -CUDART_INF_F;
+    return;
+  }
+  const int c0 = rs / per, c1 = (re - 1) / per;
+  if (c0 == c1) return;   // finished in place by its cluster
+  float M = -CUDART_INF_F;
+  for (int c = c0; c <= c1; ++c) M = fmaxf(M, a.ws_ml[(((int64_t)n + c) * HEADS + h) * 2]);
+  float L = 0.f;
+  float w[8];
+  for (int c = c0; c <= c1; ++c) {
+    const float mc = a.ws_ml[(((int64_t)n + c) * HEADS + h) * 2];
+    const float wc = (mc == -CUDART_INF_F) ? 0.f : exp2f(mc - M);
+    L += wc * a.ws_ml[(((int64_t)n + c) * HEADS + h) * 2 + 1];
+    if (c - c0 < 8) w[c - c0] = wc;
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  float acc[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+  for (int c = c0; c <= c1; ++c) {
+    float wc;
+    if (c - c0 < 8) {
+      wc = w[c - c0];
+    } else {
+      const float mc = a.ws_ml[(((int64_t)n + c) * HEADS + h) * 2];
+      wc = (mc == -CUDART_INF_F) ? 0.f : exp2f(mc - M);
+    }
+    if (wc == 0.f) continue;
+    const float4* src = reinterpret_cast<const float4*>(a.ws_o + (((int64_t)n + c) * HEADS + h) * RANK) + lane * 4;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const float4 x = src[v];
+      acc[4 * v] = fmaf(wc, x.x, acc[4 * v]);
+      acc[4 * v + 1] = fmaf(wc, x.y, acc[4 * v + 1]);
+      acc[4 * v + 2] = fmaf(wc, x.z, acc[4 * v + 2]);
+      acc[4 * v + 3] = fmaf(wc, x.w, acc[4 * v + 3]);
+    }
+  }
+  if (a.out_f32) {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.ctx) + orow) + lane * 4;
+#pragma unroll
+    for (int v = 0; v < 4; ++v)
+      dst[v] = make_float4(acc[4 * v] * inv, acc[4 * v + 1] * inv, acc[4 * v + 2] * inv, acc[4 * v + 3] * inv);
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.ctx) + orow) + lane * 2;
+#pragma unroll
+    for (int v = 0; v < 2; ++v)
+      dst[v] = make_uint4(pack_bf16x2(acc[8 * v] * inv, acc[8 * v + 1] * inv),
+                          pack_bf16x2(acc[8 * v + 2] * inv, acc[8 * v + 3] * inv),
+                          pack_bf16x2(acc[8 * v + 4] * inv, acc[8 * v + 5] * inv),
+                          pack_bf16x2(acc[8 * v + 6] * inv, acc[8 * v + 7] * inv));
+  }
+  if (lane == 0 && a.lse) a.lse[(int64_t)n * HEADS + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -CUDART_INF_F;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+int tc_decode_clusters() { return device_sm_count() / 2; }
+
+size_t tc_decode_workspace(int32_t n_q, int32_t heads, int32_t rank) {
+  const size_t slots = (size_t)n_q + tc_decode_clusters();
+  return align256((size_t)(n_q + 1) * 4) + align256((size_t)n_q * 4) +
+         align256(slots * heads * rank * 4) + align256(slots * heads * 2 * 4);
+}
+
+cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream) {
+  const int n_q = g.batch * g.s_q;
+  const int nclusters = tc_decode_clusters();
+  if (workspace_bytes < tc_decode_workspace(n_q, g.heads, g.rank)) return cudaErrorInvalidValue;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  TcDecodeArgs a;
+  a.q = static_cast<const __nv_bfloat16*>(g.q);
+  a.q_row_stride = g.q_row_stride;
+  a.q_head_stride = g.q_head_stride;
+  a.latent = static_cast<const __nv_bfloat16*>(g.latent);
+  a.latent_row_stride = g.latent_row_stride;
+  a.latent_batch_stride = g.latent_batch_stride;
+  a.rope = static_cast<const __nv_bfloat16*>(g.rope);
+  a.rope_row_stride = g.rope_row_stride;
+  a.rope_batch_stride = g.rope_batch_stride;
+  a.kv_start = g.kv_start;
+  a.kv_len = g.kv_len;
+  a.s_q = g.s_q;
+  a.n_q = n_q;
+  a.sel = g.sel;
+  a.sel_count = g.sel_count;
+  a.k_max = g.k_max;
+  a.scale_log2 = g.scale_log2;
+  a.ctx = g.ctx_out;
+  a.ctx_row_stride = g.ctx_row_stride;
+  a.ctx_head_stride = g.ctx_head_stride;
+  a.out_f32 = out_dtype == MLA_DTYPE_F32;
+  a.lse = g.lse_out;
+  a.status = g.device_status;
+  size_t off = 0;
+  a.prefix = reinterpret_cast<int32_t*>(ws + off);
+  off += align256((size_t)(n_q + 1) * 4);
+  a.keys = reinterpret_cast<int32_t*>(ws + off);
+  off += align256((size_t)n_q * 4);
+  const size_t slots = (size_t)n_q + nclusters;
+  a.ws_o = reinterpret_cast<float*>(ws + off);
+  off += align256(slots * g.heads * g.rank * 4);
+  a.ws_ml = reinterpret_cast<float*>(ws + off);
+  a.num_clusters = nclusters;
+  a.batch_in_map = (g.latent_batch_stride != 0 || g.rope_batch_stride != 0) ? 1 : 0;
+
+  // Tensor maps over [B_buf, t_max, dims] (the batch axis has extent 1 for a
+  // packed-flat cache whose batch stride is 0).
+  const uint64_t bmap = a.batch_in_map ? (uint64_t)g.batch : 1;
+  CUtensorMap lat_map, rope_map;
+  {
+    const uint64_t dims[3] = {(uint64_t)g.rank, (uint64_t)g.t_max, bmap};
+    const uint64_t bstride = a.batch_in_map ? (uint64_t)g.latent_batch_stride * 2
+                                            : (uint64_t)g.t_max * g.latent_row_stride * 2;
+    const uint64_t strides[2] = {(uint64_t)g.latent_row_stride * 2, bstride};
+    const uint32_t box[3] = {64, BN, 1};
+    if (!encode_tmap_bf16(&lat_map, g.latent, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)g.rope_dim, (uint64_t)g.t_max, bmap};
+    const uint64_t bstride = a.batch_in_map ? (uint64_t)g.rope_batch_stride * 2
+                                            : (uint64_t)g.t_max * g.rope_row_stride * 2;
+    const uint64_t strides[2] = {(uint64_t)g.rope_row_stride * 2, bstride};
+    const uint32_t box[3] = {64, BN, 1};
+    if (!encode_tmap_bf16(&rope_map, g.rope, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(tc_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    attr = true;
+  }
+  tc_plan_kernel<<<1, 1024, 0, stream>>>(a);
+  tc_decode_kernel<<<2 * nclusters, THREADS, SMEM_BYTES, stream>>>(lat_map, rope_map, a);
+  tc_combine_kernel<<<dim3(n_q, g.heads / 4), 128, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -206,26 +206,33 @@ def attend_reconstructed(q_nope, q_rope, latent, rope, kv_b_proj, kv_start, kv_l
     hs = list(range(H)) if head_subset is None else list(head_subset)
     out = np.full((n_q, len(hs), v), np.nan)
     lse = np.full((n_q, len(hs)), np.nan)
-    rows = range(n_q) if rows is None else rows
-    for n in rows:
-        b, i = divmod(n, s_q)
+    rows = list(range(n_q)) if rows is None else list(rows)
+    w_all = np.asarray(kv_b_proj, dtype=F64)
+    # Query rows of one batch row share its cache; K/V of a row's window are
+    # reconstructed once per head and each token takes the keys it sees.
+    for b in sorted({n // s_q for n in rows}):
         bb = b if batch_buffer_rows is None else int(batch_buffer_rows[b])
-        keys = visible_rows(b, i, s_q, kv_start, kv_len, sel, sel_count)
-        if keys.size == 0:
-            out[n] = 0.0
-            lse[n] = -np.inf
-            continue
-        lat = np.asarray(latent[bb][keys], dtype=F64)            # [N, rank]
-        rp = np.asarray(rope[bb][keys], dtype=F64)               # [N, rope]
+        toks = [n for n in rows if n // s_q == b]
+        keys_of = {n: visible_rows(b, n % s_q, s_q, kv_start, kv_len, sel, sel_count) for n in toks}
+        union = np.unique(np.concatenate([keys_of[n] for n in toks] + [np.zeros(0, np.int64)]))
+        where = {int(k): j for j, k in enumerate(union)}
+        lat = np.asarray(latent[bb][union], dtype=F64)            # [U, rank]
+        rp = np.asarray(rope[bb][union], dtype=F64)               # [U, rope]
         for j, h in enumerate(hs):
-            w_uk, w_uv = head_weights(np.asarray(kv_b_proj), h, nope, v)
+            w_uk, w_uv = head_weights(w_all, h, nope, v)
             k_nope, values = reconstruct_kv(lat, np.concatenate([w_uk, w_uv]), 1, nope, v)
-            key = np.concatenate([k_nope[:, 0, :], rp], axis=-1)            # [N, nope+rope]
-            query = np.concatenate([q_nope[n, h], q_rope[n, h]])            # [nope+rope]
-            scores = (key @ query) * scale
-            p, l = _softmax_rows(scores[None, :])
-            out[n, j] = p[0] @ values[:, 0, :]
-            lse[n, j] = l[0]
+            key = np.concatenate([k_nope[:, 0, :], rp], axis=-1)            # [U, nope+rope]
+            for n in toks:
+                idx = np.array([where[int(k)] for k in keys_of[n]], dtype=np.int64)
+                if idx.size == 0:
+                    out[n, j] = 0.0
+                    lse[n, j] = -np.inf
+                    continue
+                query = np.concatenate([q_nope[n, h], q_rope[n, h]])        # [nope+rope]
+                scores = (key[idx] @ query) * scale
+                p, l = _softmax_rows(scores[None, :])
+                out[n, j] = p[0] @ values[idx, 0, :]
+                lse[n, j] = l[0]
     return out, lse
 
 
@@ -311,7 +318,8 @@ def attend_absorbed(q_nope, q_rope, latent, rope, kv_b_proj, kv_start, kv_len,
 def gather_selected(latent, rope, kv_start, kv_len, s_q: int, sel, sel_count, k_max: int,
                     batch_buffer_rows=None):
     """Selected cache rows ``latent || rope`` copied to ``[n_q, k_max, rank+rope]``
-    (``takeAxis`` of attendAbsorbed), in the storage dtype; unused slots are 0."""
+    (``takeAxis`` of attendAbsorbed), in the storage dtype; unused slots are 0.
+    A dense row (count -1) lists its visible window keys in order, at most ``k_max``."""
     latent = np.asarray(latent)
     rope = np.asarray(rope)
     n_q = len(sel_count)
@@ -319,7 +327,7 @@ def gather_selected(latent, rope, kv_start, kv_len, s_q: int, sel, sel_count, k_
     for n in range(n_q):
         b, i = divmod(n, s_q)
         bb = b if batch_buffer_rows is None else int(batch_buffer_rows[b])
-        keys = visible_rows(b, i, s_q, kv_start, kv_len, sel, sel_count)
+        keys = visible_rows(b, i, s_q, kv_start, kv_len, sel, sel_count)[:k_max]
         out[n, :keys.size, :latent.shape[-1]] = latent[bb][keys]
         out[n, :keys.size, latent.shape[-1]:] = rope[bb][keys]
     return out
