@@ -267,6 +267,8 @@ int mla_decode_attend(const void* q, int64_t q_row_stride, int64_t q_head_stride
                   rope_batch_stride % 8 == 0 && ctx_row_stride % ovec == 0 && ctx_head_stride % ovec == 0,
               "decode: strides must be multiples of 16 bytes");
     MLA_CHECK((int64_t)batch * s_q <= (1 << 20), "decode: at most 2^20 query rows");
+    MLA_CHECK((latent_batch_stride == 0) == (rope_batch_stride == 0),
+              "decode: latent and rope batch strides must both be zero (packed rows) or both non-zero");
     return cuda_status(launch_tc_decode(g, out_dtype, workspace, workspace_bytes, (cudaStream_t)stream),
                        "decode (tensor core) launch");
   }

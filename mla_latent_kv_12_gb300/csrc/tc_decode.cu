@@ -49,6 +49,9 @@ constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + X_BYTES;
 constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 416, TM_P = 480;  // TMEM columns
 constexpr long long kWaitLimit = 1LL << 32;  // clock cycles (~2 s)
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
+// A group's tile range is at least this long: each split writes a 256 KB f32
+// partial, worth it only against a few 72 KB tiles of cache read.
+constexpr int kMinTilesPerGroup = 4;
 
 struct TcDecodeArgs {
   const __nv_bfloat16* q;
@@ -69,11 +72,14 @@ struct TcDecodeArgs {
   int32_t out_f32;
   float* lse;
   int32_t* status;
-  int32_t* prefix;     // [n_q + 1] tile prefix (planner)
-  int32_t* keys;       // [n_q] visible entries per row (planner)
+  int32_t* prefix;     // [n_units + 1] tile prefix over work units (planner)
+  int32_t* keys;       // [n_q] visible entries per query row (planner)
   float* ws_o;         // [slots][H][512] partial O
   float* ws_ml;        // [slots][H][2] partial (m, l), log2 domain
   int32_t num_clusters;
+  int32_t width;       // query rows per work unit = clusters per group
+  int32_t n_units;     // n_q / width
+  int32_t min_tiles;   // smallest tile range given to a group
   int32_t batch_in_map;  // 1: use batch coordinate b in the tensor maps
 };
 
@@ -87,34 +93,46 @@ __device__ __forceinline__ int row_limit(const TcDecodeArgs& a, int n) {
   return lim;
 }
 
-// Iterates this cluster's range of the flattened tile sequence row by row.
+// Work units are query rows, or -- for a dense multi-token verify -- whole
+// batch rows whose `width` = s_q tokens are served by a group of `width`
+// clusters in lockstep (member i takes token i), so the tokens of a batch row
+// read each cache tile at the same time and three of four reads hit L2.
+// The units' tiles form one flattened sequence cut into equal ranges, one per
+// group (at least `min_tiles` each, so a short sequence uses fewer groups).
+__device__ __forceinline__ int group_span(const TcDecodeArgs& a, int total) {
+  const int ngroups = a.num_clusters / a.width;
+  const int per = (total + ngroups - 1) / ngroups;
+  return per > a.min_tiles ? per : a.min_tiles;
+}
+
 struct WorkIter {
   const int32_t* prefix;
-  int n_q, n, t, t_begin, t_end;
-  __device__ void init(const int32_t* p, int nq, int cluster, int nclusters) {
-    prefix = p;
-    n_q = nq;
-    const int total = p[nq];
-    const int per = (total + nclusters - 1) / nclusters;
-    t_begin = min(total, cluster * per);
-    t_end = min(total, t_begin + per);
-    // first row with prefix[n+1] > t_begin
-    int lo = 0, hi = nq - 1;
+  int n, t, t_begin, t_end;
+  __device__ void init(const TcDecodeArgs& a, int group) {
+    prefix = a.prefix;
+    const int total = a.prefix[a.n_units];
+    const int per = group_span(a, total);
+    const int ngroups = a.num_clusters / a.width;
+    const long long b0 = group < ngroups ? (long long)group * per : total;
+    t_begin = (int)min((long long)total, b0);
+    t_end = (int)min((long long)total, (long long)t_begin + per);
+    // first unit with prefix[n+1] > t_begin
+    int lo = 0, hi = a.n_units - 1;
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
-      if (p[mid + 1] > t_begin) hi = mid; else lo = mid + 1;
+      if (prefix[mid + 1] > t_begin) hi = mid; else lo = mid + 1;
     }
     n = lo;
     t = t_begin;
   }
-  // Next segment: row n, row-local tiles [t0, t1); `whole` if the row lies
-  // entirely inside this cluster's range.
-  __device__ bool next(int& row, int& t0, int& t1, bool& whole) {
+  // Next segment: unit u, unit-local tiles [t0, t1); `whole` if the unit lies
+  // entirely inside this group's range.
+  __device__ bool next(int& u, int& t0, int& t1, bool& whole) {
     if (t >= t_end) return false;
     while (prefix[n + 1] <= t) ++n;
     const int rs = prefix[n], re = prefix[n + 1];
     const int e = min(t_end, re);
-    row = n;
+    u = n;
     t0 = t - rs;
     t1 = e - rs;
     whole = rs >= t_begin && re <= t_end;
@@ -123,39 +141,59 @@ struct WorkIter {
   }
 };
 
+// A member's share of a unit segment: its query row n and the segment's tiles
+// clipped to that row's own tiles (a verify token sees a shorter prefix than
+// the last token).  False if nothing is left.
+__device__ __forceinline__ bool member_segment(const TcDecodeArgs& a, int u, int member, int& n, int& t0,
+                                               int& t1) {
+  n = u * a.width + member;
+  const int tiles = (a.keys[n] + BN - 1) / BN;
+  if (t1 > tiles) t1 = tiles;
+  return t0 < t1;
+}
+
 // ------------------------------------------------------------------ planner
 // One block: per query row the number of visible entries and tiles, and the
 // exclusive prefix of tiles.  Bad selection counts are flagged and give 0.
+__device__ __forceinline__ int row_keys(const TcDecodeArgs& a, int n) {
+  int keys = row_limit(a, n);
+  if (a.sel) {
+    const int c = a.sel_count[n];
+    if (c != -1) {
+      if (c <= 0 || c > a.k_max) {
+        keys = 0;
+        if (a.status) atomicOr(a.status, MLA_DEVICE_BAD_SELECTION_COUNT);
+      } else {
+        keys = c;
+      }
+    }
+  }
+  return keys;
+}
+
 __global__ void __launch_bounds__(1024) tc_plan_kernel(const __grid_constant__ TcDecodeArgs a) {
   __shared__ int warp_sums[32];
   __shared__ int carry_s;
   if (threadIdx.x == 0) carry_s = 0;
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int base = 0; base < a.n_q; base += 1024) {
-    const int n = base + threadIdx.x;
-    int keys = 0;
-    if (n < a.n_q) {
-      keys = row_limit(a, n);
-      if (a.sel) {
-        const int c = a.sel_count[n];
-        if (c != -1) {
-          if (c <= 0 || c > a.k_max) {
-            keys = 0;
-            if (a.status) atomicOr(a.status, MLA_DEVICE_BAD_SELECTION_COUNT);
-          } else {
-            keys = c;
-          }
-        }
+  for (int base = 0; base < a.n_units; base += 1024) {
+    const int u = base + threadIdx.x;
+    int tiles = 0;
+    if (u < a.n_units) {
+      for (int i = 0; i < a.width; ++i) {
+        const int n = u * a.width + i;
+        const int keys = row_keys(a, n);
+        a.keys[n] = keys;
+        const int t = (keys + BN - 1) / BN;
+        tiles = t > tiles ? t : tiles;
       }
-      a.keys[n] = keys;
     }
-    const int tiles = (keys + BN - 1) / BN;
     int v = tiles;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += u;
+      const int x = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += x;
     }
     if (lane == 31) warp_sums[warp] = v;
     __syncthreads();
@@ -163,19 +201,19 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const __grid_constant__ T
       int w = warp_sums[lane];
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, w, o);
-        if (lane >= o) w += u;
+        const int x = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += x;
       }
       warp_sums[lane] = w;
     }
     __syncthreads();
     const int excl = carry_s + (warp ? warp_sums[warp - 1] : 0) + v - tiles;
-    if (n < a.n_q) a.prefix[n] = excl;
+    if (u < a.n_units) a.prefix[u] = excl;
     __syncthreads();
     if (threadIdx.x == 1023) carry_s = excl + tiles;
     __syncthreads();
   }
-  if (threadIdx.x == 0) a.prefix[a.n_q] = carry_s;
+  if (threadIdx.x == 0) a.prefix[a.n_units] = carry_s;
 }
 
 // ------------------------------------------------------------------ decode
@@ -200,6 +238,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const int nch = 4 + (int)rank;            // 64-dim chunks this CTA scores
   const int dim_base = 256 * (int)rank;     // first latent dim of this CTA
   const int cluster = blockIdx.x >> 1;
+  const int group = cluster / a.width, member = cluster % a.width;
   const bool gather = a.sel != nullptr;
 
   if (threadIdx.x == 0) {
@@ -232,7 +271,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const uint32_t tmem = tmem_base_s;
 
   WorkIter it;
-  it.init(a.prefix, a.n_q, cluster, a.num_clusters);
+  it.init(a, group);
 
   auto fail = [&]() {
     abort_s = 1;
@@ -247,9 +286,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     bool issued[STAGES];
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) issued[s] = false, issued_phase[s] = 0;
-    int n, t0, t1;
+    int u, n, t0, t1;
     bool whole;
-    while (!aborted() && it.next(n, t0, t1, whole)) {
+    while (!aborted() && it.next(u, t0, t1, whole)) {
+      if (!member_segment(a, u, member, n, t0, t1)) continue;
       const int b = n / a.s_q;
       const int start = a.kv_start ? a.kv_start[b] : 0;
       const int limit = row_limit(a, n);
@@ -289,8 +329,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const int64_t row = (int64_t)start + (vr ? pr : 0);
             const __nv_bfloat16* lrow = a.latent + lat_b + row * a.latent_row_stride + dim_base;
             const __nv_bfloat16* rrow = a.rope + rope_b + row * a.rope_row_stride;
-            for (int u = lane; u < nch * 8; u += 32) {
-              const int c = u >> 3, uu = u & 7;
+            for (int q16 = lane; q16 < nch * 8; q16 += 32) {
+              const int c = q16 >> 3, uu = q16 & 7;
               const __nv_bfloat16* src = (c < 4) ? lrow + c * 64 + uu * 8 : rrow + uu * 8;
               const uint32_t dst = dst0 + c * CHUNK_BYTES + r * 128 + ((uu ^ (r & 7)) << 4);
               cp_async_16(dst, src, vr ? 16u : 0u);
@@ -314,7 +354,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     uint32_t phase = 0;
     uint32_t tile = 0;      // global tile counter (S / P / PV phases)
     uint32_t seg = 0;       // segment counter (q_full / o_free phases)
-    int n, t0, t1;
+    int u, n, t0, t1;
     bool whole;
     bool pending = false;   // a tile whose P.V is not yet issued
     int pend_stage = 0;
@@ -335,7 +375,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       __syncwarp();
       return true;
     };
-    while (!aborted() && it.next(n, t0, t1, whole)) {
+    while (!aborted() && it.next(u, t0, t1, whole)) {
+      if (!member_segment(a, u, member, n, t0, t1)) continue;
       const int keys = a.keys[n];
       if (!mbar_wait_warp(&q_full, seg & 1u, kWaitLimit)) { fail(); break; }
       bool first_tile = true;
@@ -346,8 +387,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           // a non-finite value left in the caller's buffer.
           const int valid = keys % BN;
           uint8_t* st = stages + stage * STAGE_BYTES;
-          for (int u = lane; u < (BN - valid) * 4 * 8; u += 32) {
-            const int c = u / ((BN - valid) * 8), rem = u % ((BN - valid) * 8);
+          for (int q16 = lane; q16 < (BN - valid) * 4 * 8; q16 += 32) {
+            const int c = q16 / ((BN - valid) * 8), rem = q16 % ((BN - valid) * 8);
             const int r = valid + rem / 8, uu = rem % 8;
             *reinterpret_cast<uint4*>(st + c * CHUNK_BYTES + r * 128 + uu * 16) = make_uint4(0, 0, 0, 0);
           }
@@ -403,11 +444,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const uint32_t xbuf_peer = mapa(smem_u32(xbuf), peer);
     uint32_t tile = 0, seg = 0;
     uint32_t pv_seen = 0;   // P.V completions waited for
-    int n, t0, t1;
+    int u, n, t0, t1;
     bool whole;
-    while (!aborted() && it.next(n, t0, t1, whole)) {
+    while (!aborted() && it.next(u, t0, t1, whole)) {
+      const bool any = member_segment(a, u, member, n, t0, t1);
+      const int64_t slot = ((int64_t)u + group) * a.width + member;
+      if (!any) {
+        // Nothing of this row in the group's range: an empty partial (weight 0).
+        if (!whole && rank == 0) {
+          a.ws_ml[(slot * HEADS + h) * 2] = -CUDART_INF_F;
+          a.ws_ml[(slot * HEADS + h) * 2 + 1] = 0.f;
+        }
+        continue;
+      }
       const int keys = a.keys[n];
-      const int b = n / a.s_q;
       const int limit = row_limit(a, n);
       const int32_t* list = (gather && a.sel_count[n] != -1) ? a.sel + (int64_t)n * a.k_max : nullptr;
       // ---- Q row of this head (this CTA's dims) into TMEM
@@ -533,7 +583,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
       if (aborted()) break;
       tc_fence_after();
-      const int64_t slot = (int64_t)n + cluster;
       if (whole) {
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const int64_t off = (int64_t)n * a.ctx_row_stride + (int64_t)h * a.ctx_head_stride + dim_base;
@@ -578,7 +627,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       tc_fence_before();
       mbar_arrive(&o_free);
       ++seg;
-      (void)b;
     }
   }
 
@@ -598,11 +646,11 @@ __global__ void __launch_bounds__(128) tc_combine_kernel(const __grid_constant__
   const int n = blockIdx.x;
   const int h = blockIdx.y * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  const int total = a.prefix[a.n_q];
-  const int per = (total + a.num_clusters - 1) / a.num_clusters;
-  const int rs = a.prefix[n], re = a.prefix[n + 1];
+  const int u = n / a.width, member = n % a.width;
+  const int per = group_span(a, a.prefix[a.n_units]);
+  const int rs = a.prefix[u], re = a.prefix[u + 1];
   const int64_t orow = (int64_t)n * a.ctx_row_stride + (int64_t)h * a.ctx_head_stride;
-  if (re == rs) {   // nothing visible: ctx = 0, lse = -inf
+  if (a.keys[n] == 0) {   // nothing visible: ctx = 0, lse = -inf
     for (int d = lane; d < RANK; d += 32) {
       if (a.out_f32) static_cast<float*>(a.ctx)[orow + d] = 0.f;
       else static_cast<__nv_bfloat16*>(a.ctx)[orow + d] = __float2bfloat16_rn(0.f);
@@ -611,15 +659,16 @@ __global__ void __launch_bounds__(128) tc_combine_kernel(const __grid_constant__
     return;
   }
   const int c0 = rs / per, c1 = (re - 1) / per;
-  if (c0 == c1) return;   // finished in place by its cluster
+  if (c0 == c1) return;   // finished in place by its group
+  auto slot_of = [&](int g) -> int64_t { return ((int64_t)u + g) * a.width + member; };
   float M = -CUDART_INF_F;
-  for (int c = c0; c <= c1; ++c) M = fmaxf(M, a.ws_ml[(((int64_t)n + c) * HEADS + h) * 2]);
+  for (int c = c0; c <= c1; ++c) M = fmaxf(M, a.ws_ml[(slot_of(c) * HEADS + h) * 2]);
   float L = 0.f;
   float w[8];
   for (int c = c0; c <= c1; ++c) {
-    const float mc = a.ws_ml[(((int64_t)n + c) * HEADS + h) * 2];
+    const float mc = a.ws_ml[(slot_of(c) * HEADS + h) * 2];
     const float wc = (mc == -CUDART_INF_F) ? 0.f : exp2f(mc - M);
-    L += wc * a.ws_ml[(((int64_t)n + c) * HEADS + h) * 2 + 1];
+    L += wc * a.ws_ml[(slot_of(c) * HEADS + h) * 2 + 1];
     if (c - c0 < 8) w[c - c0] = wc;
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
@@ -631,11 +680,11 @@ __global__ void __launch_bounds__(128) tc_combine_kernel(const __grid_constant__
     if (c - c0 < 8) {
       wc = w[c - c0];
     } else {
-      const float mc = a.ws_ml[(((int64_t)n + c) * HEADS + h) * 2];
+      const float mc = a.ws_ml[(slot_of(c) * HEADS + h) * 2];
       wc = (mc == -CUDART_INF_F) ? 0.f : exp2f(mc - M);
     }
     if (wc == 0.f) continue;
-    const float4* src = reinterpret_cast<const float4*>(a.ws_o + (((int64_t)n + c) * HEADS + h) * RANK) + lane * 4;
+    const float4* src = reinterpret_cast<const float4*>(a.ws_o + (slot_of(c) * HEADS + h) * RANK) + lane * 4;
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
       const float4 x = src[v];
@@ -714,6 +763,11 @@ cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* works
   off += align256(slots * g.heads * g.rank * 4);
   a.ws_ml = reinterpret_cast<float*>(ws + off);
   a.num_clusters = nclusters;
+  // A dense multi-token verify serves each batch row's tokens with a group of
+  // clusters in lockstep; everything else is one query row per unit.
+  a.width = (g.sel == nullptr && g.s_q > 1 && g.s_q <= 8) ? g.s_q : 1;
+  a.n_units = n_q / a.width;
+  a.min_tiles = kMinTilesPerGroup;
   a.batch_in_map = (g.latent_batch_stride != 0 || g.rope_batch_stride != 0) ? 1 : 0;
 
   // Tensor maps over [B_buf, t_max, dims] (the batch axis has extent 1 for a
