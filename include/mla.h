@@ -156,6 +156,44 @@ int mla_decode_attend(const void* q, int64_t q_row_stride, int64_t q_head_stride
                       int64_t ctx_head_stride, int out_dtype, float* lse_out, void* workspace,
                       size_t workspace_bytes, int32_t* device_status, mla_stream_t stream);
 
+/*
+ * Decode attention for callers that cannot allocate device memory.  The pages
+ * have no counterpart of this entry point; it exists for users of the library.
+ *
+ * Same arguments, results, checks and device-status bits as
+ * mla_decode_attend, without `workspace` / `workspace_bytes`: the split-K
+ * scratch is a fixed array of MLA_NO_ALLOC_SCRATCH_BYTES that the library
+ * reserves on every GPU that loads it, held until the process exits.  Meant
+ * for callers that cannot call cudaMalloc when they decode: a serving process
+ * whose memory pool has already claimed the free device memory, a plugin or
+ * foreign-language host that passes tensors in but has no allocator to hand,
+ * or a latency-bound loop in which an allocation (and the device-wide
+ * synchronisation it may cause) is not acceptable.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ * Set-up: the first call on a device looks up the array's device address with
+ * that device current; make that first call before any stream capture.
+ * Limit: a request whose mla_decode_workspace_size(...) exceeds
+ * MLA_NO_ALLOC_SCRATCH_BYTES returns MLA_ERR_UNSUPPORTED and launches nothing
+ * (at H = 128, rank 512 on a 152-SM GB300 this allows about 170 query rows).
+ * Sharing: every call on a device uses the same array, which keeps the last
+ * call's contents; nothing in it has to start at zero (each call writes what
+ * it later reads).  Calls whose work overlaps on the GPU -- unordered streams,
+ * or several host threads at once -- race on the array and give undefined
+ * results; order them on one stream.
+ */
+#define MLA_NO_ALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int mla_decode_attend_no_alloc(const void* q, int64_t q_row_stride, int64_t q_head_stride,
+                               const void* latent, int64_t latent_row_stride,
+                               int64_t latent_batch_stride, const void* rope,
+                               int64_t rope_row_stride, int64_t rope_batch_stride, int dtype,
+                               const int32_t* kv_start, const int32_t* kv_len, int32_t batch,
+                               int32_t s_q, int32_t heads, int32_t rank, int32_t rope_dim,
+                               int64_t t_max, const int32_t* selected_positions,
+                               const int32_t* selected_counts, int32_t k_max, float softmax_scale,
+                               void* ctx_out, int64_t ctx_row_stride, int64_t ctx_head_stride,
+                               int out_dtype, float* lse_out, int32_t* device_status,
+                               mla_stream_t stream);
+
 /* Workspace bytes mla_decode_attend needs for these sizes on the current
  * device (0 on an invalid request).  `selected` is non-zero when a selection
  * will be passed. */

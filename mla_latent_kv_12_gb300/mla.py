@@ -27,7 +27,7 @@ EXPORTS = (
     "mla_status_string", "mla_last_error_detail", "mla_version",
     "mla_rope_partial_interleaved", "mla_absorb_q", "mla_decode_attend",
     "mla_decode_workspace_size", "mla_decode_kernel_kind", "mla_project_v",
-    "mla_gather_selected",
+    "mla_gather_selected", "mla_decode_attend_no_alloc",
 )
 
 
@@ -66,6 +66,10 @@ def _load() -> ctypes.CDLL:
     lib.mla_project_v.restype = ctypes.c_int
     lib.mla_project_v.argtypes = [vp, i64, i64, vp, ctypes.c_int, vp, i64, ctypes.c_int, i32, i32, i32,
                                   i32, i32, vp]
+    lib.mla_decode_attend_no_alloc.restype = ctypes.c_int
+    lib.mla_decode_attend_no_alloc.argtypes = [vp, i64, i64, vp, i64, i64, vp, i64, i64, ctypes.c_int, vp,
+                                               vp, i32, i32, i32, i32, i32, i64, vp, vp, i32, f32, vp, i64,
+                                               i64, ctypes.c_int, vp, vp, vp]
     lib.mla_gather_selected.restype = ctypes.c_int
     lib.mla_gather_selected.argtypes = [vp, i64, i64, vp, i64, i64, ctypes.c_int, vp, vp, i32, i32, i32,
                                         i32, i64, vp, vp, i32, vp, vp, vp]
