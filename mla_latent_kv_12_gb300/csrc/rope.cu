@@ -8,6 +8,7 @@
 #include <cuda_bf16.h>
 
 #include "mla_internal.h"
+#include "tc_host.h"
 
 namespace mla {
 namespace {
@@ -35,6 +36,7 @@ constexpr int kMaxTailPerLane = 8;                          // tail <= 256
 
 template <typename T>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) rope_kernel(const __grid_constant__ RopeParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int64_t vec = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int64_t nvec = p.rows * p.tokens * p.inner;
@@ -94,11 +96,11 @@ cudaError_t launch_rope(const RopeParams& p, int dtype, cudaStream_t stream) {
   const int64_t nvec = p.rows * p.tokens * p.inner;
   const int64_t blocks = (nvec + kWarpsPerBlock - 1) / kWarpsPerBlock;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (dtype == MLA_DTYPE_F32)
-    rope_kernel<float><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(p);
-  else
-    rope_kernel<__nv_bfloat16><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  const cudaError_t e =
+      dtype == MLA_DTYPE_F32
+          ? launch_pdl(rope_kernel<float>, dim3((unsigned)blocks), dim3(kWarpsPerBlock * 32), 0, stream, p)
+          : launch_pdl(rope_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(kWarpsPerBlock * 32), 0, stream, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace mla

@@ -8,23 +8,25 @@
 //    keys come in tiles of 64 (the N side of the score MMA, the K side of P.V).
 //  * A cluster of two CTAs (an SM pair) owns one stream of work.  The f32
 //    context accumulator [128 x 512] would fill a whole SM's TMEM, so the pair
-//    splits the feature axis: CTA 0 reads latent dims [0,256), CTA 1 reads
-//    latent dims [256,512) plus the 64 rope dims.  Each computes a partial
-//    score S_r = Q[:, dims_r] . C[:, dims_r]^T, the pair swaps partials through
-//    distributed shared memory and both form S = S_0 + S_1 (commutative, so
-//    bit-identical), run the same online softmax, and each accumulates
-//    O[:, own 256 latent dims] += P . latent[:, own dims].  Every cache byte is
-//    read from HBM once and no MMA work is repeated.
+//    splits the feature axis evenly: CTA r scores latent dims [256r, 256r+256)
+//    and rope dims [32r, 32r+32) (18 MMA K-steps each).  The pair swaps its
+//    partial scores through distributed shared memory (st.async, counted as
+//    transactions on the receiving barrier) and both form S = S_0 + S_1
+//    (commutative, so bit-identical), run the same online softmax, and each
+//    accumulates O[:, own 256 latent dims] += P . latent[:, own dims].  No MMA
+//    work is repeated and every latent byte is read by one CTA (the 128-byte
+//    rope row is read by both, from L2 the second time).
 //  * Q (the CTA's dims) and P live in TMEM as the MMA A operand; cache tiles
 //    are TMA-loaded (128-byte swizzle) into a 4-stage ring; one tile serves the
 //    score MMA (K-major B) and the P.V MMA (MN-major B) through two descriptors.
-//  * Warp roles: warp 0 loads (TMA, or cp.async row gathers for selected
-//    positions), warp 1 issues MMAs, warps 2..5 (one thread per head) run the
-//    exchange, online softmax (log2 domain, lazy rescale), and the epilogue.
+//  * Warp roles: warp 0 loads (TMA tiles, or TMA gather4 / cp.async row
+//    gathers for selected positions), warp 1 issues MMAs, warps 2..5 (one
+//    thread per head) run the exchange, online softmax (log2 domain, lazy
+//    rescale), and the epilogue.
 //  * Split-K: a planner kernel counts each query row's tiles; the flattened
-//    tile sequence is cut into equal ranges, one per cluster.  A row wholly
-//    inside one range is finished in place; otherwise each piece writes an
-//    f32 partial (O, m, l) and a combine kernel merges them.
+//    tile sequence is cut into equal ranges, one per cluster group.  A row
+//    wholly inside one range is finished in place; otherwise each piece writes
+//    an f32 partial (O, m, l; heads contiguous) and a combine kernel merges them.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -39,14 +41,14 @@ using namespace tc;
 
 constexpr int BN = 64;                    // keys per tile
 constexpr int STAGES = 4;
-constexpr int NCH_MAX = 5;                // 64-dim chunks per CTA (CTA 0: 4, CTA 1: 5)
+constexpr int NCH = 5;                    // 64-dim chunks per stage: 4 latent + the rope row
 constexpr int CHUNK_BYTES = BN * 128;     // one [64 keys x 64 dims] bf16 box
-constexpr int STAGE_BYTES = NCH_MAX * CHUNK_BYTES;
+constexpr int STAGE_BYTES = NCH * CHUNK_BYTES;
 constexpr int X_BYTES = 128 * BN * 4;     // exchanged f32 partial scores
-constexpr int HEADS = 128, RANK = 512, ROPE = 64, DV = 256;  // DV: latent dims per CTA
+constexpr int HEADS = 128, RANK = 512, DV = 256;  // DV: latent dims per CTA
 constexpr int THREADS = 192;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + X_BYTES;
-constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 416, TM_P = 480;  // TMEM columns
+constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 400, TM_P = 464;  // TMEM columns (Q: 128 + 16)
 constexpr long long kWaitLimit = 1LL << 32;  // clock cycles (~2 s)
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
 // A group's tile range is at least this long: each split writes a 256 KB f32
@@ -74,13 +76,15 @@ struct TcDecodeArgs {
   int32_t* status;
   int32_t* prefix;     // [n_units + 1] tile prefix over work units (planner)
   int32_t* keys;       // [n_q] visible entries per query row (planner)
-  float* ws_o;         // [slots][H][512] partial O
-  float* ws_ml;        // [slots][H][2] partial (m, l), log2 domain
+  float* ws_o;         // [slots][512][H] partial O (heads contiguous)
+  float* ws_ml;        // [slots][2][H] partial (m, l), log2 domain
   int32_t num_clusters;
   int32_t width;       // query rows per work unit = clusters per group
   int32_t n_units;     // n_q / width
   int32_t min_tiles;   // smallest tile range given to a group
   int32_t batch_in_map;  // 1: use batch coordinate b in the tensor maps
+  int32_t gather_tma;    // 1: selected rows come by TMA gather4 (else cp.async)
+  int32_t lat_rows_per_batch, rope_rows_per_batch;  // batch stride in rows (gather maps)
 };
 
 // ------------------------------------------------------------------ helpers
@@ -172,6 +176,7 @@ __device__ __forceinline__ int row_keys(const TcDecodeArgs& a, int n) {
 }
 
 __global__ void __launch_bounds__(1024) tc_plan_kernel(const __grid_constant__ TcDecodeArgs a) {
+  pdl_wait();
   __shared__ int warp_sums[32];
   __shared__ int carry_s;
   if (threadIdx.x == 0) carry_s = 0;
@@ -214,12 +219,14 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const __grid_constant__ T
     __syncthreads();
   }
   if (threadIdx.x == 0) a.prefix[a.n_units] = carry_s;
+  pdl_trigger();
 }
 
 // ------------------------------------------------------------------ decode
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc_decode_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__ CUtensorMap rope_map,
+                     const __grid_constant__ CUtensorMap lat_rows_map, const __grid_constant__ CUtensorMap rope_rows_map,
                      const __grid_constant__ TcDecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -235,7 +242,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
-  const int nch = 4 + (int)rank;            // 64-dim chunks this CTA scores
+  const int nch = NCH;                      // chunks this CTA loads per tile
   const int dim_base = 256 * (int)rank;     // first latent dim of this CTA
   const int cluster = blockIdx.x >> 1;
   const int group = cluster / a.width, member = cluster % a.width;
@@ -244,8 +251,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&lat_map);
     tma_prefetch_desc(&rope_map);
+    if (gather && a.gather_tma) {
+      tma_prefetch_desc(&lat_rows_map);
+      tma_prefetch_desc(&rope_rows_map);
+    }
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full_bar[s], gather ? 32 : 1);
+      mbar_init(&full_bar[s], (gather && !a.gather_tma) ? 32 : 1);
       mbar_init(&empty_bar[s], 1);
     }
     mbar_init(&s_full, 1);
@@ -254,7 +265,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     mbar_init(&pv_done, 1);
     mbar_init(&q_full, 128);
     mbar_init(&o_free, 128);
-    mbar_init(&x_full, 128);
+    mbar_init(&x_full, 1);      // local expect_tx arrival + the peer's st.async bytes
     mbar_init(&x_free, 128);
     mbar_init(&mma_drain, 1);
     abort_s = 0;
@@ -269,6 +280,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   cluster_sync();   // peer barriers initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
+  pdl_wait();       // the planner's prefix and counts (and the query) are complete
 
   WorkIter it;
   it.init(a, group);
@@ -305,7 +317,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const int y = start + t * BN;
             for (int c = 0; c < 4; ++c)
               tma_load_3d(dst + c * CHUNK_BYTES, &lat_map, &full_bar[stage], dim_base + 64 * c, y, zb);
-            if (rank == 1) tma_load_3d(dst + 4 * CHUNK_BYTES, &rope_map, &full_bar[stage], 0, y, zb);
+            tma_load_3d(dst + 4 * CHUNK_BYTES, &rope_map, &full_bar[stage], 0, y, zb);
+          }
+        } else if (a.gather_tma) {
+          // Row gather by TMA: lane g < 16 owns keys 4g..4g+3 of the tile and
+          // issues one gather4 per 64-dim chunk.  Entries past the count or out
+          // of range load the window's first row (finite data; the softmax
+          // gives them p = 0).
+          int lr[4], rr[4];
+          if (lane < 16) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int e = t * BN + 4 * lane + j;
+              bool v = e < keys;
+              int p = e;
+              if (v && list) {
+                p = list[e];
+                if (p < 0 || p >= limit) {
+                  v = false;
+                  if (a.status && rank == 0) atomicOr(a.status, MLA_DEVICE_INDEX_OUT_OF_RANGE);
+                }
+              }
+              const int w = start + (v ? p : 0);
+              lr[j] = b * a.lat_rows_per_batch + w;
+              rr[j] = b * a.rope_rows_per_batch + w;
+            }
+          }
+          if (lane == 0) mbar_arrive_expect_tx(&full_bar[stage], nch * CHUNK_BYTES);
+          __syncwarp();
+          if (lane < 16) {
+            uint8_t* dst = stages + stage * STAGE_BYTES + lane * 4 * 128;
+            for (int c = 0; c < 4; ++c)
+              tma_gather4(dst + c * CHUNK_BYTES, &lat_rows_map, &full_bar[stage], dim_base + 64 * c, lr[0], lr[1],
+                          lr[2], lr[3]);
+            tma_gather4(dst + 4 * CHUNK_BYTES, &rope_rows_map, &full_bar[stage], 0, rr[0], rr[1], rr[2], rr[3]);
           }
         } else {
           // Row gather: lane L owns keys L and L+32 of the tile.
@@ -365,10 +410,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       if (lane == 0) {
         const uint32_t base = smem_u32(stages + st * STAGE_BYTES);
 #pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          const uint64_t bd = smem_desc(base + k * 2048, CHUNK_BYTES, 1024, kSwizzle128B);
-          mma_ts(tmem + TM_O, tmem + TM_P + k * 8, bd, idesc_pv, (first && k == 0) ? 0u : 1u);
-        }
+        const uint64_t d0 = smem_desc(base, CHUNK_BYTES, 1024, kSwizzle128B);
+        for (int k = 0; k < BN / 16; ++k)
+          mma_ts(tmem + TM_O, tmem + TM_P + k * 8, d0 + (uint64_t)((k * 2048) >> 4), idesc_pv,
+                 (first && k == 0) ? 0u : 1u);
         mma_commit(&empty_bar[st]);
         mma_commit(&pv_done);
       }
@@ -395,18 +440,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           fence_proxy_async_smem();
           __syncwarp();
         }
-        if (gather) fence_proxy_async_smem();
+        if (gather && !a.gather_tma) fence_proxy_async_smem();
         if (tile > 0 && !mbar_wait_warp(&s_free, (tile - 1) & 1u, kWaitLimit)) { fail(); break; }
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t base = smem_u32(stages + stage * STAGE_BYTES);
-          for (int c = 0; c < nch; ++c) {
+          // 16 latent K-steps, then this CTA's two rope K-steps.  Descriptors
+          // differ only in the start address (16-byte units, low bits).
+          const uint64_t d0 = smem_desc(smem_u32(stages + stage * STAGE_BYTES), 16, 1024, kSwizzle128B);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t bd = smem_desc(base + c * CHUNK_BYTES + k * 32, 16, 1024, kSwizzle128B);
-              mma_ts(tmem + TM_S, tmem + TM_Q + c * 32 + k * 8, bd, idesc_s, (c | k) != 0);
-            }
+          for (int c = 0; c < 4; ++c) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_ts(tmem + TM_S, tmem + TM_Q + c * 32 + k * 8, d0 + (uint64_t)((c * CHUNK_BYTES + k * 32) >> 4),
+                     idesc_s, (c | k) != 0);
           }
+#pragma unroll
+          for (int k = 0; k < 2; ++k)
+            mma_ts(tmem + TM_S, tmem + TM_Q + 128 + k * 8,
+                   d0 + (uint64_t)((4 * CHUNK_BYTES + (2 * (int)rank + k) * 32) >> 4), idesc_s, 1u);
           mma_commit(&s_full);
         }
         __syncwarp();
@@ -452,8 +503,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       if (!any) {
         // Nothing of this row in the group's range: an empty partial (weight 0).
         if (!whole && rank == 0) {
-          a.ws_ml[(slot * HEADS + h) * 2] = -CUDART_INF_F;
-          a.ws_ml[(slot * HEADS + h) * 2 + 1] = 0.f;
+          a.ws_ml[(slot * 2) * HEADS + h] = -CUDART_INF_F;
+          a.ws_ml[(slot * 2 + 1) * HEADS + h] = 0.f;
         }
         continue;
       }
@@ -462,16 +513,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const int32_t* list = (gather && a.sel_count[n] != -1) ? a.sel + (int64_t)n * a.k_max : nullptr;
       // ---- Q row of this head (this CTA's dims) into TMEM
       {
+        // Latent dims [dim_base, dim_base+256) as four 64-dim chunks, then the
+        // rope half [32*rank, 32*rank+32).  Two chunks in flight: chunk c+1's
+        // loads are issued before chunk c's TMEM store (a compiler barrier).
         const __nv_bfloat16* qrow = a.q + (int64_t)n * a.q_row_stride + (int64_t)h * a.q_head_stride;
-        for (int c = 0; c < nch; ++c) {
-          const uint4* src = reinterpret_cast<const uint4*>(qrow + (c < 4 ? dim_base + 64 * c : RANK));
+        const uint4* qlat = reinterpret_cast<const uint4*>(qrow + dim_base);
+        const uint4* qrope = reinterpret_cast<const uint4*>(qrow + RANK + 32 * (int)rank);
+        uint4 qa[8], qb[8];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) qa[v] = __ldg(qlat + v);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int v = 0; v < 8; ++v) qb[v] = (c < 3) ? __ldg(qlat + 8 * (c + 1) + v) : (v < 4 ? __ldg(qrope + v) : qa[v]);
           uint32_t r[32];
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            const uint4 x = __ldg(src + v);
-            r[4 * v] = x.x, r[4 * v + 1] = x.y, r[4 * v + 2] = x.z, r[4 * v + 3] = x.w;
-          }
+          for (int v = 0; v < 8; ++v) r[4 * v] = qa[v].x, r[4 * v + 1] = qa[v].y, r[4 * v + 2] = qa[v].z, r[4 * v + 3] = qa[v].w;
           tmem_st32(tmem + TM_Q + c * 32 + lane_off, r);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) qa[v] = qb[v];
+        }
+        {
+          uint32_t r[16];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) r[4 * v] = qa[v].x, r[4 * v + 1] = qa[v].y, r[4 * v + 2] = qa[v].z, r[4 * v + 3] = qa[v].w;
+          tmem_st16(tmem + TM_Q + 128 + lane_off, r);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -505,12 +571,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const uint32_t* src = c < 8 ? &sa[4 * c] : &sb[4 * (c - 8)];
-          const uint32_t dst = xbuf_peer + (uint32_t)((c * 128 + h) * 16);
-          asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(src[0]), "r"(src[1]),
-                       "r"(src[2]), "r"(src[3])
-                       : "memory");
+          st_async_v4(xbuf_peer + (uint32_t)((c * 128 + h) * 16), src[0], src[1], src[2], src[3], x_full_peer);
         }
-        mbar_arrive_remote(x_full_peer);
+        if (h == 0) mbar_arrive_expect_tx_u32(smem_u32(&x_full), X_BYTES);
         if (!mbar_wait_cluster_warp(&x_full, tile & 1u, kWaitLimit)) { fail(); break; }
         float s[BN];
 #pragma unroll
@@ -523,33 +586,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           s[4 * c + 3] = __uint_as_float(own[3]) + x.w;
         }
         mbar_arrive_remote(x_free_peer);
-        // ---- online softmax (log2 domain) with lazy rescaling
-        float mx = -CUDART_INF_F;
+        // ---- online softmax (log2 domain) with lazy rescaling; independent
+        // partial maxima / sums keep the dependency chains short.
+        float mx8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = -CUDART_INF_F;
 #pragma unroll
         for (int k = 0; k < BN; ++k) {
           s[k] = ((valid >> k) & 1ull) ? s[k] * a.scale_log2 : -CUDART_INF_F;
-          mx = fmaxf(mx, s[k]);
+          mx8[k & 7] = fmaxf(mx8[k & 7], s[k]);
         }
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         float alpha = 1.f;
         bool rescale = false;
         if (mx > m_used + kRescaleThreshold || m_used == -CUDART_INF_F) {
           const float m_new = fmaxf(m_used, mx);
           if (m_new != m_used) {
-            alpha = (m_used == -CUDART_INF_F) ? 0.f : exp2f(m_used - m_new);
+            alpha = (m_used == -CUDART_INF_F) ? 0.f : ex2_approx(m_used - m_new);
             rescale = !first_tile && m_used != -CUDART_INF_F;
             m_used = m_new;
           }
         }
+        // With m_used finite, ex2(-inf - m) = +0 masks an entry; a tile with no
+        // visible entry so far (m_used = -inf) contributes nothing.
+        const float m_sub = (m_used == -CUDART_INF_F) ? 0.f : m_used;
         uint32_t pk[32];
-        float psum = 0.f;
+        float ps8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ps8[k] = 0.f;
 #pragma unroll
         for (int k = 0; k < BN; k += 2) {
-          const float p0 = (s[k] == -CUDART_INF_F) ? 0.f : exp2f(s[k] - m_used);
-          const float p1 = (s[k + 1] == -CUDART_INF_F) ? 0.f : exp2f(s[k + 1] - m_used);
+          const float p0 = ex2_approx(s[k] - m_sub);
+          const float p1 = ex2_approx(s[k + 1] - m_sub);
           const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-          psum += __low2float(pb) + __high2float(pb);
+          ps8[(k >> 1) & 7] += __low2float(pb) + __high2float(pb);
           pk[k >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
         }
+        const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
         l = l * alpha + psum;
         // ---- P into TMEM once the previous P.V has consumed it (and O is stable)
         while (pv_seen < tile) {
@@ -609,19 +683,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (rank == 0 && a.lse)
           a.lse[(int64_t)n * HEADS + h] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
       } else {
-        float4* dst = reinterpret_cast<float4*>(a.ws_o + (slot * HEADS + h) * RANK + dim_base);
+        // Partial O stored dims-major, heads contiguous: a warp's 32 heads
+        // write one 128-byte line per dim.
+        float* dst = a.ws_o + (slot * RANK + dim_base) * HEADS + h;
         for (int c = 0; c < DV / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(tmem + TM_O + c * 32 + lane_off, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[c * 8 + v] = make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
-                                         __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
+          for (int k = 0; k < 32; ++k) dst[(c * 32 + k) * HEADS] = __uint_as_float(o[k]);
         }
         if (rank == 0) {
-          a.ws_ml[(slot * HEADS + h) * 2] = l > 0.f ? m_used : -CUDART_INF_F;
-          a.ws_ml[(slot * HEADS + h) * 2 + 1] = l;
+          a.ws_ml[(slot * 2) * HEADS + h] = l > 0.f ? m_used : -CUDART_INF_F;
+          a.ws_ml[(slot * 2 + 1) * HEADS + h] = l;
         }
       }
       tc_fence_before();
@@ -631,6 +705,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
 
   // ---------------------------------------------------------------- teardown
+  pdl_trigger();
   tc_fence_before();
   __syncthreads();
   cluster_sync();   // the peer no longer writes into this CTA's shared memory
@@ -641,74 +716,71 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }
 
 // ------------------------------------------------------------------ combine
-// grid (n_q, H/4); 128 threads = 4 heads x 32 lanes x 16 dims.
+// grid (n_q, RANK / CDIMS); 128 threads = heads; thread h merges dims
+// [d0, d0 + CDIMS) of head h over the row's pieces.  Partials are heads
+// contiguous, so every load instruction of a warp reads one 128-byte line.
+constexpr int CDIMS = 8;
+
 __global__ void __launch_bounds__(128) tc_combine_kernel(const __grid_constant__ TcDecodeArgs a) {
+  pdl_wait();
   const int n = blockIdx.x;
-  const int h = blockIdx.y * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
+  const int d0 = blockIdx.y * CDIMS;
+  const int h = threadIdx.x;
   const int u = n / a.width, member = n % a.width;
-  const int per = group_span(a, a.prefix[a.n_units]);
-  const int rs = a.prefix[u], re = a.prefix[u + 1];
-  const int64_t orow = (int64_t)n * a.ctx_row_stride + (int64_t)h * a.ctx_head_stride;
-  if (a.keys[n] == 0) {   // nothing visible: ctx = 0, lse = -inf
-    for (int d = lane; d < RANK; d += 32) {
-      if (a.out_f32) static_cast<float*>(a.ctx)[orow + d] = 0.f;
-      else static_cast<__nv_bfloat16*>(a.ctx)[orow + d] = __float2bfloat16_rn(0.f);
-    }
-    if (lane == 0 && a.lse) a.lse[(int64_t)n * HEADS + h] = -CUDART_INF_F;
-    return;
-  }
-  const int c0 = rs / per, c1 = (re - 1) / per;
-  if (c0 == c1) return;   // finished in place by its group
-  auto slot_of = [&](int g) -> int64_t { return ((int64_t)u + g) * a.width + member; };
-  float M = -CUDART_INF_F;
-  for (int c = c0; c <= c1; ++c) M = fmaxf(M, a.ws_ml[(slot_of(c) * HEADS + h) * 2]);
-  float L = 0.f;
-  float w[8];
-  for (int c = c0; c <= c1; ++c) {
-    const float mc = a.ws_ml[(slot_of(c) * HEADS + h) * 2];
-    const float wc = (mc == -CUDART_INF_F) ? 0.f : exp2f(mc - M);
-    L += wc * a.ws_ml[(slot_of(c) * HEADS + h) * 2 + 1];
-    if (c - c0 < 8) w[c - c0] = wc;
-  }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  float acc[16];
+  const int64_t orow = (int64_t)n * a.ctx_row_stride + (int64_t)h * a.ctx_head_stride + d0;
+  float acc[CDIMS];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-  for (int c = c0; c <= c1; ++c) {
-    float wc;
-    if (c - c0 < 8) {
-      wc = w[c - c0];
+  for (int j = 0; j < CDIMS; ++j) acc[j] = 0.f;
+  float M = -CUDART_INF_F, L = 0.f;
+  bool write = true;
+  if (a.keys[n] != 0) {
+    const int per = group_span(a, a.prefix[a.n_units]);
+    const int rs = a.prefix[u], re = a.prefix[u + 1];
+    const int c0 = rs / per, c1 = (re - 1) / per;
+    if (c0 == c1) {
+      write = false;                       // finished in place by its group
     } else {
-      const float mc = a.ws_ml[(slot_of(c) * HEADS + h) * 2];
-      wc = (mc == -CUDART_INF_F) ? 0.f : exp2f(mc - M);
-    }
-    if (wc == 0.f) continue;
-    const float4* src = reinterpret_cast<const float4*>(a.ws_o + (slot_of(c) * HEADS + h) * RANK) + lane * 4;
+      auto slot_of = [&](int g) -> int64_t { return ((int64_t)u + g) * a.width + member; };
+      for (int c = c0; c <= c1; ++c) M = fmaxf(M, a.ws_ml[(slot_of(c) * 2) * HEADS + h]);
+      for (int c = c0; c <= c1; c += 4) {
+        float wc[4], x[4][CDIMS];
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const float4 x = src[v];
-      acc[4 * v] = fmaf(wc, x.x, acc[4 * v]);
-      acc[4 * v + 1] = fmaf(wc, x.y, acc[4 * v + 1]);
-      acc[4 * v + 2] = fmaf(wc, x.z, acc[4 * v + 2]);
-      acc[4 * v + 3] = fmaf(wc, x.w, acc[4 * v + 3]);
+        for (int q = 0; q < 4; ++q) {
+          wc[q] = 0.f;
+          if (c + q <= c1) {
+            const int64_t sl = slot_of(c + q);
+            const float mc = a.ws_ml[(sl * 2) * HEADS + h];
+            if (mc != -CUDART_INF_F) {
+              wc[q] = exp2f(mc - M);
+              L += wc[q] * a.ws_ml[(sl * 2 + 1) * HEADS + h];
+            }
+#pragma unroll
+            for (int j = 0; j < CDIMS; ++j) x[q][j] = a.ws_o[(sl * RANK + d0 + j) * HEADS + h];
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int j = 0; j < CDIMS; ++j) acc[j] = (wc[q] != 0.f) ? fmaf(wc[q], x[q][j], acc[j]) : acc[j];
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+      for (int j = 0; j < CDIMS; ++j) acc[j] *= inv;
     }
   }
-  if (a.out_f32) {
-    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.ctx) + orow) + lane * 4;
-#pragma unroll
-    for (int v = 0; v < 4; ++v)
-      dst[v] = make_float4(acc[4 * v] * inv, acc[4 * v + 1] * inv, acc[4 * v + 2] * inv, acc[4 * v + 3] * inv);
-  } else {
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.ctx) + orow) + lane * 2;
-#pragma unroll
-    for (int v = 0; v < 2; ++v)
-      dst[v] = make_uint4(pack_bf16x2(acc[8 * v] * inv, acc[8 * v + 1] * inv),
-                          pack_bf16x2(acc[8 * v + 2] * inv, acc[8 * v + 3] * inv),
-                          pack_bf16x2(acc[8 * v + 4] * inv, acc[8 * v + 5] * inv),
-                          pack_bf16x2(acc[8 * v + 6] * inv, acc[8 * v + 7] * inv));
+  if (write) {
+    if (a.out_f32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.ctx) + orow);
+      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    } else {
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.ctx) + orow) =
+          make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                     pack_bf16x2(acc[6], acc[7]));
+    }
+    if (blockIdx.y == 0 && a.lse)
+      a.lse[(int64_t)n * HEADS + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -CUDART_INF_F;
   }
-  if (lane == 0 && a.lse) a.lse[(int64_t)n * HEADS + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -CUDART_INF_F;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -790,14 +862,36 @@ cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* works
     const uint32_t box[3] = {64, BN, 1};
     if (!encode_tmap_bf16(&rope_map, g.rope, 3, dims, strides, box)) return cudaErrorInvalidValue;
   }
+  // Row maps for gathers: the cache as [rows, dims] with one-row boxes; a
+  // batch row's rows start at b * (batch stride / row stride).
+  CUtensorMap lat_rows_map = lat_map, rope_rows_map = rope_map;
+  a.gather_tma = 0;
+  a.lat_rows_per_batch = a.rope_rows_per_batch = 0;
+  if (g.sel != nullptr && g.latent_batch_stride % g.latent_row_stride == 0 &&
+      g.rope_batch_stride % g.rope_row_stride == 0) {
+    a.lat_rows_per_batch = a.batch_in_map ? (int32_t)(g.latent_batch_stride / g.latent_row_stride) : 0;
+    a.rope_rows_per_batch = a.batch_in_map ? (int32_t)(g.rope_batch_stride / g.rope_row_stride) : 0;
+    const uint64_t lrows = (uint64_t)(a.batch_in_map ? g.batch - 1 : 0) * a.lat_rows_per_batch + g.t_max;
+    const uint64_t rrows = (uint64_t)(a.batch_in_map ? g.batch - 1 : 0) * a.rope_rows_per_batch + g.t_max;
+    const uint64_t ld[2] = {(uint64_t)g.rank, lrows}, rd[2] = {(uint64_t)g.rope_dim, rrows};
+    const uint64_t ls[1] = {(uint64_t)g.latent_row_stride * 2}, rs[1] = {(uint64_t)g.rope_row_stride * 2};
+    const uint32_t box[2] = {64, 1};
+    if (lrows < (1ull << 31) && rrows < (1ull << 31) && encode_tmap_bf16(&lat_rows_map, g.latent, 2, ld, ls, box) &&
+        encode_tmap_bf16(&rope_rows_map, g.rope, 2, rd, rs, box))
+      a.gather_tma = 1;
+  }
   static bool attr = false;
   if (!attr) {
     cudaFuncSetAttribute(tc_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     attr = true;
   }
-  tc_plan_kernel<<<1, 1024, 0, stream>>>(a);
-  tc_decode_kernel<<<2 * nclusters, THREADS, SMEM_BYTES, stream>>>(lat_map, rope_map, a);
-  tc_combine_kernel<<<dim3(n_q, g.heads / 4), 128, 0, stream>>>(a);
+  cudaError_t e = launch_pdl(tc_plan_kernel, dim3(1), dim3(1024), 0, stream, a);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(tc_decode_kernel, dim3(2 * nclusters), dim3(THREADS), SMEM_BYTES, stream, lat_map, rope_map,
+                 lat_rows_map, rope_rows_map, a);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(tc_combine_kernel, dim3(n_q, RANK / CDIMS), dim3(HEADS), 0, stream, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -67,6 +67,7 @@ __global__ void __launch_bounds__(128) tc_absorb_kernel(const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
   bool ok = true;
+  pdl_wait();
 
   if (threadIdx.x == 0) {
     const uint32_t bytes = 2 * 16384 + 2 * npad * 128;
@@ -110,6 +111,7 @@ __global__ void __launch_bounds__(128) tc_absorb_kernel(const __grid_constant__ 
       }
     }
   }
+  pdl_trigger();
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, ncols);
@@ -159,6 +161,7 @@ __global__ void __launch_bounds__(128) tc_project_kernel(const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
   bool ok = true;
+  pdl_wait();
 
   if (threadIdx.x == 0) {
     const int row0 = h * a.w_head_rows + a.w_row0;  // first row of W_UV_h in kv_b_proj
@@ -209,6 +212,7 @@ __global__ void __launch_bounds__(128) tc_project_kernel(const __grid_constant__
       }
     }
   }
+  pdl_trigger();
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, ncols);
@@ -240,8 +244,8 @@ cudaError_t launch_tc_absorb(const AbsorbParams& p, cudaStream_t stream) {
     cudaFuncSetAttribute(tc_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 1024 + 32768 + 2 * 256 * 128);
     attr = true;
   }
-  tc_absorb_kernel<<<dim3(p.rank / 128, p.heads), 128, smem, stream>>>(wmap, qmap, a);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(tc_absorb_kernel, dim3(p.rank / 128, p.heads), dim3(128), smem, stream, wmap, qmap, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_tc_project(const ProjectParams& p, int out_dtype, cudaStream_t stream) {
@@ -268,8 +272,8 @@ cudaError_t launch_tc_project(const ProjectParams& p, int out_dtype, cudaStream_
     cudaFuncSetAttribute(tc_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 1024 + 8 * 16384 + 8 * 64 * 128);
     attr = true;
   }
-  tc_project_kernel<<<p.heads, 128, smem, stream>>>(wmap, cmap, a);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(tc_project_kernel, dim3(p.heads), dim3(128), smem, stream, wmap, cmap, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace mla

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace mla {
 
 // Encodes a bf16 tensor map of rank 2 or 3 with 128-byte swizzle.
@@ -13,5 +15,25 @@ namespace mla {
 // dims[i+1].  Returns false (and sets the error detail) on failure.
 bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                       const uint64_t* strides_bytes, const uint32_t* box);
+
+// Launch with programmatic dependent launch allowed: the kernel may start its
+// prologue while the previous kernel in the stream drains; every kernel
+// launched this way calls griddepcontrol.wait before it touches memory the
+// previous kernels write, and griddepcontrol.launch_dependents when done.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace mla
