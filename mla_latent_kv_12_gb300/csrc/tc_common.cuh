@@ -135,6 +135,32 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t x, ui
                : "memory");
 }
 
+// Bulk copy of `bytes` from this CTA's shared memory into another CTA's
+// (shared::cluster address), completing as transactions on that CTA's barrier.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t remote_dst, uint32_t local_src, uint32_t bytes,
+                                                  uint32_t remote_bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t"
+      "cp.async.bulk.commit_group;"
+      ::"r"(remote_dst), "r"(local_src), "r"(bytes), "r"(remote_bar)
+      : "memory");
+}
+
+// Wait until this thread's bulk copies have finished reading their source.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Wait until this thread's bulk copies have completed (source read, destination written).
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Named barrier over `count` threads (id > 0; id 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // 2^x on the special-function unit (PTX ex2.approx; relative error ~2^-22,
 // +0 for -inf).
 __device__ __forceinline__ float ex2_approx(float x) {

@@ -44,10 +44,10 @@ constexpr int STAGES = 4;
 constexpr int NCH = 5;                    // 64-dim chunks per stage: 4 latent + the rope row
 constexpr int CHUNK_BYTES = BN * 128;     // one [64 keys x 64 dims] bf16 box
 constexpr int STAGE_BYTES = NCH * CHUNK_BYTES;
-constexpr int X_BYTES = 128 * BN * 4;     // exchanged f32 partial scores
+constexpr int X_BYTES = 128 * BN * 4;     // f32 partial scores of one tile (sent / received)
 constexpr int HEADS = 128, RANK = 512, DV = 256;  // DV: latent dims per CTA
 constexpr int THREADS = 192;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + X_BYTES;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 2 * X_BYTES;
 constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 400, TM_P = 464;  // TMEM columns (Q: 128 + 16)
 constexpr long long kWaitLimit = 1LL << 32;  // clock cycles (~2 s)
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
@@ -232,9 +232,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
   float* xbuf = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES);  // [16][128][4] written by the peer
+  float* xout = xbuf + X_BYTES / 4;                                        // [16][128][4] staged for the peer
 
   __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES];
   __shared__ __align__(8) uint64_t s_full, s_free, p_full, pv_done, q_full, o_free, x_full, x_free, mma_drain;
+  __shared__ __align__(8) uint64_t xo_free, xo_full;   // staging buffer: free to write / fully written
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
   auto aborted = [&]() -> bool { return __any_sync(0xffffffffu, abort_s != 0); };
@@ -260,14 +262,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       mbar_init(&empty_bar[s], 1);
     }
     mbar_init(&s_full, 1);
-    mbar_init(&s_free, 128);
-    mbar_init(&p_full, 128);
+    mbar_init(&s_free, 4);      // one arrival per softmax warp
+    mbar_init(&p_full, 4);
     mbar_init(&pv_done, 1);
-    mbar_init(&q_full, 128);
-    mbar_init(&o_free, 128);
-    mbar_init(&x_full, 1);      // local expect_tx arrival + the peer's st.async bytes
-    mbar_init(&x_free, 128);
+    mbar_init(&q_full, 4);
+    mbar_init(&o_free, 4);
+    mbar_init(&x_full, 1);      // local expect_tx arrival + the peer's bulk-copy bytes
+    mbar_init(&x_free, 4);      // the peer's softmax warps, once they have read their copy
     mbar_init(&mma_drain, 1);
+    mbar_init(&xo_free, 1);     // the exchange issuer: its previous copy has read the staging buffer
+    mbar_init(&xo_full, 4);     // the softmax warps: their rows are staged
     abort_s = 0;
     fence_mbar_init();
   }
@@ -541,7 +545,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&q_full);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_full);
       }
       float m_used = -CUDART_INF_F, l = 0.f;
       bool first_tile = true;
@@ -565,15 +570,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         tmem_ld32(tmem + TM_S + 32 + lane_off, sb);
         tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(&s_free);
-        // ---- exchange with the peer CTA
-        if (tile > 0 && !mbar_wait_cluster_warp(&x_free, (tile - 1) & 1u, kWaitLimit)) { fail(); break; }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free);
+        // ---- exchange with the peer CTA: stage the own partial locally, then
+        // one thread moves all 32 KB with a single bulk copy into the peer's
+        // receive buffer, counted as transaction bytes on the peer's barrier.
+        // (mbarrier hand-offs, all with bounded waits, order the staging.)
+        if (h == 0) {
+          if (tile > 0) bulk_wait_read();          // the previous copy has read the staging buffer
+          mbar_arrive(&xo_free);
+        }
+        if (!mbar_wait_warp(&xo_free, tile & 1u, kWaitLimit)) { fail(); break; }
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const uint32_t* src = c < 8 ? &sa[4 * c] : &sb[4 * (c - 8)];
-          st_async_v4(xbuf_peer + (uint32_t)((c * 128 + h) * 16), src[0], src[1], src[2], src[3], x_full_peer);
+          *reinterpret_cast<uint4*>(xout + (c * 128 + h) * 4) = make_uint4(src[0], src[1], src[2], src[3]);
         }
-        if (h == 0) mbar_arrive_expect_tx_u32(smem_u32(&x_full), X_BYTES);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xo_full);
+        if (h == 0) {
+          if (!mbar_wait(&xo_full, tile & 1u, kWaitLimit) ||
+              (tile > 0 && !mbar_wait_cluster(&x_free, (tile - 1) & 1u, kWaitLimit)))
+            fail();
+          else
+            bulk_copy_to_peer(xbuf_peer, smem_u32(xout), X_BYTES, x_full_peer);
+          mbar_arrive_expect_tx_u32(smem_u32(&x_full), X_BYTES);
+        }
         if (!mbar_wait_cluster_warp(&x_full, tile & 1u, kWaitLimit)) { fail(); break; }
         float s[BN];
 #pragma unroll
@@ -585,19 +608,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           s[4 * c + 2] = __uint_as_float(own[2]) + x.z;
           s[4 * c + 3] = __uint_as_float(own[3]) + x.w;
         }
-        mbar_arrive_remote(x_free_peer);
-        // ---- online softmax (log2 domain) with lazy rescaling; independent
-        // partial maxima / sums keep the dependency chains short.
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(x_free_peer);
+        // ---- online softmax (log2 domain) with lazy rescaling.  The scale is
+        // positive, so the row maximum is taken on raw scores and scaled once;
+        // each probability is ex2(fma(s, scale, -m)).  Independent partial
+        // maxima / sums keep the dependency chains short.
+        if (valid != ~0ull) {
+#pragma unroll
+          for (int k = 0; k < BN; ++k) s[k] = ((valid >> k) & 1ull) ? s[k] : -CUDART_INF_F;
+        }
         float mx8[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = -CUDART_INF_F;
+        for (int k = 0; k < 8; ++k) mx8[k] = s[k];
 #pragma unroll
-        for (int k = 0; k < BN; ++k) {
-          s[k] = ((valid >> k) & 1ull) ? s[k] * a.scale_log2 : -CUDART_INF_F;
-          mx8[k & 7] = fmaxf(mx8[k & 7], s[k]);
-        }
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int k = 8; k < BN; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], s[k]);
+        const float mx = a.scale_log2 * fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         float alpha = 1.f;
         bool rescale = false;
         if (mx > m_used + kRescaleThreshold || m_used == -CUDART_INF_F) {
@@ -608,19 +635,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             m_used = m_new;
           }
         }
-        // With m_used finite, ex2(-inf - m) = +0 masks an entry; a tile with no
-        // visible entry so far (m_used = -inf) contributes nothing.
-        const float m_sub = (m_used == -CUDART_INF_F) ? 0.f : m_used;
+        // With m_used finite, ex2(-inf) = +0 masks an entry; while no entry has
+        // been visible (m_used = -inf) every p is 0.
+        const float neg_m = (m_used == -CUDART_INF_F) ? -CUDART_INF_F : -m_used;
         uint32_t pk[32];
         float ps8[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) ps8[k] = 0.f;
 #pragma unroll
         for (int k = 0; k < BN; k += 2) {
-          const float p0 = ex2_approx(s[k] - m_sub);
-          const float p1 = ex2_approx(s[k + 1] - m_sub);
+          const float p0 = ex2_approx(fmaf(s[k], a.scale_log2, neg_m));
+          const float p1 = ex2_approx(fmaf(s[k + 1], a.scale_log2, neg_m));
+          ps8[(k >> 1) & 7] += p0 + p1;
           const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-          ps8[(k >> 1) & 7] += __low2float(pb) + __high2float(pb);
           pk[k >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
         }
         const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
@@ -645,7 +672,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         tmem_st32(tmem + TM_P + lane_off, pk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&p_full);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full);
         first_tile = false;
         ++tile;
       }
@@ -699,12 +727,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&o_free);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_free);
       ++seg;
     }
   }
 
   // ---------------------------------------------------------------- teardown
+  if (warp >= 2 && (32 * (warp & 3) + lane) == 0) bulk_wait_all();   // the exchange issuer's copies are done
   pdl_trigger();
   tc_fence_before();
   __syncthreads();
