@@ -28,6 +28,7 @@
 //    wholly inside one range is finished in place; otherwise each piece writes
 //    an f32 partial (O, m, l; heads contiguous) and a combine kernel merges them.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math_constants.h>
 
 #include "mla_internal.h"
@@ -44,10 +45,10 @@ constexpr int STAGES = 4;
 constexpr int NCH = 5;                    // 64-dim chunks per stage: 4 latent + the rope row
 constexpr int CHUNK_BYTES = BN * 128;     // one [64 keys x 64 dims] bf16 box
 constexpr int STAGE_BYTES = NCH * CHUNK_BYTES;
-constexpr int X_BYTES = 128 * BN * 4;     // f32 partial scores of one tile (sent / received)
+constexpr int XH_BYTES = 128 * BN * 2;    // fp16 partial scores of one tile (one send / receive buffer)
 constexpr int HEADS = 128, RANK = 512, DV = 256;  // DV: latent dims per CTA
-constexpr int THREADS = 192;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 2 * X_BYTES;
+constexpr int THREADS = 320;   // producer, MMA, 4 softmax warps, 4 exchange warps
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 4 * XH_BYTES;  // + send[2], receive[2]
 constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 400, TM_P = 464;  // TMEM columns (Q: 128 + 16)
 constexpr long long kWaitLimit = 1LL << 32;  // clock cycles (~2 s)
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
@@ -231,12 +232,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
-  float* xbuf = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES);  // [16][128][4] written by the peer
-  float* xout = xbuf + X_BYTES / 4;                                        // [16][128][4] staged for the peer
+  // Exchange buffers, each [8][128 heads][16 B] of fp16 scores: xin[b] is written
+  // by the peer's bulk copy, xout[b] is staged here and copied to the peer.
+  uint8_t* xin = smem + STAGES * STAGE_BYTES;        // 2 x XH_BYTES
+  uint8_t* xout = xin + 2 * XH_BYTES;                // 2 x XH_BYTES
 
   __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES];
-  __shared__ __align__(8) uint64_t s_full, s_free, p_full, pv_done, q_full, o_free, x_full, x_free, mma_drain;
-  __shared__ __align__(8) uint64_t xo_free, xo_full;   // staging buffer: free to write / fully written
+  __shared__ __align__(8) uint64_t s_full, s_free, p_full, pv_done, q_full, o_free, mma_drain;
+  __shared__ __align__(8) uint64_t x_full[2], x_free[2], xo_full[2], xo_free[2];  // per exchange buffer
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
   auto aborted = [&]() -> bool { return __any_sync(0xffffffffu, abort_s != 0); };
@@ -262,16 +265,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       mbar_init(&empty_bar[s], 1);
     }
     mbar_init(&s_full, 1);
-    mbar_init(&s_free, 4);      // one arrival per softmax warp
-    mbar_init(&p_full, 4);
+    mbar_init(&s_free, 4);      // the exchange warps have read S
+    mbar_init(&p_full, 4);      // one arrival per softmax warp
     mbar_init(&pv_done, 1);
     mbar_init(&q_full, 4);
     mbar_init(&o_free, 4);
-    mbar_init(&x_full, 1);      // local expect_tx arrival + the peer's bulk-copy bytes
-    mbar_init(&x_free, 4);      // the peer's softmax warps, once they have read their copy
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&x_full[b], 1);   // local expect_tx arrival + the peer's bulk-copy bytes
+      mbar_init(&x_free[b], 4);   // the peer's softmax warps have read xin[b] (so our copy is done)
+      mbar_init(&xo_full[b], 4);  // our exchange warps have staged xout[b]
+      mbar_init(&xo_free[b], 4);  // our softmax warps have read xout[b]
+    }
     mbar_init(&mma_drain, 1);
-    mbar_init(&xo_free, 1);     // the exchange issuer: its previous copy has read the staging buffer
-    mbar_init(&xo_full, 4);     // the softmax warps: their rows are staged
     abort_s = 0;
     fence_mbar_init();
   }
@@ -489,14 +494,76 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (lane == 0) mma_commit(&mma_drain);
     __syncwarp();
     mbar_wait_warp(&mma_drain, 0, kWaitLimit);
+  } else if (warp >= 6) {
+    // ============================================================ exchange warps
+    // Read this CTA's partial scores from TMEM, round them to fp16 (saturating)
+    // and send them to the peer with one bulk copy per tile, one tile ahead of
+    // the softmax warps (two send and two receive buffers).
+    const int quarter = warp & 3;
+    const int h = 32 * quarter + lane;
+    const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
+    const bool issuer = (h == 0);
+    const uint32_t xin_peer = mapa(smem_u32(xin), peer);
+    uint32_t x_full_peer[2];
+    x_full_peer[0] = mapa(smem_u32(&x_full[0]), peer);
+    x_full_peer[1] = mapa(smem_u32(&x_full[1]), peer);
+    uint32_t tile = 0;
+    int u, n, t0, t1;
+    bool whole;
+    while (!aborted() && it.next(u, t0, t1, whole)) {
+      if (!member_segment(a, u, member, n, t0, t1)) continue;
+      for (int t = t0; t < t1; ++t) {
+        const uint32_t b = tile & 1u, use = tile >> 1;
+        if (tile >= 2) {
+          // the peer has read our copy of tile-2 (so xout[b] is read too), and
+          // our softmax warps have read their own half of it
+          if (!mbar_wait_cluster_warp(&x_free[b], (use - 1) & 1u, kWaitLimit)) { fail(); break; }
+          if (!mbar_wait_warp(&xo_free[b], (use - 1) & 1u, kWaitLimit)) { fail(); break; }
+        }
+        if (!mbar_wait_warp(&s_full, tile & 1u, kWaitLimit)) { fail(); break; }
+        tc_fence_after();
+        uint32_t sa[32], sb[32];
+        tmem_ld32(tmem + TM_S + lane_off, sa);
+        tmem_ld32(tmem + TM_S + 32 + lane_off, sb);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free);
+        uint8_t* xo = xout + b * XH_BYTES;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int k = 8 * c + 2 * q;   // scores k, k+1
+            const float lo = fminf(fmaxf(__uint_as_float(k < 32 ? sa[k] : sb[k - 32]), -65504.f), 65504.f);
+            const float hi = fminf(fmaxf(__uint_as_float(k < 32 ? sa[k + 1] : sb[k - 31]), -65504.f), 65504.f);
+            const __half2 hv = __floats2half2_rn(lo, hi);
+            w[q] = *reinterpret_cast<const uint32_t*>(&hv);
+          }
+          *reinterpret_cast<uint4*>(xo + (c * 128 + h) * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xo_full[b]);
+        if (issuer) {
+          if (!mbar_wait(&xo_full[b], use & 1u, kWaitLimit))
+            fail();
+          else
+            bulk_copy_to_peer(xin_peer + b * XH_BYTES, smem_u32(xo), XH_BYTES, x_full_peer[b]);
+          mbar_arrive_expect_tx_u32(smem_u32(&x_full[b]), XH_BYTES);
+        }
+        ++tile;
+      }
+    }
   } else {
-    // ============================================================ softmax / exchange / epilogue
+    // ============================================================ softmax / epilogue
     const int quarter = warp & 3;
     const int h = 32 * quarter + lane;                    // head = TMEM lane
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
-    const uint32_t x_full_peer = mapa(smem_u32(&x_full), peer);
-    const uint32_t x_free_peer = mapa(smem_u32(&x_free), peer);
-    const uint32_t xbuf_peer = mapa(smem_u32(xbuf), peer);
+    uint32_t x_free_peer[2];
+    x_free_peer[0] = mapa(smem_u32(&x_free[0]), peer);
+    x_free_peer[1] = mapa(smem_u32(&x_free[1]), peer);
     uint32_t tile = 0, seg = 0;
     uint32_t pv_seen = 0;   // P.V completions waited for
     int u, n, t0, t1;
@@ -562,54 +629,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           }
           valid = (uint64_t)__ballot_sync(0xffffffffu, v0) | ((uint64_t)__ballot_sync(0xffffffffu, v1) << 32);
         }
-        // ---- own partial scores
-        if (!mbar_wait_warp(&s_full, tile & 1u, kWaitLimit)) { fail(); break; }
-        tc_fence_after();
-        uint32_t sa[32], sb[32];
-        tmem_ld32(tmem + TM_S + lane_off, sa);
-        tmem_ld32(tmem + TM_S + 32 + lane_off, sb);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free);
-        // ---- exchange with the peer CTA: stage the own partial locally, then
-        // one thread moves all 32 KB with a single bulk copy into the peer's
-        // receive buffer, counted as transaction bytes on the peer's barrier.
-        // (mbarrier hand-offs, all with bounded waits, order the staging.)
-        if (h == 0) {
-          if (tile > 0) bulk_wait_read();          // the previous copy has read the staging buffer
-          mbar_arrive(&xo_free);
-        }
-        if (!mbar_wait_warp(&xo_free, tile & 1u, kWaitLimit)) { fail(); break; }
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const uint32_t* src = c < 8 ? &sa[4 * c] : &sb[4 * (c - 8)];
-          *reinterpret_cast<uint4*>(xout + (c * 128 + h) * 4) = make_uint4(src[0], src[1], src[2], src[3]);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&xo_full);
-        if (h == 0) {
-          if (!mbar_wait(&xo_full, tile & 1u, kWaitLimit) ||
-              (tile > 0 && !mbar_wait_cluster(&x_free, (tile - 1) & 1u, kWaitLimit)))
-            fail();
-          else
-            bulk_copy_to_peer(xbuf_peer, smem_u32(xout), X_BYTES, x_full_peer);
-          mbar_arrive_expect_tx_u32(smem_u32(&x_full), X_BYTES);
-        }
-        if (!mbar_wait_cluster_warp(&x_full, tile & 1u, kWaitLimit)) { fail(); break; }
+        // ---- scores: own and peer fp16 partials, summed in the same order-free
+        // way in both CTAs (fp32 addition of the same two values)
+        const uint32_t b = tile & 1u, use = tile >> 1;
+        if (!mbar_wait_warp(&xo_full[b], use & 1u, kWaitLimit)) { fail(); break; }
+        if (!mbar_wait_cluster_warp(&x_full[b], use & 1u, kWaitLimit)) { fail(); break; }
         float s[BN];
+        {
+          const uint8_t* xo = xout + b * XH_BYTES;
+          const uint8_t* xi = xin + b * XH_BYTES;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float4 x = *reinterpret_cast<const float4*>(xbuf + (c * 128 + h) * 4);
-          const uint32_t* own = c < 8 ? &sa[4 * c] : &sb[4 * (c - 8)];
-          s[4 * c + 0] = __uint_as_float(own[0]) + x.x;
-          s[4 * c + 1] = __uint_as_float(own[1]) + x.y;
-          s[4 * c + 2] = __uint_as_float(own[2]) + x.z;
-          s[4 * c + 3] = __uint_as_float(own[3]) + x.w;
+          for (int c = 0; c < 8; ++c) {
+            const uint4 o4 = *reinterpret_cast<const uint4*>(xo + (c * 128 + h) * 16);
+            const uint4 i4 = *reinterpret_cast<const uint4*>(xi + (c * 128 + h) * 16);
+            const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w}, iw[4] = {i4.x, i4.y, i4.z, i4.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float2 of = __half22float2(*reinterpret_cast<const __half2*>(&ow[q]));
+              const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&iw[q]));
+              s[8 * c + 2 * q] = of.x + pf.x;
+              s[8 * c + 2 * q + 1] = of.y + pf.y;
+            }
+          }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(x_free_peer);
+        if (lane == 0) {
+          mbar_arrive(&xo_free[b]);
+          mbar_arrive_remote(x_free_peer[b]);
+        }
         // ---- online softmax (log2 domain) with lazy rescaling.  The scale is
         // positive, so the row maximum is taken on raw scores and scaled once;
         // each probability is ex2(fma(s, scale, -m)).  Independent partial
@@ -734,7 +781,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
 
   // ---------------------------------------------------------------- teardown
-  if (warp >= 2 && (32 * (warp & 3) + lane) == 0) bulk_wait_all();   // the exchange issuer's copies are done
+  if (warp == 8 && lane == 0) bulk_wait_all();   // the exchange issuer's copies are done
   pdl_trigger();
   tc_fence_before();
   __syncthreads();
