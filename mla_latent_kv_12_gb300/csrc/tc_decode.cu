@@ -47,7 +47,7 @@ constexpr int CHUNK_BYTES = BN * 128;     // one [64 keys x 64 dims] bf16 box
 constexpr int STAGE_BYTES = NCH * CHUNK_BYTES;
 constexpr int XH_BYTES = 128 * BN * 2;    // fp16 partial scores of one tile (one send / receive buffer)
 constexpr int HEADS = 128, RANK = 512, DV = 256;  // DV: latent dims per CTA
-constexpr int THREADS = 320;   // producer, MMA, 4 softmax warps, 4 exchange warps
+constexpr int THREADS = 352;   // producer, score MMA, 4 softmax, 4 exchange, P.V MMA warps
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 4 * XH_BYTES;  // + send[2], receive[2]
 constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 400, TM_P = 464;  // TMEM columns (Q: 128 + 16)
 constexpr long long kWaitLimit = 1LL << 32;  // clock cycles (~2 s)
@@ -238,7 +238,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   uint8_t* xout = xin + 2 * XH_BYTES;                // 2 x XH_BYTES
 
   __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES];
-  __shared__ __align__(8) uint64_t s_full, s_free, p_full, pv_done, q_full, o_free, mma_drain;
+  __shared__ __align__(8) uint64_t s_full, s_free, p_full, pv_done, q_full, o_free, mma_drain, pv_drain;
   __shared__ __align__(8) uint64_t x_full[2], x_free[2], xo_full[2], xo_free[2];  // per exchange buffer
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
@@ -277,6 +277,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       mbar_init(&xo_free[b], 4);  // our softmax warps have read xout[b]
     }
     mbar_init(&mma_drain, 1);
+    mbar_init(&pv_drain, 1);
     abort_s = 0;
     fence_mbar_init();
   }
@@ -401,39 +402,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     for (int s = 0; s < STAGES; ++s)
       if (issued[s]) mbar_wait(&full_bar[s], issued_phase[s], kWaitLimit);
   } else if (warp == 1) {
-    // ============================================================ MMA issuer
+    // ============================================================ score MMA issuer
+    // S(t) as soon as tile t has landed and the exchange warps have read S(t-1);
+    // the P.V issuer (warp 10) runs independently, so scores run ahead.
     const uint32_t idesc_s = idesc_bf16_f32(128, BN, 0, 0);
-    const uint32_t idesc_pv = idesc_bf16_f32(128, DV, 0, 1);
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t tile = 0;      // global tile counter (S / P / PV phases)
-    uint32_t seg = 0;       // segment counter (q_full / o_free phases)
+    uint32_t tile = 0;      // global tile counter (S phases)
+    uint32_t seg = 0;       // segment counter (q_full phases)
     int u, n, t0, t1;
     bool whole;
-    bool pending = false;   // a tile whose P.V is not yet issued
-    int pend_stage = 0;
-    bool pend_first = false;
-    auto issue_pv = [&](int st, bool first, uint32_t j) -> bool {
-      if (!mbar_wait_warp(&p_full, j & 1u, kWaitLimit)) return false;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t base = smem_u32(stages + st * STAGE_BYTES);
-#pragma unroll
-        const uint64_t d0 = smem_desc(base, CHUNK_BYTES, 1024, kSwizzle128B);
-        for (int k = 0; k < BN / 16; ++k)
-          mma_ts(tmem + TM_O, tmem + TM_P + k * 8, d0 + (uint64_t)((k * 2048) >> 4), idesc_pv,
-                 (first && k == 0) ? 0u : 1u);
-        mma_commit(&empty_bar[st]);
-        mma_commit(&pv_done);
-      }
-      __syncwarp();
-      return true;
-    };
     while (!aborted() && it.next(u, t0, t1, whole)) {
       if (!member_segment(a, u, member, n, t0, t1)) continue;
       const int keys = a.keys[n];
       if (!mbar_wait_warp(&q_full, seg & 1u, kWaitLimit)) { fail(); break; }
-      bool first_tile = true;
       for (int t = t0; t < t1; ++t) {
         if (!mbar_wait_warp(&full_bar[stage], phase, kWaitLimit)) { fail(); break; }
         if (!gather && t == (keys - 1) / BN && (keys % BN) != 0) {
@@ -470,31 +452,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           mma_commit(&s_full);
         }
         __syncwarp();
-        if (pending) {
-          if (pend_first && seg > 0 && !mbar_wait_warp(&o_free, (seg - 1) & 1u, kWaitLimit)) { fail(); break; }
-          if (!issue_pv(pend_stage, pend_first, tile - 1)) { fail(); break; }
-        }
-        pending = true;
-        pend_stage = stage;
-        pend_first = first_tile;
-        first_tile = false;
         ++tile;
         if (++stage == STAGES) stage = 0, phase ^= 1u;
       }
       if (aborted()) break;
-      // the segment's last P.V
-      if (pending) {
-        if (pend_first && seg > 0 && !mbar_wait_warp(&o_free, (seg - 1) & 1u, kWaitLimit)) { fail(); break; }
-        if (!issue_pv(pend_stage, pend_first, tile - 1)) { fail(); break; }
-        pending = false;
-      }
       ++seg;
     }
-    // All MMAs of this CTA complete before TMEM is released.
+    // All score MMAs complete before TMEM is released.
     if (lane == 0) mma_commit(&mma_drain);
     __syncwarp();
     mbar_wait_warp(&mma_drain, 0, kWaitLimit);
-  } else if (warp >= 6) {
+  } else if (warp == 10) {
+    // ============================================================ P.V MMA issuer
+    const uint32_t idesc_pv = idesc_bf16_f32(128, DV, 0, 1);
+    int stage = 0;
+    uint32_t tile = 0, seg = 0;
+    int u, n, t0, t1;
+    bool whole;
+    while (!aborted() && it.next(u, t0, t1, whole)) {
+      if (!member_segment(a, u, member, n, t0, t1)) continue;
+      for (int t = t0; t < t1; ++t) {
+        const bool first = (t == t0);
+        // O is overwritten by a segment's first P.V: the previous segment's
+        // epilogue must have read it.
+        if (first && seg > 0 && !mbar_wait_warp(&o_free, (seg - 1) & 1u, kWaitLimit)) { fail(); break; }
+        if (!mbar_wait_warp(&p_full, tile & 1u, kWaitLimit)) { fail(); break; }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint64_t d0 = smem_desc(smem_u32(stages + stage * STAGE_BYTES), CHUNK_BYTES, 1024, kSwizzle128B);
+#pragma unroll
+          for (int k = 0; k < BN / 16; ++k)
+            mma_ts(tmem + TM_O, tmem + TM_P + k * 8, d0 + (uint64_t)((k * 2048) >> 4), idesc_pv,
+                   (first && k == 0) ? 0u : 1u);
+          mma_commit(&empty_bar[stage]);
+          mma_commit(&pv_done);
+        }
+        __syncwarp();
+        ++tile;
+        if (++stage == STAGES) stage = 0;
+      }
+      if (aborted()) break;
+      ++seg;
+    }
+    if (lane == 0) mma_commit(&pv_drain);
+    __syncwarp();
+    mbar_wait_warp(&pv_drain, 0, kWaitLimit);
+  } else if (warp >= 6 && warp < 10) {
     // ============================================================ exchange warps
     // Read this CTA's partial scores from TMEM, round them to fp16 (saturating)
     // and send them to the peer with one bulk copy per tile, one tile ahead of
