@@ -211,6 +211,13 @@ __device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, uint64_
       : "memory");
 }
 
+// Bring a tile of a 3-D tensor map into L2 ahead of its shared-memory load.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+               ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // ------------------------------------------------------------------ cp.async (gathers)
 
 // 16-byte global -> shared copy; `src_bytes` = 0 writes zeros.

@@ -55,6 +55,7 @@ constexpr float kRescaleThreshold = 8.0f;    // log2 units
 // A group's tile range is at least this long: each split writes a 256 KB f32
 // partial, worth it only against a few 72 KB tiles of cache read.
 constexpr int kMinTilesPerGroup = 4;
+constexpr int kPrefetchAhead = 6;    // tiles of the current row pulled into L2 ahead of their load
 
 struct TcDecodeArgs {
   const __nv_bfloat16* q;
@@ -318,6 +319,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const int keys = a.keys[n];
       const int zb = a.batch_in_map ? b : 0;
       const int32_t* list = (gather && a.sel_count[n] != -1) ? a.sel + (int64_t)n * a.k_max : nullptr;
+      if (!gather && lane == 0) {
+        // the segment's first tiles that the loop's look-ahead will not cover
+        for (int t = t0 + STAGES; t < t0 + kPrefetchAhead && t < t1; ++t) {
+          for (int c = 0; c < 4; ++c) tma_prefetch_l2_3d(&lat_map, dim_base + 64 * c, start + t * BN, zb);
+          if (rank == 0) tma_prefetch_l2_3d(&rope_map, 0, start + t * BN, zb);
+        }
+      }
       for (int t = t0; t < t1 && !aborted(); ++t) {
         if (!mbar_wait_warp(&empty_bar[stage], phase ^ 1u, kWaitLimit)) { fail(); break; }
         if (!gather) {
@@ -328,6 +336,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             for (int c = 0; c < 4; ++c)
               tma_load_3d(dst + c * CHUNK_BYTES, &lat_map, &full_bar[stage], dim_base + 64 * c, y, zb);
             tma_load_3d(dst + 4 * CHUNK_BYTES, &rope_map, &full_bar[stage], 0, y, zb);
+            // Pull a tile a few steps ahead into L2, so that refilling a stage
+            // once it frees costs an L2 rather than an HBM round trip.
+            if (t + kPrefetchAhead < t1) {
+              const int yp = y + kPrefetchAhead * BN;
+              for (int c = 0; c < 4; ++c) tma_prefetch_l2_3d(&lat_map, dim_base + 64 * c, yp, zb);
+              if (rank == 0) tma_prefetch_l2_3d(&rope_map, 0, yp, zb);
+            }
           }
         } else if (a.gather_tma) {
           // Row gather by TMA: lane g < 16 owns keys 4g..4g+3 of the tile and
