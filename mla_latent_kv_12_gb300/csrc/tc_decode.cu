@@ -9,9 +9,10 @@
 //  * A cluster of two CTAs (an SM pair) owns one stream of work.  The f32
 //    context accumulator [128 x 512] would fill a whole SM's TMEM, so the pair
 //    splits the feature axis evenly: CTA r scores latent dims [256r, 256r+256)
-//    and rope dims [32r, 32r+32) (18 MMA K-steps each).  The pair swaps its
-//    partial scores through distributed shared memory (st.async, counted as
-//    transactions on the receiving barrier) and both form S = S_0 + S_1
+//    and rope dims [32r, 32r+32) (18 MMA K-steps each).  Each CTA rounds its
+//    partial scores to fp16 and sends them to the peer with one bulk copy per
+//    tile into the peer's shared memory (counted as transactions on the
+//    receiving barrier); both CTAs then add the same two fp16 partials in f32
 //    (commutative, so bit-identical), run the same online softmax, and each
 //    accumulates O[:, own 256 latent dims] += P . latent[:, own dims].  No MMA
 //    work is repeated and every latent byte is read by one CTA (the 128-byte
@@ -20,13 +21,15 @@
 //    are TMA-loaded (128-byte swizzle) into a 4-stage ring; one tile serves the
 //    score MMA (K-major B) and the P.V MMA (MN-major B) through two descriptors.
 //  * Warp roles: warp 0 loads (TMA tiles, or TMA gather4 / cp.async row
-//    gathers for selected positions), warp 1 issues MMAs, warps 2..5 (one
-//    thread per head) run the exchange, online softmax (log2 domain, lazy
-//    rescale), and the epilogue.
-//  * Split-K: a planner kernel counts each query row's tiles; the flattened
-//    tile sequence is cut into equal ranges, one per cluster group.  A row
-//    wholly inside one range is finished in place; otherwise each piece writes
-//    an f32 partial (O, m, l; heads contiguous) and a combine kernel merges them.
+//    gathers for selected positions, plus L2 prefetch ahead); warp 1 issues the
+//    score MMAs; warps 6..9 read the scores from TMEM and run the exchange;
+//    warps 2..5 (one thread per head) run the online softmax (log2 domain,
+//    lazy rescale) and the epilogue; warp 10 issues the P.V MMAs.
+//  * Split-K: each query row's tiles are counted (by every CTA in its prologue
+//    for up to 128 rows, else by a planner kernel); the flattened tile
+//    sequence is cut into equal ranges, one per cluster group.  A row wholly
+//    inside one range is finished in place; otherwise each piece writes an f32
+//    partial (O, m, l) and a combine kernel merges them.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math_constants.h>
@@ -56,6 +59,9 @@ constexpr float kRescaleThreshold = 8.0f;    // log2 units
 // partial, worth it only against a few 72 KB tiles of cache read.
 constexpr int kMinTilesPerGroup = 4;
 constexpr int kPrefetchAhead = 6;    // tiles of the current row pulled into L2 ahead of their load
+// Up to this many query rows, every CTA plans the split itself in its prologue
+// (no planner launch); larger batches use the planner kernel.
+constexpr int kMaxRowsInKernelPlan = 128;
 
 struct TcDecodeArgs {
   const __nv_bfloat16* q;
@@ -87,6 +93,7 @@ struct TcDecodeArgs {
   int32_t batch_in_map;  // 1: use batch coordinate b in the tensor maps
   int32_t gather_tma;    // 1: selected rows come by TMA gather4 (else cp.async)
   int32_t lat_rows_per_batch, rope_rows_per_batch;  // batch stride in rows (gather maps)
+  int32_t plan_in_kernel;  // 1: n_q <= kMaxRowsInKernelPlan, each CTA plans (CTA 0 also stores the plan)
 };
 
 // ------------------------------------------------------------------ helpers
@@ -114,9 +121,9 @@ __device__ __forceinline__ int group_span(const TcDecodeArgs& a, int total) {
 struct WorkIter {
   const int32_t* prefix;
   int n, t, t_begin, t_end;
-  __device__ void init(const TcDecodeArgs& a, int group) {
-    prefix = a.prefix;
-    const int total = a.prefix[a.n_units];
+  __device__ void init(const TcDecodeArgs& a, const int32_t* unit_prefix, int group) {
+    prefix = unit_prefix;
+    const int total = prefix[a.n_units];
     const int per = group_span(a, total);
     const int ngroups = a.num_clusters / a.width;
     const long long b0 = group < ngroups ? (long long)group * per : total;
@@ -150,25 +157,26 @@ struct WorkIter {
 // A member's share of a unit segment: its query row n and the segment's tiles
 // clipped to that row's own tiles (a verify token sees a shorter prefix than
 // the last token).  False if nothing is left.
-__device__ __forceinline__ bool member_segment(const TcDecodeArgs& a, int u, int member, int& n, int& t0,
-                                               int& t1) {
+__device__ __forceinline__ bool member_segment(const TcDecodeArgs& a, const int32_t* keys, int u, int member,
+                                               int& n, int& t0, int& t1) {
   n = u * a.width + member;
-  const int tiles = (a.keys[n] + BN - 1) / BN;
+  const int tiles = (keys[n] + BN - 1) / BN;
   if (t1 > tiles) t1 = tiles;
   return t0 < t1;
 }
 
 // ------------------------------------------------------------------ planner
-// One block: per query row the number of visible entries and tiles, and the
-// exclusive prefix of tiles.  Bad selection counts are flagged and give 0.
-__device__ __forceinline__ int row_keys(const TcDecodeArgs& a, int n) {
+// Per query row the number of visible entries; the planner (or the decode
+// prologue) turns them into tiles and the exclusive prefix of tiles over work
+// units.  Bad selection counts give 0 and are flagged where `flag` is set.
+__device__ __forceinline__ int row_keys(const TcDecodeArgs& a, int n, bool flag) {
   int keys = row_limit(a, n);
   if (a.sel) {
     const int c = a.sel_count[n];
     if (c != -1) {
       if (c <= 0 || c > a.k_max) {
         keys = 0;
-        if (a.status) atomicOr(a.status, MLA_DEVICE_BAD_SELECTION_COUNT);
+        if (flag && a.status) atomicOr(a.status, MLA_DEVICE_BAD_SELECTION_COUNT);
       } else {
         keys = c;
       }
@@ -190,7 +198,7 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const __grid_constant__ T
     if (u < a.n_units) {
       for (int i = 0; i < a.width; ++i) {
         const int n = u * a.width + i;
-        const int keys = row_keys(a, n);
+        const int keys = row_keys(a, n, true);
         a.keys[n] = keys;
         const int t = (keys + BN - 1) / BN;
         tiles = t > tiles ? t : tiles;
@@ -243,6 +251,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   __shared__ __align__(8) uint64_t x_full[2], x_free[2], xo_full[2], xo_free[2];  // per exchange buffer
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
+  __shared__ int32_t plan_keys_s[kMaxRowsInKernelPlan];
+  __shared__ int32_t plan_prefix_s[kMaxRowsInKernelPlan + 1];
   auto aborted = [&]() -> bool { return __any_sync(0xffffffffu, abort_s != 0); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -291,10 +301,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   cluster_sync();   // peer barriers initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
-  pdl_wait();       // the planner's prefix and counts (and the query) are complete
+  pdl_wait();       // the query (and the planner's prefix and counts) are complete
 
+  const int32_t* keys_p = a.keys;
+  const int32_t* prefix_p = a.prefix;
+  if (a.plan_in_kernel) {
+    // Visible entries per query row, then per unit its tiles (the longest of
+    // its `width` rows) and their exclusive prefix, scanned by warp 0 (at most
+    // 128 units, four per lane in unit order).
+    if (threadIdx.x < a.n_q) plan_keys_s[threadIdx.x] = row_keys(a, threadIdx.x, blockIdx.x == 0);
+    __syncthreads();
+    if (warp == 0) {
+      int carry = 0;
+      for (int j = 0; j < kMaxRowsInKernelPlan / 32; ++j) {
+        const int u = 32 * j + lane;
+        int tiles = 0;
+        if (u < a.n_units)
+          for (int i = 0; i < a.width; ++i) tiles = max(tiles, (plan_keys_s[u * a.width + i] + BN - 1) / BN);
+        int v = tiles;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int x = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += x;
+        }
+        if (u < a.n_units) plan_prefix_s[u] = carry + v - tiles;
+        carry += __shfl_sync(0xffffffffu, v, 31);
+      }
+      if (lane == 0) plan_prefix_s[a.n_units] = carry;
+    }
+    __syncthreads();
+    keys_p = plan_keys_s;
+    prefix_p = plan_prefix_s;
+    if (blockIdx.x == 0) {   // the combine kernel reads the plan from the workspace
+      for (int i = threadIdx.x; i < a.n_q; i += THREADS) a.keys[i] = plan_keys_s[i];
+      for (int i = threadIdx.x; i <= a.n_units; i += THREADS) a.prefix[i] = plan_prefix_s[i];
+    }
+  }
   WorkIter it;
-  it.init(a, group);
+  it.init(a, prefix_p, group);
 
   auto fail = [&]() {
     abort_s = 1;
@@ -312,11 +356,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     int u, n, t0, t1;
     bool whole;
     while (!aborted() && it.next(u, t0, t1, whole)) {
-      if (!member_segment(a, u, member, n, t0, t1)) continue;
+      if (!member_segment(a, keys_p, u, member, n, t0, t1)) continue;
       const int b = n / a.s_q;
       const int start = a.kv_start ? a.kv_start[b] : 0;
       const int limit = row_limit(a, n);
-      const int keys = a.keys[n];
+      const int keys = keys_p[n];
       const int zb = a.batch_in_map ? b : 0;
       const int32_t* list = (gather && a.sel_count[n] != -1) ? a.sel + (int64_t)n * a.k_max : nullptr;
       if (!gather && lane == 0) {
@@ -428,8 +472,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     int u, n, t0, t1;
     bool whole;
     while (!aborted() && it.next(u, t0, t1, whole)) {
-      if (!member_segment(a, u, member, n, t0, t1)) continue;
-      const int keys = a.keys[n];
+      if (!member_segment(a, keys_p, u, member, n, t0, t1)) continue;
+      const int keys = keys_p[n];
       if (!mbar_wait_warp(&q_full, seg & 1u, kWaitLimit)) { fail(); break; }
       for (int t = t0; t < t1; ++t) {
         if (!mbar_wait_warp(&full_bar[stage], phase, kWaitLimit)) { fail(); break; }
@@ -485,7 +529,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     int u, n, t0, t1;
     bool whole;
     while (!aborted() && it.next(u, t0, t1, whole)) {
-      if (!member_segment(a, u, member, n, t0, t1)) continue;
+      if (!member_segment(a, keys_p, u, member, n, t0, t1)) continue;
       for (int t = t0; t < t1; ++t) {
         const bool first = (t == t0);
         // O is overwritten by a segment's first P.V: the previous segment's
@@ -529,7 +573,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     int u, n, t0, t1;
     bool whole;
     while (!aborted() && it.next(u, t0, t1, whole)) {
-      if (!member_segment(a, u, member, n, t0, t1)) continue;
+      if (!member_segment(a, keys_p, u, member, n, t0, t1)) continue;
       for (int t = t0; t < t1; ++t) {
         const uint32_t b = tile & 1u, use = tile >> 1;
         if (tile >= 2) {
@@ -587,7 +631,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     int u, n, t0, t1;
     bool whole;
     while (!aborted() && it.next(u, t0, t1, whole)) {
-      const bool any = member_segment(a, u, member, n, t0, t1);
+      const bool any = member_segment(a, keys_p, u, member, n, t0, t1);
       const int64_t slot = ((int64_t)u + group) * a.width + member;
       if (!any) {
         // Nothing of this row in the group's range: an empty partial (weight 0).
@@ -597,7 +641,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         continue;
       }
-      const int keys = a.keys[n];
+      const int keys = keys_p[n];
       const int limit = row_limit(a, n);
       const int32_t* list = (gather && a.sel_count[n] != -1) ? a.sel + (int64_t)n * a.k_max : nullptr;
       // ---- Q row of this head (this CTA's dims) into TMEM
@@ -750,20 +794,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
       if (aborted()) break;
       tc_fence_after();
+      // O leaves TMEM 32 columns at a time, the next chunk's load in flight
+      // while the current one is stored.
+      auto drain_o = [&](auto&& store_chunk) {
+        uint32_t oa[32], ob[32];
+        tmem_ld32(tmem + TM_O + lane_off, oa);
+#pragma unroll
+        for (int c = 0; c < DV / 32; c += 2) {
+          tmem_wait_ld_regs(oa);
+          tmem_ld32(tmem + TM_O + (c + 1) * 32 + lane_off, ob);
+          store_chunk(c, oa);
+          tmem_wait_ld_regs(ob);
+          if (c + 2 < DV / 32) tmem_ld32(tmem + TM_O + (c + 2) * 32 + lane_off, oa);
+          store_chunk(c + 1, ob);
+        }
+      };
       if (whole) {
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const int64_t off = (int64_t)n * a.ctx_row_stride + (int64_t)h * a.ctx_head_stride + dim_base;
-        for (int c = 0; c < DV / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tmem + TM_O + c * 32 + lane_off, o);
-          tmem_wait_ld();
-          if (a.out_f32) {
+        if (a.out_f32) {
+          drain_o([&](int c, const uint32_t(&o)[32]) {
             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.ctx) + off + c * 32);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
               dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
                                    __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
-          } else {
+          });
+        } else {
+          drain_o([&](int c, const uint32_t(&o)[32]) {
             uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.ctx) + off + c * 32);
 #pragma unroll
             for (int v = 0; v < 4; ++v)
@@ -771,21 +829,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                                   pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv),
                                   pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv),
                                   pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv));
-          }
+          });
         }
         if (rank == 0 && a.lse)
           a.lse[(int64_t)n * HEADS + h] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
       } else {
-        // Partial O stored dims-major, heads contiguous: a warp's 32 heads
-        // write one 128-byte line per dim.
-        float* dst = a.ws_o + (slot * RANK + dim_base) * HEADS + h;
-        for (int c = 0; c < DV / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tmem + TM_O + c * 32 + lane_off, o);
-          tmem_wait_ld();
+        // Partial O as [slot][RANK/8][H][8] f32: a thread stores 8 dims of its
+        // head as one 32-byte sector, a warp 1 KB contiguous.
+        float* dst = a.ws_o + ((slot * (RANK / 8) + dim_base / 8) * HEADS + h) * 8;
+        drain_o([&](int c, const uint32_t(&o)[32]) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) dst[(c * 32 + k) * HEADS] = __uint_as_float(o[k]);
-        }
+          for (int q = 0; q < 4; ++q) {
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(o[8 * q + j]);
+            st_global_v8(dst + (int64_t)(4 * c + q) * HEADS * 8, v);
+          }
+        });
         if (rank == 0) {
           a.ws_ml[(slot * 2) * HEADS + h] = l > 0.f ? m_used : -CUDART_INF_F;
           a.ws_ml[(slot * 2 + 1) * HEADS + h] = l;
@@ -812,8 +872,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
 // ------------------------------------------------------------------ combine
 // grid (n_q, RANK / CDIMS); 128 threads = heads; thread h merges dims
-// [d0, d0 + CDIMS) of head h over the row's pieces.  Partials are heads
-// contiguous, so every load instruction of a warp reads one 128-byte line.
+// [d0, d0 + CDIMS) of head h over the row's pieces.  Partials are stored as
+// [slot][RANK/8][H][8], so a warp's 32-byte loads per piece read 1 KB.
 constexpr int CDIMS = 8;
 
 __global__ void __launch_bounds__(128) tc_combine_kernel(const __grid_constant__ TcDecodeArgs a) {
@@ -827,6 +887,7 @@ __global__ void __launch_bounds__(128) tc_combine_kernel(const __grid_constant__
 #pragma unroll
   for (int j = 0; j < CDIMS; ++j) acc[j] = 0.f;
   float M = -CUDART_INF_F, L = 0.f;
+  static_assert(CDIMS == 8, "one 8-dim group of the partial layout per thread");
   bool write = true;
   if (a.keys[n] != 0) {
     const int per = group_span(a, a.prefix[a.n_units]);
@@ -849,8 +910,7 @@ __global__ void __launch_bounds__(128) tc_combine_kernel(const __grid_constant__
               wc[q] = exp2f(mc - M);
               L += wc[q] * a.ws_ml[(sl * 2 + 1) * HEADS + h];
             }
-#pragma unroll
-            for (int j = 0; j < CDIMS; ++j) x[q][j] = a.ws_o[(sl * RANK + d0 + j) * HEADS + h];
+            ld_global_v8(a.ws_o + ((sl * (RANK / 8) + d0 / 8) * HEADS + h) * 8, x[q]);
           }
         }
 #pragma unroll
@@ -936,6 +996,7 @@ cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* works
   a.n_units = n_q / a.width;
   a.min_tiles = kMinTilesPerGroup;
   a.batch_in_map = (g.latent_batch_stride != 0 || g.rope_batch_stride != 0) ? 1 : 0;
+  a.plan_in_kernel = n_q <= kMaxRowsInKernelPlan ? 1 : 0;
 
   // Tensor maps over [B_buf, t_max, dims] (the batch axis has extent 1 for a
   // packed-flat cache whose batch stride is 0).
@@ -980,8 +1041,11 @@ cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* works
     cudaFuncSetAttribute(tc_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     attr = true;
   }
-  cudaError_t e = launch_pdl(tc_plan_kernel, dim3(1), dim3(1024), 0, stream, a);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (!a.plan_in_kernel) {
+    e = launch_pdl(tc_plan_kernel, dim3(1), dim3(1024), 0, stream, a);
+    if (e != cudaSuccess) return e;
+  }
   e = launch_pdl(tc_decode_kernel, dim3(2 * nclusters), dim3(THREADS), SMEM_BYTES, stream, lat_map, rope_map,
                  lat_rows_map, rope_rows_map, a);
   if (e != cudaSuccess) return e;

@@ -101,11 +101,12 @@ class DecodeStep:
         return 3 + self.attend_launches()
 
     def attend_launches(self) -> int:
-        """Tensor-core decode: planner + decode + combine.  CUDA-core decode:
-        the decode kernel, plus a combine when it splits the keys."""
+        """Tensor-core decode: decode + combine (+ a planner launch above 128
+        query rows).  CUDA-core decode: the decode kernel, plus a combine when
+        it splits the keys."""
         w = self.w
         if mla.decode_kernel_kind(w.heads, w.rank, w.rope, self.dtype, self.dtype) == 1:
-            return 3
+            return 2 if self.n_q <= 128 else 3
         k_max = self.sel.shape[1] if self.sel is not None else 0
         nbytes = mla.decode_workspace_size(w.batch, w.s_q, w.heads, w.rank, w.rope,
                                            self.latent.shape[1], k_max, self.sel is not None,
