@@ -232,6 +232,9 @@ def ours(args):
     # (planner + decode + combine) to time the dominant kernel without host gaps.
     for s in steps:
         s.run()
+        if s.fused:      # the decode-only graphs read the absorbed query of the separate entry points
+            s.rope_q()
+            s.absorb()
     torch.cuda.synchronize()
     g_step, g_att = [], []
     cap = torch.cuda.Stream()

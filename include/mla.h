@@ -214,12 +214,53 @@ int mla_decode_kernel_kind(int32_t heads, int32_t rank, int32_t rope_dim, int dt
  * ctx[n, h, c] sits at ctx + n*ctx_row_stride + h*ctx_head_stride + c.  The
  * output stops before o_proj.  fp32 accumulation.  ctx and kv_b_proj have
  * `dtype`; out has out_dtype.  bf16 inputs with rank = 512, v_dim = 128,
- * n_q <= 256 and 16-byte aligned pointers/strides run on the tensor cores.
+ * n_q <= 64 and 16-byte aligned pointers/strides run on the tensor cores.
  */
 int mla_project_v(const void* ctx, int64_t ctx_row_stride, int64_t ctx_head_stride,
                   const void* kv_b_proj, int dtype, void* out, int64_t out_row_stride,
                   int out_dtype, int32_t n_q, int32_t heads, int32_t nope, int32_t v_dim,
                   int32_t rank, mla_stream_t stream);
+
+/*
+ * One whole decode step of the attention layer in three launches: the four
+ * operations above composed as the MLA page's attendAbsorbed composes them,
+ * with RoPE folded into the absorb launch and the split combine folded into
+ * the W_UV projection launch.
+ *
+ * Inputs: q_nope[n*q_nope_row_stride + h*q_nope_head_stride + 0:nope] and the
+ * raw (pair-interleaved, unrotated) q_rope[n*q_rope_row_stride +
+ * h*q_rope_head_stride + 0:rope_dim] of query row n = b*s_q + i, rotated at
+ * position offset_b + i (offset_b = q_row_offsets[b], device, or
+ * q_position_offset when q_row_offsets is NULL) with base `theta`, as
+ * mla_rope_partial_interleaved does; kv_b_proj, the cache, the windows and
+ * the selection exactly as mla_absorb_q and mla_decode_attend take them.
+ * Output: out[n*out_row_stride + h*v_dim + j] as mla_project_v writes it, in
+ * out_dtype, and lse_out[n*heads + h] as mla_decode_attend writes it (may be
+ * NULL).  The absorbed query and the context stay in `workspace`, which must
+ * hold mla_decode_step_workspace_size(...) bytes (256-byte aligned).
+ * Served: bf16 with heads 128, nope 128, v_dim 128, rank 512, rope_dim 64 and
+ * at most 64 query rows (16-byte aligned q_nope, q_rope, kv_b_proj and cache;
+ * q_nope and cache strides multiples of 16 bytes); other requests return
+ * MLA_ERR_UNSUPPORTED and launch nothing -- compose the four entry points.
+ * Device-side checks and status bits are those of mla_decode_attend.
+ */
+int mla_decode_step(const void* q_nope, int64_t q_nope_row_stride, int64_t q_nope_head_stride,
+                    const void* q_rope, int64_t q_rope_row_stride, int64_t q_rope_head_stride,
+                    const int32_t* q_row_offsets, int64_t q_position_offset, float theta,
+                    const void* kv_b_proj, const void* latent, int64_t latent_row_stride,
+                    int64_t latent_batch_stride, const void* rope, int64_t rope_row_stride,
+                    int64_t rope_batch_stride, int dtype, const int32_t* kv_start, const int32_t* kv_len,
+                    int32_t batch, int32_t s_q, int32_t heads, int32_t nope, int32_t v_dim, int32_t rank,
+                    int32_t rope_dim, int64_t t_max, const int32_t* selected_positions,
+                    const int32_t* selected_counts, int32_t k_max, float softmax_scale, void* out,
+                    int64_t out_row_stride, int out_dtype, float* lse_out, void* workspace,
+                    size_t workspace_bytes, int32_t* device_status, mla_stream_t stream);
+
+/* Workspace bytes mla_decode_step needs (0 if the request is invalid or not
+ * served by the fused step). */
+size_t mla_decode_step_workspace_size(int32_t batch, int32_t s_q, int32_t heads, int32_t nope, int32_t v_dim,
+                                      int32_t rank, int32_t rope_dim, int64_t t_max, int32_t k_max,
+                                      int selected, int dtype);
 
 /*
  * Test hook: the selected-position gather of attendAbsorbed (takeAxis on

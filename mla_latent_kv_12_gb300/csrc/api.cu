@@ -41,6 +41,15 @@ void set_error_detail(const char* fmt, ...) {
   va_end(ap);
 }
 
+void rope_inverse_frequencies(float theta, int rotary_dims, float* inv_freq) {
+  // The page's f32 roundings: exponent f32(f32(-2j)/d), invf f32(pow(f32 theta, exponent)).
+  const double theta32 = (double)(float)theta;
+  for (int j = 0; j < rotary_dims / 2; ++j) {
+    const float exponent = (float)((double)(float)(-2.0 * j) / (double)rotary_dims);
+    inv_freq[j] = (float)pow(theta32, (double)exponent);
+  }
+}
+
 int device_sm_count() {
   static int cache[64] = {0};
   int dev = 0;
@@ -115,12 +124,7 @@ int mla_rope_partial_interleaved(const void* in, void* out, int dtype, int64_t r
   p.rotary_dims = rotary_dims;
   p.row_offsets = row_offsets;
   p.position_offset = position_offset;
-  // The page's f32 roundings: exponent f32(f32(-2j)/d), invf f32(pow(f32 theta, exponent)).
-  const double theta32 = (double)(float)theta;
-  for (int j = 0; j < rotary_dims / 2; ++j) {
-    const float exponent = (float)((double)(float)(-2.0 * j) / (double)rotary_dims);
-    p.inv_freq[j] = (float)pow(theta32, (double)exponent);
-  }
+  rope_inverse_frequencies(theta, rotary_dims, p.inv_freq);
   return cuda_status(launch_rope(p, dtype, (cudaStream_t)stream), "rope launch");
 }
 
@@ -275,6 +279,100 @@ int mla_decode_attend(const void* q, int64_t q_row_stride, int64_t q_head_stride
   return cuda_status(launch_simt_decode(g, dtype, out_dtype, workspace, workspace_bytes,
                                         (cudaStream_t)stream),
                      "decode launch");
+}
+
+static size_t step_q_bytes(int32_t n_q) { return ((size_t)n_q * 128 * 576 * 2 + 255) & ~(size_t)255; }
+static size_t step_ctx_bytes(int32_t n_q) { return ((size_t)n_q * 128 * 512 * 2 + 255) & ~(size_t)255; }
+static bool step_shape(int dtype, int32_t heads, int32_t nope, int32_t v_dim, int32_t rank, int32_t rope_dim,
+                       int64_t n_q) {
+  return dtype == MLA_DTYPE_BF16 && heads == 128 && nope == 128 && v_dim == 128 && rank == 512 &&
+         rope_dim == 64 && n_q > 0 && n_q <= 64;
+}
+
+size_t mla_decode_step_workspace_size(int32_t batch, int32_t s_q, int32_t heads, int32_t nope, int32_t v_dim,
+                                      int32_t rank, int32_t rope_dim, int64_t t_max, int32_t k_max,
+                                      int selected, int dtype) {
+  if (batch <= 0 || s_q <= 0 || t_max <= 0 || (selected && k_max <= 0) ||
+      !step_shape(dtype, heads, nope, v_dim, rank, rope_dim, (int64_t)batch * s_q))
+    return 0;
+  const int32_t n_q = batch * s_q;
+  return step_q_bytes(n_q) + step_ctx_bytes(n_q) +
+         ((tc_decode_workspace(n_q, heads, rank) + 255) & ~(size_t)255);
+}
+
+int mla_decode_step(const void* q_nope, int64_t q_nope_row_stride, int64_t q_nope_head_stride,
+                    const void* q_rope, int64_t q_rope_row_stride, int64_t q_rope_head_stride,
+                    const int32_t* q_row_offsets, int64_t q_position_offset, float theta,
+                    const void* kv_b_proj, const void* latent, int64_t latent_row_stride,
+                    int64_t latent_batch_stride, const void* rope, int64_t rope_row_stride,
+                    int64_t rope_batch_stride, int dtype, const int32_t* kv_start, const int32_t* kv_len,
+                    int32_t batch, int32_t s_q, int32_t heads, int32_t nope, int32_t v_dim, int32_t rank,
+                    int32_t rope_dim, int64_t t_max, const int32_t* selected_positions,
+                    const int32_t* selected_counts, int32_t k_max, float softmax_scale, void* out,
+                    int64_t out_row_stride, int out_dtype, float* lse_out, void* workspace,
+                    size_t workspace_bytes, int32_t* device_status, mla_stream_t stream) {
+  g_detail[0] = 0;
+  MLA_CHECK(q_nope && q_rope && kv_b_proj && out && workspace, "decode_step: NULL pointer");
+  MLA_CHECK(valid_dtype(dtype) && valid_dtype(out_dtype), "decode_step: bad dtype");
+  MLA_CHECK(batch > 0 && s_q > 0 && heads > 0 && nope > 0 && v_dim > 0 && rank > 0 && rope_dim > 0,
+            "decode_step: sizes must be positive");
+  MLA_CHECK(isfinite(theta) && theta > 0.f, "decode_step: theta must be positive and finite");
+  MLA_CHECK(q_row_offsets || q_position_offset >= 0, "decode_step: position offset must be non-negative");
+  const int64_t n_q = (int64_t)batch * s_q;
+  if (!step_shape(dtype, heads, nope, v_dim, rank, rope_dim, n_q))
+    return fail(MLA_ERR_UNSUPPORTED,
+                "decode_step: the fused step serves bf16, heads 128, nope 128, v 128, rank 512, rope 64 and at "
+                "most 64 query rows; compose the four entry points for other requests");
+  MLA_CHECK(aligned16(q_nope) && aligned16(q_rope) && aligned16(kv_b_proj) && aligned16(latent) &&
+                aligned16(rope),
+            "decode_step: q_nope, q_rope, kv_b_proj, latent and rope must be 16-byte aligned");
+  MLA_CHECK(q_nope_head_stride >= nope && q_nope_row_stride >= 0 && q_nope_head_stride % 8 == 0 &&
+                q_nope_row_stride % 8 == 0,
+            "decode_step: q_nope strides must cover nope and be multiples of 16 bytes");
+  MLA_CHECK(q_rope_head_stride >= rope_dim && q_rope_row_stride >= 0 && q_rope_head_stride % 2 == 0 &&
+                q_rope_row_stride % 2 == 0,
+            "decode_step: q_rope strides must cover rope_dim and be even");
+  MLA_CHECK(out_row_stride >= (int64_t)heads * v_dim, "decode_step: out_row_stride < heads * v_dim");
+  MLA_CHECK(latent_row_stride % 8 == 0 && latent_batch_stride % 8 == 0 && rope_row_stride % 8 == 0 &&
+                rope_batch_stride % 8 == 0,
+            "decode_step: cache strides must be multiples of 16 bytes");
+  MLA_CHECK((latent_batch_stride == 0) == (rope_batch_stride == 0),
+            "decode_step: latent and rope batch strides must both be zero (packed rows) or both non-zero");
+  const size_t need = mla_decode_step_workspace_size(batch, s_q, heads, nope, v_dim, rank, rope_dim, t_max, k_max,
+                                                     selected_positions != nullptr, dtype);
+  MLA_CHECK(need > 0 && workspace_bytes >= need, "decode_step: workspace of %zu bytes < %zu needed",
+            workspace_bytes, need);
+  MLA_CHECK((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0,
+            "decode_step: workspace must be 256-byte aligned");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* qbuf = ws;
+  void* ctxbuf = ws + step_q_bytes((int32_t)n_q);
+  uint8_t* dws = ws + step_q_bytes((int32_t)n_q) + step_ctx_bytes((int32_t)n_q);
+  const size_t dws_bytes = workspace_bytes - (size_t)(dws - ws);
+  const int64_t D = rank + rope_dim;
+  DecodeGeometry g;
+  int st = decode_geometry(g, qbuf, heads * D, D, latent, latent_row_stride, latent_batch_stride, rope,
+                           rope_row_stride, rope_batch_stride, dtype, kv_start, kv_len, batch, s_q, heads, rank,
+                           rope_dim, t_max, selected_positions, selected_counts, k_max, softmax_scale, ctxbuf,
+                           (int64_t)heads * rank, rank, lse_out, device_status, true);
+  if (st != MLA_OK) return st;
+  AbsorbParams ap{q_nope, q_nope_row_stride, q_nope_head_stride, kv_b_proj, qbuf, heads * D, D,
+                  (int32_t)n_q, heads, nope, v_dim, rank};
+  AbsorbRope rp;
+  memset(&rp, 0, sizeof(rp));
+  rp.q_rope = q_rope;
+  rp.row_stride = q_rope_row_stride;
+  rp.head_stride = q_rope_head_stride;
+  rp.s_q = s_q;
+  rp.row_offsets = q_row_offsets;
+  rp.position_offset = q_position_offset;
+  rp.out_col = rank;
+  rope_inverse_frequencies(theta, rope_dim, rp.inv_freq);
+  st = cuda_status(launch_tc_absorb(ap, (cudaStream_t)stream, &rp), "decode_step: absorb + rope launch");
+  if (st != MLA_OK) return st;
+  DecodeTail tail{kv_b_proj, out, out_row_stride, out_dtype, heads, nope, v_dim, rank};
+  return cuda_status(launch_tc_decode(g, MLA_DTYPE_BF16, dws, dws_bytes, (cudaStream_t)stream, &tail),
+                     "decode_step: decode + combine/projection launch");
 }
 
 int mla_project_v(const void* ctx, int64_t ctx_row_stride, int64_t ctx_head_stride,

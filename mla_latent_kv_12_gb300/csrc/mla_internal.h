@@ -53,10 +53,19 @@ size_t simt_decode_workspace(const DecodeGeometry& g, int* splits_out);
 cudaError_t launch_simt_decode(const DecodeGeometry& g, int dtype, int out_dtype, void* workspace,
                                size_t workspace_bytes, cudaStream_t stream);
 
-// Tensor-core decode (bf16, heads 128, rank 512, rope 64).
+// Tensor-core decode (bf16, heads 128, rank 512, rope 64).  With a tail, the
+// split combine is fused with the W_UV projection (bf16 context in
+// g.ctx_out, n_q <= 64, v_dim 128) and `tail->out` receives [n_q, H*v].
+struct DecodeTail {
+  const void* w;  // kv_b_proj [heads*(nope+v_dim), rank] bf16
+  void* out;
+  int64_t out_row_stride;
+  int out_dtype;
+  int32_t heads, nope, v_dim, rank;
+};
 size_t tc_decode_workspace(int32_t n_q, int32_t heads, int32_t rank);
 cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* workspace,
-                             size_t workspace_bytes, cudaStream_t stream);
+                             size_t workspace_bytes, cudaStream_t stream, const DecodeTail* tail = nullptr);
 
 struct AbsorbParams {
   const void* q_nope;
@@ -66,8 +75,25 @@ struct AbsorbParams {
   int64_t out_row_stride, out_head_stride;
   int32_t n_q, heads, nope, v_dim, rank;
 };
+// RoPE of the query's rope part folded into the tensor-core absorb launch
+// (bf16, 64 rotary dims = the whole rope part): q_rope[n, h, 0:64] enters
+// pair-interleaved and leaves rotated at q_out[n, h, out_col : out_col+64].
+// Position of query row n = b*s_q + i is offset_b + i.
+struct AbsorbRope {
+  const void* q_rope;
+  int64_t row_stride, head_stride;
+  int32_t s_q;
+  const int32_t* row_offsets;  // device [batch] or NULL
+  int64_t position_offset;     // used when row_offsets is NULL
+  int32_t out_col;
+  float inv_freq[32];
+};
+// The page's f32 roundings of the inverse frequencies:
+// invf_j = f32(pow(f32 theta, f32(f32(-2j) / d))).
+void rope_inverse_frequencies(float theta, int rotary_dims, float* inv_freq);
+
 cudaError_t launch_simt_absorb(const AbsorbParams& p, int dtype, cudaStream_t stream);
-cudaError_t launch_tc_absorb(const AbsorbParams& p, cudaStream_t stream);
+cudaError_t launch_tc_absorb(const AbsorbParams& p, cudaStream_t stream, const AbsorbRope* rope = nullptr);
 
 struct ProjectParams {
   const void* ctx;

@@ -2,12 +2,11 @@
 //
 // One warp per feature vector (r, t, i): every lane first reads its pairs and
 // tail elements into registers, the warp synchronises, then writes -- so the
-// call may run in place.  The angle is f32(p * invf_j), formed exactly in
-// double and rounded once (the page forms it in f64 and rounds with fround);
-// sin/cos are CUDA's accurate sincosf of that f32 angle.
+// call may run in place.  The per-pair arithmetic is rope_rotate_pair.
 #include <cuda_bf16.h>
 
 #include "mla_internal.h"
+#include "rope_math.cuh"
 #include "tc_host.h"
 
 namespace mla {
@@ -58,13 +57,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) rope_kernel(const __grid_
     re[k] = 0.f;
     im[k] = 0.f;
     if (j < half) {
-      const float a = load_f(src + 2 * j);
-      const float b = load_f(src + 2 * j + 1);
-      const float ang = __double2float_rn((double)pos * (double)p.inv_freq[j]);
-      float s, c;
-      sincosf(ang, &s, &c);
-      re[k] = a * c - b * s;
-      im[k] = b * c + a * s;
+      rope_rotate_pair(load_f(src + 2 * j), load_f(src + 2 * j + 1), pos, p.inv_freq[j], re[k], im[k]);
     }
   }
   const int tail = (int)(p.width - p.rotary_dims);

@@ -768,13 +768,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         if (aborted()) break;
         tc_fence_after();
-        if (rescale) {
+        // tcgen05.ld / st are warp-collective: the whole warp takes the
+        // rescale pass when any of its heads needs it, the others with factor 1.
+        if (__any_sync(0xffffffffu, rescale)) {
+          const float f = rescale ? alpha : 1.f;
           for (int c = 0; c < DV / 32; ++c) {
             uint32_t o[32];
             tmem_ld32(tmem + TM_O + c * 32 + lane_off, o);
-            tmem_wait_ld();
+            tmem_wait_ld_regs(o);
 #pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
             tmem_st32(tmem + TM_O + c * 32 + lane_off, o);
           }
         }
@@ -938,6 +941,181 @@ __global__ void __launch_bounds__(128) tc_combine_kernel(const __grid_constant__
   }
 }
 
+// ------------------------------------------------------------------ combine + W_UV projection
+// The fused tail of a decode step: grid (heads), 128 threads.  CTA h merges
+// the split partials of head h for every query row into the bf16 context rows
+// (the rows finished in place are read back from the context buffer), lays
+// them out as the K-major B operand [npad rows x 512] of a tcgen05 MMA in
+// shared memory, and multiplies by W_UV_h [128 x 512] (A, TMA-loaded) into
+// out[n, h*128 + j] -- the same contraction as mla_project_v.
+struct ProjectTail {
+  void* out;
+  int64_t out_row_stride;
+  int32_t out_f32;
+  int32_t npad;               // n_q rounded up to 16 (the MMA's N)
+  int32_t v_dim;
+  int32_t w_row0, w_head_rows;  // W_UV_h starts at row h*w_head_rows + w_row0
+};
+
+constexpr int PROJ_THREADS = 128;
+constexpr int PROJ_BOX_BYTES = 128 * 128;                  // [128 v rows][64 dims] bf16
+constexpr int PROJ_SMEM_MAX = 1024 + 8 * PROJ_BOX_BYTES + 8 * 64 * 128;
+
+__global__ void __launch_bounds__(PROJ_THREADS) tc_combine_project_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                                          const __grid_constant__ TcDecodeArgs a,
+                                                                          const __grid_constant__ ProjectTail p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;                       // 8 K-boxes of W_UV_h
+  uint8_t* sB = smem + 8 * PROJ_BOX_BYTES;  // 8 K-boxes of [npad rows][64 dims] context
+  __shared__ __align__(8) uint64_t bar_full[8];
+  __shared__ __align__(8) uint64_t bar_mma;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int mma_ok_s;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x;
+  const int npad = p.npad;
+  const uint32_t ncols = npad <= 32 ? 32 : 64;
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&wmap);
+    for (int i = 0; i < 8; ++i) mbar_init(&bar_full[i], 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_base_s, ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  // W_UV_h is not written by the decode kernel this one depends on, and every
+  // launch before that kernel has completed by the time this grid starts (each
+  // launch of the step lets its dependants start only after its own wait), so
+  // the weight loads are issued before the wait and overlap the decode's tail.
+  if (threadIdx.x == 0) {
+    const int row0 = h * p.w_head_rows + p.w_row0;
+    for (int i = 0; i < 8; ++i) {
+      mbar_arrive_expect_tx(&bar_full[i], PROJ_BOX_BYTES);
+      tma_load_2d(sA + i * PROJ_BOX_BYTES, &wmap, &bar_full[i], 64 * i, row0);
+    }
+  }
+  pdl_wait();
+
+  // ---- context rows of head h into sB (bf16, 128-byte swizzle: the 16-byte
+  // chunk c of row n sits at chunk c ^ (n & 7)); thread = (row parity, 8-dim group)
+  {
+    const int g = threadIdx.x & 63;
+    const int total = a.prefix[a.n_units];
+    const int per = group_span(a, total);
+    for (int n = threadIdx.x >> 6; n < npad; n += 2) {
+      uint4 packed = make_uint4(0, 0, 0, 0);
+      if (n < a.n_q && a.keys[n] != 0) {
+        const int u = n / a.width, member = n % a.width;
+        const int rs = a.prefix[u], re = a.prefix[u + 1];
+        const int c0 = rs / per, c1 = (re - 1) / per;
+        if (c0 == c1) {
+          // finished in place by its group: bf16 context (and lse) already written
+          packed = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.ctx) +
+                                                   (int64_t)n * a.ctx_row_stride + (int64_t)h * a.ctx_head_stride +
+                                                   8 * g);
+        } else {
+          auto slot_of = [&](int c) -> int64_t { return ((int64_t)u + c) * a.width + member; };
+          float M = -CUDART_INF_F, L = 0.f;
+          for (int c = c0; c <= c1; ++c) M = fmaxf(M, a.ws_ml[(slot_of(c) * 2) * HEADS + h]);
+          float acc[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+          for (int c = c0; c <= c1; c += 4) {
+            float wc[4], x[4][8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              wc[q] = 0.f;
+              if (c + q <= c1) {
+                const int64_t sl = slot_of(c + q);
+                const float mc = a.ws_ml[(sl * 2) * HEADS + h];
+                if (mc != -CUDART_INF_F) {
+                  wc[q] = exp2f(mc - M);
+                  L += wc[q] * a.ws_ml[(sl * 2 + 1) * HEADS + h];
+                }
+                ld_global_v8(a.ws_o + ((sl * (RANK / 8) + g) * HEADS + h) * 8, x[q]);
+              }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+              for (int j = 0; j < 8; ++j) acc[j] = (wc[q] != 0.f) ? fmaf(wc[q], x[q][j], acc[j]) : acc[j];
+          }
+          const float inv = L > 0.f ? 1.f / L : 0.f;
+          packed = make_uint4(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv),
+                              pack_bf16x2(acc[4] * inv, acc[5] * inv), pack_bf16x2(acc[6] * inv, acc[7] * inv));
+          if (g == 0 && a.lse)
+            a.lse[(int64_t)n * HEADS + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -CUDART_INF_F;
+        }
+      } else if (n < a.n_q && g == 0 && a.lse) {
+        a.lse[(int64_t)n * HEADS + h] = -CUDART_INF_F;   // no visible key: ctx 0, lse -inf
+      }
+      *reinterpret_cast<uint4*>(sB + (g >> 3) * (npad * 128) + n * 128 + (((g & 7) ^ (n & 7)) << 4)) = packed;
+    }
+  }
+  fence_proxy_async_smem();   // generic-proxy writes of sB, read by the MMA
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  bool ok = true;
+  if (threadIdx.x == 0) {
+    const uint32_t idesc = idesc_bf16_f32(128, npad, 0, 0);
+    const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+    for (int i = 0; i < 8 && ok; ++i) {
+      ok = mbar_wait(&bar_full[i], 0, kWaitLimit);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint64_t ad = smem_desc(a0 + i * PROJ_BOX_BYTES + k * 32, 16, 1024, kSwizzle128B);
+        const uint64_t bd = smem_desc(b0 + i * npad * 128 + k * 32, 16, 1024, kSwizzle128B);
+        mma_ss(tmem, ad, bd, idesc, (i | k) != 0);
+      }
+    }
+    if (!ok) {
+      if (a.status) atomicOr(a.status, MLA_DEVICE_TIMEOUT);
+      for (int i = 0; i < 8; ++i) mbar_wait(&bar_full[i], 0, kWaitLimit);  // drain in-flight copies
+    }
+    mma_ok_s = ok ? 1 : 0;
+    mma_commit(&bar_mma);
+  }
+  __syncthreads();
+  ok = mbar_wait_warp(&bar_mma, 0, kWaitLimit) && mma_ok_s != 0;
+  tc_fence_after();
+  if (ok) {
+    const uint32_t row_addr = tmem + ((uint32_t)(32 * warp) << 16);
+    const int j = 32 * warp + lane;
+    for (int c0 = 0; c0 < npad; c0 += 16) {
+      uint32_t r[16];
+      tmem_ld16(row_addr + c0, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const int n = c0 + t;
+        if (n >= a.n_q) continue;
+        const float v = __uint_as_float(r[t]);
+        const int64_t off = (int64_t)n * p.out_row_stride + (int64_t)h * p.v_dim + j;
+        if (p.out_f32)
+          static_cast<float*>(p.out)[off] = v;
+        else
+          static_cast<__nv_bfloat16*>(p.out)[off] = __float2bfloat16_rn(v);
+      }
+    }
+  }
+  pdl_trigger();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, ncols);
+}
+
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
@@ -951,7 +1129,7 @@ size_t tc_decode_workspace(int32_t n_q, int32_t heads, int32_t rank) {
 }
 
 cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* workspace, size_t workspace_bytes,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, const DecodeTail* tail) {
   const int n_q = g.batch * g.s_q;
   const int nclusters = tc_decode_clusters();
   if (workspace_bytes < tc_decode_workspace(n_q, g.heads, g.rank)) return cudaErrorInvalidValue;
@@ -1049,7 +1227,34 @@ cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* works
   e = launch_pdl(tc_decode_kernel, dim3(2 * nclusters), dim3(THREADS), SMEM_BYTES, stream, lat_map, rope_map,
                  lat_rows_map, rope_rows_map, a);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(tc_combine_kernel, dim3(n_q, RANK / CDIMS), dim3(HEADS), 0, stream, a);
+  if (tail == nullptr) {
+    e = launch_pdl(tc_combine_kernel, dim3(n_q, RANK / CDIMS), dim3(HEADS), 0, stream, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
+  // Fused tail: combine + W_UV projection (bf16 context, n_q <= 64).
+  CUtensorMap wmap;
+  {
+    const uint64_t dims[2] = {(uint64_t)tail->rank, (uint64_t)tail->heads * (tail->nope + tail->v_dim)};
+    const uint64_t strides[1] = {(uint64_t)tail->rank * 2};
+    const uint32_t box[2] = {64, 128};
+    if (!encode_tmap_bf16(&wmap, tail->w, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  ProjectTail p;
+  p.out = tail->out;
+  p.out_row_stride = tail->out_row_stride;
+  p.out_f32 = tail->out_dtype == MLA_DTYPE_F32 ? 1 : 0;
+  p.npad = (n_q + 15) & ~15;
+  p.v_dim = tail->v_dim;
+  p.w_row0 = tail->nope;
+  p.w_head_rows = tail->nope + tail->v_dim;
+  static bool attr_tail = false;
+  if (!attr_tail) {
+    cudaFuncSetAttribute(tc_combine_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PROJ_SMEM_MAX);
+    attr_tail = true;
+  }
+  const size_t smem = 1024 + 8 * PROJ_BOX_BYTES + 8 * (size_t)p.npad * 128;
+  e = launch_pdl(tc_combine_project_kernel, dim3(tail->heads), dim3(PROJ_THREADS), smem, stream, wmap, a, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

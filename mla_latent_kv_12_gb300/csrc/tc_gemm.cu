@@ -9,8 +9,10 @@
 // (swap-AB), so the few query rows become the N dimension (padded to 16).
 // Accumulation is f32 in TMEM; one warp quarter reads back 32 rows each.
 #include <cuda_bf16.h>
+#include <string.h>
 
 #include "mla_internal.h"
+#include "rope_math.cuh"
 #include "tc_common.cuh"
 #include "tc_host.h"
 
@@ -35,6 +37,8 @@ struct AbsorbArgs {
   int32_t n_q, npad;
   int32_t w_head_rows;  // W_UK_h starts at row h*w_head_rows
   int32_t* status;
+  int32_t with_rope;    // CTAs of blockIdx.x == 0 also rotate q_rope of head h
+  AbsorbRope rope;
 };
 
 __global__ void __launch_bounds__(128) tc_absorb_kernel(const __grid_constant__ CUtensorMap wmap,
@@ -94,7 +98,25 @@ __global__ void __launch_bounds__(128) tc_absorb_kernel(const __grid_constant__ 
     }
   }
   __syncwarp();
-  ok = mbar_wait(&bar_mma, 0, kWaitLimit);
+  if (a.with_rope && blockIdx.x == 0) {
+    // While the MMAs run: RoPE of head h's rope part, lane j = rotary pair j,
+    // warp w = query rows w, w+4, ...
+    const AbsorbRope& r = a.rope;
+    for (int n = warp; n < a.n_q; n += 4) {
+      const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(r.q_rope) + (int64_t)n * r.row_stride +
+                                 (int64_t)h * r.head_stride;
+      const __nv_bfloat162 ab = reinterpret_cast<const __nv_bfloat162*>(src)[lane];
+      const int b = n / r.s_q, i = n % r.s_q;
+      const int64_t pos = (r.row_offsets ? (int64_t)r.row_offsets[b] : r.position_offset) + i;
+      float re, im;
+      rope_rotate_pair(__low2float(ab), __high2float(ab), pos, r.inv_freq[lane], re, im);
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + (int64_t)n * a.out_row_stride +
+                           (int64_t)h * a.out_head_stride + r.out_col;
+      dst[lane] = __float2bfloat16_rn(re);
+      dst[32 + lane] = __float2bfloat16_rn(im);
+    }
+  }
+  ok = mbar_wait_warp(&bar_mma, 0, kWaitLimit);   // warp-uniform: the epilogue's TMEM loads are collective
   if (!ok && lane == 0) flag_timeout(a.status);
   tc_fence_after();
   if (ok) {
@@ -190,7 +212,9 @@ __global__ void __launch_bounds__(128) tc_project_kernel(const __grid_constant__
     mma_commit(&bar_mma);
   }
   __syncwarp();
-  ok = mbar_wait(&bar_mma, 0, kWaitLimit) && ok;
+  // warp-uniform (the epilogue's TMEM loads are collective); thread 0's own
+  // result joins through the barrier wait of warp 0
+  ok = __all_sync(0xffffffffu, mbar_wait(&bar_mma, 0, kWaitLimit) && ok);
   tc_fence_after();
   if (ok) {
     const uint32_t row_addr = tmem + ((uint32_t)(32 * warp) << 16);
@@ -222,7 +246,7 @@ int pad16(int n) { return (n + 15) & ~15; }
 
 }  // namespace
 
-cudaError_t launch_tc_absorb(const AbsorbParams& p, cudaStream_t stream) {
+cudaError_t launch_tc_absorb(const AbsorbParams& p, cudaStream_t stream, const AbsorbRope* rope) {
   const int npad = pad16(p.n_q);
   CUtensorMap wmap, qmap;
   {
@@ -237,7 +261,18 @@ cudaError_t launch_tc_absorb(const AbsorbParams& p, cudaStream_t stream) {
     const uint32_t box[3] = {64, 1, (uint32_t)npad};
     if (!encode_tmap_bf16(&qmap, p.q_nope, 3, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  AbsorbArgs a{p.out, p.out_row_stride, p.out_head_stride, p.n_q, npad, p.nope + p.v_dim, nullptr};
+  AbsorbArgs a;
+  memset(&a, 0, sizeof(a));
+  a.out = p.out;
+  a.out_row_stride = p.out_row_stride;
+  a.out_head_stride = p.out_head_stride;
+  a.n_q = p.n_q;
+  a.npad = npad;
+  a.w_head_rows = p.nope + p.v_dim;
+  if (rope) {
+    a.with_rope = 1;
+    a.rope = *rope;
+  }
   const size_t smem = 1024 + 32768 + 2 * (size_t)npad * 128;
   static bool attr = false;
   if (!attr) {

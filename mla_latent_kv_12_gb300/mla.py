@@ -27,7 +27,8 @@ EXPORTS = (
     "mla_status_string", "mla_last_error_detail", "mla_version",
     "mla_rope_partial_interleaved", "mla_absorb_q", "mla_decode_attend",
     "mla_decode_workspace_size", "mla_decode_kernel_kind", "mla_project_v",
-    "mla_gather_selected", "mla_decode_attend_no_alloc",
+    "mla_gather_selected", "mla_decode_attend_no_alloc", "mla_decode_step",
+    "mla_decode_step_workspace_size",
 )
 
 
@@ -70,6 +71,13 @@ def _load() -> ctypes.CDLL:
     lib.mla_decode_attend_no_alloc.argtypes = [vp, i64, i64, vp, i64, i64, vp, i64, i64, ctypes.c_int, vp,
                                                vp, i32, i32, i32, i32, i32, i64, vp, vp, i32, f32, vp, i64,
                                                i64, ctypes.c_int, vp, vp, vp]
+    lib.mla_decode_step.restype = ctypes.c_int
+    lib.mla_decode_step.argtypes = [vp, i64, i64, vp, i64, i64, vp, i64, f32, vp, vp, i64, i64, vp, i64, i64,
+                                    ctypes.c_int, vp, vp, i32, i32, i32, i32, i32, i32, i32, i64, vp, vp, i32,
+                                    f32, vp, i64, ctypes.c_int, vp, vp, sz, vp, vp]
+    lib.mla_decode_step_workspace_size.restype = sz
+    lib.mla_decode_step_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i64, i32, ctypes.c_int,
+                                                   ctypes.c_int]
     lib.mla_gather_selected.restype = ctypes.c_int
     lib.mla_gather_selected.argtypes = [vp, i64, i64, vp, i64, i64, ctypes.c_int, vp, vp, i32, i32, i32,
                                         i32, i64, vp, vp, i32, vp, vp, vp]
@@ -176,6 +184,41 @@ def project_v(ctx: torch.Tensor, kv_b_proj: torch.Tensor, out: torch.Tensor, hea
     _check(lib.mla_project_v(_ptr(ctx), ctx.stride(0), ctx.stride(1), _ptr(kv_b_proj), _dt(ctx),
                              _ptr(out), out.stride(0), _dt(out), n_q, heads, nope, v_dim, rank,
                              _stream(stream)))
+    return out
+
+
+def decode_step_workspace_size(batch, s_q, heads, nope, v_dim, rank, rope_dim, t_max, k_max=0,
+                               selected=False, dtype=torch.bfloat16) -> int:
+    return lib.mla_decode_step_workspace_size(batch, s_q, heads, nope, v_dim, rank, rope_dim, t_max, k_max,
+                                              1 if selected else 0, _DT[dtype])
+
+
+def decode_step(q_nope: torch.Tensor, q_rope: torch.Tensor, theta: float, kv_b_proj: torch.Tensor,
+                latent: torch.Tensor, rope: torch.Tensor, kv_start, kv_len, batch: int, s_q: int, nope: int,
+                v_dim: int, softmax_scale: float, out: torch.Tensor, lse_out: Optional[torch.Tensor] = None,
+                row_offsets: Optional[torch.Tensor] = None, position_offset: int = 0,
+                sel: Optional[torch.Tensor] = None, sel_count: Optional[torch.Tensor] = None,
+                workspace: Optional[torch.Tensor] = None, device_status: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+    """Fused decode step.  ``q_nope`` ``[n_q, H, >=nope]`` and ``q_rope`` ``[n_q, H, >=rope]`` views
+    (raw, pair-interleaved); cache views as for ``decode_attend``; ``out`` ``[n_q, H*v]``."""
+    n_q, heads, _ = q_nope.shape
+    rank, rope_dim = latent.shape[-1], rope.shape[-1]
+    t_max = latent.shape[1]
+    lat_bs = latent.stride(0) if latent.shape[0] > 1 else 0
+    rope_bs = rope.stride(0) if rope.shape[0] > 1 else 0
+    k_max = sel.shape[1] if sel is not None else 0
+    if workspace is None:
+        nbytes = decode_step_workspace_size(batch, s_q, heads, nope, v_dim, rank, rope_dim, t_max, k_max,
+                                            sel is not None, latent.dtype)
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=latent.device)
+    _check(lib.mla_decode_step(
+        _ptr(q_nope), q_nope.stride(0), q_nope.stride(1), _ptr(q_rope), q_rope.stride(0), q_rope.stride(1),
+        _ptr(row_offsets), int(position_offset), float(theta), _ptr(kv_b_proj),
+        _ptr(latent), latent.stride(1), lat_bs, _ptr(rope), rope.stride(1), rope_bs, _dt(latent),
+        _ptr(kv_start), _ptr(kv_len), batch, s_q, heads, nope, v_dim, rank, rope_dim, t_max,
+        _ptr(sel), _ptr(sel_count), k_max, float(softmax_scale), _ptr(out), out.stride(0), _dt(out),
+        _ptr(lse_out), _ptr(workspace), workspace.numel(), _ptr(device_status), _stream(stream)))
     return out
 
 

@@ -4,8 +4,11 @@
 runs the hot path in order: RoPE of the new query's rope part (written into
 the packed query), absorption of ``q_nope`` through ``W_UK`` (into the same
 packed query), latent attention over the cache (split-K + combine), and the
-``W_UV`` projection.  Cache keys are rotated once at set-up with the same RoPE
-entry point (as an append would), at their positions ``0 .. kv_len-1``.
+``W_UV`` projection.  ``run`` takes the fused entry point (three launches)
+where it serves the shapes and the four entry points otherwise; the four
+methods stay callable one by one.  Cache keys are rotated once at set-up with
+the same RoPE entry point (as an append would), at their positions
+``0 .. kv_len-1``.
 """
 from __future__ import annotations
 
@@ -33,7 +36,7 @@ def rotate_cache_keys(inp: DecodeInputs, rope_raw_dev: torch.Tensor, rope_dev: t
 
 class DecodeStep:
     def __init__(self, inp: DecodeInputs, device="cuda", out_dtype: Optional[torch.dtype] = None,
-                 with_selection: bool = True):
+                 with_selection: bool = True, fused: bool = True):
         w = inp.w
         self.w, self.inp = w, inp
         dt = DTYPES[w.dtype]
@@ -68,6 +71,10 @@ class DecodeStep:
         self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.scale = mla.default_scale(w.nope, w.rope)
+        step_bytes = mla.decode_step_workspace_size(B, S, H, w.nope, w.v, w.rank, w.rope, self.latent.shape[1],
+                                                    k_max, self.sel is not None, dt)
+        self.fused = step_bytes > 0 and fused
+        self.step_workspace = (torch.empty(step_bytes, dtype=torch.uint8, device=dev) if self.fused else None)
 
     # The four steps; each is one (or two) kernel launches on the current stream.
     def rope_q(self, stream=None):
@@ -89,7 +96,18 @@ class DecodeStep:
         w = self.w
         mla.project_v(self.ctx, self.kv_b_proj, self.out, w.heads, w.nope, w.v, stream=stream)
 
+    def run_fused(self, stream=None) -> torch.Tensor:
+        w = self.w
+        mla.decode_step(self.q_nope, self.q_rope_raw.view(self.n_q, w.heads, w.rope), w.theta, self.kv_b_proj,
+                        self.latent, self.rope, self.kv_start, self.kv_len, w.batch, w.s_q, w.nope, w.v,
+                        self.scale, self.out, self.lse, row_offsets=self.q_offset, sel=self.sel,
+                        sel_count=self.sel_count, workspace=self.step_workspace, device_status=self.status,
+                        stream=stream)
+        return self.out
+
     def run(self, stream=None) -> torch.Tensor:
+        if self.fused:
+            return self.run_fused(stream)
         self.rope_q(stream)
         self.absorb(stream)
         self.attend(stream)
@@ -97,7 +115,11 @@ class DecodeStep:
         return self.out
 
     def launches_per_step(self) -> int:
-        """Kernels one ``run`` launches: RoPE, absorb, the decode launches, project."""
+        """Kernels one ``run`` launches: three for the fused step (absorb + RoPE,
+        decode, combine + projection); else RoPE, absorb, the decode launches,
+        project."""
+        if self.fused:
+            return 3
         return 3 + self.attend_launches()
 
     def attend_launches(self) -> int:

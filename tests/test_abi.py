@@ -84,3 +84,27 @@ def test_absorb_and_project_validation(lib):
     assert L.mla_project_v(16, 0, 512, 16, 1, 16, 100, 1, 1, 128, 128, 128, 512, None) == 1
     assert L.mla_gather_selected(16, 576, 0, 16, 576, 0, 1, None, 16, 1, 1, 512, 64, 100,
                                  16, None, 8, 16, None, None) == 1
+
+
+def test_decode_step_validation(lib):
+    L = lib.lib
+    # q_nope, strides, q_rope, strides, offsets, offset, theta, kv_b_proj, latent, strides, rope, strides,
+    # dtype, kv_start, kv_len, B, S, H, nope, v, rank, rope, T, sel, counts, k_max, scale, out, stride,
+    # out dtype, lse, workspace, bytes, status, stream
+    args = [16, 16384, 128, 16, 8192, 64, None, 0, 1e4, 16, 16, 512, 0, 16, 64, 0,
+            1, None, 16, 1, 1, 128, 128, 128, 512, 64, 4096, None, None, 0, 0.07, 16, 16384,
+            1, None, 256, 1 << 30, None, None]
+    bad = list(args); bad[0] = None                      # q_nope
+    assert L.mla_decode_step(*bad) == 1
+    bad = list(args); bad[8] = 0.0                       # theta
+    assert L.mla_decode_step(*bad) == 1
+    bad = list(args); bad[16] = 0                        # f32: not served by the fused step
+    assert L.mla_decode_step(*bad) == 2
+    assert "compose" in L.mla_last_error_detail().decode()
+    bad = list(args); bad[19] = 65                       # 65 query rows
+    assert L.mla_decode_step(*bad) == 2
+    bad = list(args); bad[36] = 1024                     # workspace too small
+    assert L.mla_decode_step(*bad) == 1
+    assert L.mla_decode_step_workspace_size(1, 1, 128, 128, 128, 512, 64, 4096, 0, 0, 1) > 0
+    assert L.mla_decode_step_workspace_size(1, 1, 64, 128, 128, 512, 64, 4096, 0, 0, 1) == 0
+    assert L.mla_decode_step_workspace_size(1, 1, 128, 128, 128, 512, 64, 4096, 0, 0, 0) == 0

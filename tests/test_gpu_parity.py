@@ -26,12 +26,20 @@ DEV = "cuda"
 
 
 def run_and_compare(inp, rows=None, heads=None, with_selection=True):
-    step = DecodeStep(inp, DEV, with_selection=with_selection)
+    """The four entry points one by one (every intermediate checked), then the
+    fused step where it serves the shapes (out and lse checked)."""
+    ref = H.oracle_reference(inp, rows, heads, with_selection)
+    step = DecodeStep(inp, DEV, with_selection=with_selection, fused=False)
     step.run()
     torch.cuda.synchronize()
-    ref = H.oracle_reference(inp, rows, heads, with_selection)
     res = H.compare_step(step, ref, inp.w.dtype)
     assert int(step.status.item()) == 0
+    fstep = DecodeStep(inp, DEV, with_selection=with_selection, fused=True)
+    if fstep.fused:
+        fstep.run()
+        torch.cuda.synchronize()
+        res["fused"] = H.compare_step(fstep, ref, inp.w.dtype)
+        assert int(fstep.status.item()) == 0
     return step, res
 
 
@@ -140,6 +148,58 @@ def test_verify_f32_tiny_causal():
     run_and_compare(inp)
 
 
+@pytest.mark.parametrize("batch", [1, 17, 64])
+def test_fused_step_row_counts(batch):
+    # 1, 17 and 64 query rows: N = 16, 32 and 64 in the fused projection MMA,
+    # rows finished in place and split rows mixed.
+    w = dataclasses.replace(W.DENSE_BF16, batch=batch, t=900 if batch > 1 else 4096)
+    inp = W.make_inputs(w)
+    rows = list(range(batch)) if batch <= 17 else [0, 1, 31, 62, 63]
+    ref = H.oracle_reference(inp, rows, [0, 5, 64, 127])
+    step = DecodeStep(inp, DEV, fused=True)
+    assert step.fused
+    step.run()
+    torch.cuda.synchronize()
+    H.compare_step(step, ref, "bf16")
+    assert int(step.status.item()) == 0
+
+
+def test_fused_step_refuses_unserved_shapes():
+    inp = W.make_inputs(W.TINY_F32)
+    step = DecodeStep(inp, DEV)
+    assert not step.fused                       # f32: composed from the four entry points
+    w = W.DENSE_BF16
+    assert mla.decode_step_workspace_size(65, 1, w.heads, w.nope, w.v, w.rank, w.rope, 4096) == 0
+    assert mla.decode_step_workspace_size(64, 1, w.heads, w.nope, w.v, w.rank, w.rope, 4096) > 0
+
+
+def test_decode_rescale_in_some_heads_only():
+    # Softmax scale 1 and a planted key aligned with head 5's query late in the
+    # window: head 5's running maximum jumps by far more than the lazy-rescale
+    # threshold in a later tile while its warp neighbours' does not, so the O
+    # rescale runs for some heads of a warp only.
+    w = dataclasses.replace(W.DENSE_BF16, batch=2, t=2000)
+    inp = W.make_inputs(w)
+    g = torch.Generator().manual_seed(11)
+    q = (torch.randn(2, 128, 576, generator=g) * 0.1).to(torch.bfloat16)
+    lat = inp.latent.clone()
+    for b in range(2):
+        d = q[b, 5, :512].float()
+        lat[b, 1300] = (d / d.square().mean().sqrt()).to(torch.bfloat16)
+    kv_len = inp.kv_len.clone()
+    ctx = torch.empty(2, 128, 512, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(2, 128, dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mla.decode_attend(q.to(DEV), lat.to(DEV), inp.rope_raw.to(DEV), None, kv_len.to(DEV), 2, 1, 1.0, ctx, lse,
+                      device_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    want_ctx, want_lse = O.attend_latent(H.f64(q[..., :512]), H.f64(q[..., 512:]), H.Rows(lat),
+                                         H.Rows(inp.rope_raw), [0, 0], kv_len.numpy(), 1, scale=1.0)
+    H.assert_close(ctx, want_ctx, "bf16", "ctx")
+    assert np.max(np.abs(H.f64(lse) - want_lse)) <= 2e-2
+
+
 # ---------------------------------------------------------------- edge cases
 
 def test_selection_edge_cases_flags_and_skips():
@@ -151,11 +211,15 @@ def test_selection_edge_cases_flags_and_skips():
     inp.sel_count[1] = 5
     inp.sel[2, 10] = 700          # == kv_len: outside the window
     inp.sel_count[3] = 0
-    step = DecodeStep(inp, DEV)
+    step = DecodeStep(inp, DEV, fused=False)
     step.run()
+    fstep = DecodeStep(inp, DEV, fused=True)
+    assert fstep.fused
+    fstep.run()
     torch.cuda.synchronize()
-    st = int(step.status.item())
-    assert st & mla.DEVICE_INDEX_OUT_OF_RANGE and st & mla.DEVICE_BAD_SELECTION_COUNT
+    for s in (step, fstep):
+        st = int(s.status.item())
+        assert st & mla.DEVICE_INDEX_OUT_OF_RANGE and st & mla.DEVICE_BAD_SELECTION_COUNT
     # the oracle: row 2 without the bad entry, row 3 attends to nothing
     sel, cnt = inp.sel.clone(), inp.sel_count.clone()
     sel[2, 10:cnt[2] - 1] = inp.sel[2, 11:cnt[2]].clone()
@@ -164,8 +228,11 @@ def test_selection_edge_cases_flags_and_skips():
     inp2 = dataclasses.replace(inp, sel=sel, sel_count=cnt)
     ref = H.oracle_reference(inp2, rows=[0, 1, 2])
     H.compare_step(step, ref, "bf16")
+    H.compare_step(fstep, ref, "bf16")
     assert torch.count_nonzero(step.ctx[3]) == 0
-    assert torch.all(torch.isneginf(step.lse[3]))
+    for s in (step, fstep):
+        assert torch.count_nonzero(s.out[3]) == 0
+        assert torch.all(torch.isneginf(s.lse[3]))
 
 
 def test_empty_and_short_rows():
@@ -173,11 +240,13 @@ def test_empty_and_short_rows():
     inp = W.make_inputs(w, rows=3, t_override=400)
     inp.kv_len[1] = 0              # empty row: ctx 0, lse -inf
     inp.kv_len[2] = 2              # 4 query tokens over 2 keys: tokens 0, 1 see nothing
-    step = DecodeStep(inp, DEV)
-    step.run()
-    torch.cuda.synchronize()
     ref = H.oracle_reference(inp)
-    H.compare_step(step, ref, "bf16")
+    for fused in (False, True):
+        step = DecodeStep(inp, DEV, fused=fused)
+        assert step.fused == fused
+        step.run()
+        torch.cuda.synchronize()
+        H.compare_step(step, ref, "bf16")
 
 
 def test_gather_is_bit_exact():

@@ -51,7 +51,7 @@ CASES = {
 @pytest.mark.parametrize("case", sorted(CASES))
 def test_no_alloc_matches_workspace_entry_point(case):
     inp = CASES[case]()
-    step = DecodeStep(inp, "cuda")
+    step = DecodeStep(inp, "cuda", fused=False)
     step.run()                                  # reference: caller-allocated workspace
     torch.cuda.synchronize()
     assert int(step.status.item()) == 0
@@ -71,7 +71,7 @@ def test_no_alloc_matches_workspace_entry_point(case):
 
 def test_no_alloc_refuses_requests_beyond_its_array():
     inp = W.make_inputs(W.DENSE_BF16)
-    step = DecodeStep(inp, "cuda")
+    step = DecodeStep(inp, "cuda", fused=False)
     big_batch = 4096                            # far more split slots than the array holds
     need = mla.decode_workspace_size(big_batch, 1, 128, 512, 64, 4096, 0, False, torch.bfloat16)
     assert need > (64 << 20)
