@@ -942,7 +942,7 @@ __global__ void __launch_bounds__(128) tc_combine_kernel(const __grid_constant__
 }
 
 // ------------------------------------------------------------------ combine + W_UV projection
-// The fused tail of a decode step: grid (heads), 128 threads.  CTA h merges
+// The fused tail of a decode step: grid (heads), 512 threads.  CTA h merges
 // the split partials of head h for every query row into the bf16 context rows
 // (the rows finished in place are read back from the context buffer), lays
 // them out as the K-major B operand [npad rows x 512] of a tcgen05 MMA in
@@ -957,9 +957,29 @@ struct ProjectTail {
   int32_t w_row0, w_head_rows;  // W_UV_h starts at row h*w_head_rows + w_row0
 };
 
-constexpr int PROJ_THREADS = 128;
+constexpr int PROJ_THREADS = 512;   // 8 groups of 64 threads (one 8-dim group of a row each)
+constexpr int PROJ_GROUPS = PROJ_THREADS / 64;
+constexpr int PROJ_UNROLL = 8;      // pieces whose loads are in flight together
 constexpr int PROJ_BOX_BYTES = 128 * 128;                  // [128 v rows][64 dims] bf16
-constexpr int PROJ_SMEM_MAX = 1024 + 8 * PROJ_BOX_BYTES + 8 * 64 * 128;
+constexpr int PROJ_MERGE_BYTES = PROJ_THREADS * 10 * 4;    // per thread (M, L, acc[8])
+constexpr int PROJ_SMEM_MAX = 1024 + 8 * PROJ_BOX_BYTES + 8 * 64 * 128 + PROJ_MERGE_BYTES;
+
+// Online merge of one split piece (m, l, O[8 dims]) into a running (M, L, acc).
+__device__ __forceinline__ void merge_piece(float& M, float& L, float (&acc)[8], float m, float l,
+                                            const float (&x)[8]) {
+  if (m == -CUDART_INF_F) return;       // an empty piece (weight 0; its O was never written)
+  if (m > M) {
+    const float f = exp2f(M - m);       // 0 while M is still -inf
+    L *= f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] *= f;
+    M = m;
+  }
+  const float w = exp2f(m - M);
+  L = fmaf(w, l, L);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = fmaf(w, x[j], acc[j]);
+}
 
 __global__ void __launch_bounds__(PROJ_THREADS) tc_combine_project_kernel(const __grid_constant__ CUtensorMap wmap,
                                                                           const __grid_constant__ TcDecodeArgs a,
@@ -1005,59 +1025,86 @@ __global__ void __launch_bounds__(PROJ_THREADS) tc_combine_project_kernel(const 
   pdl_wait();
 
   // ---- context rows of head h into sB (bf16, 128-byte swizzle: the 16-byte
-  // chunk c of row n sits at chunk c ^ (n & 7)); thread = (row parity, 8-dim group)
+  // chunk c of row n sits at chunk c ^ (n & 7)).  Thread = (group k, 8-dim
+  // group g).  With fewer than 8 query rows, `nsplit` groups share a row, each
+  // merging every nsplit-th piece, and their states are merged in shared memory.
   {
-    const int g = threadIdx.x & 63;
+    float* merge_s = reinterpret_cast<float*>(sB + 8 * npad * 128);
+    const int g = threadIdx.x & 63, k = threadIdx.x >> 6;
+    int rows_pow2 = 1;
+    while (rows_pow2 < a.n_q && rows_pow2 < PROJ_GROUPS) rows_pow2 <<= 1;
+    const int nsplit = PROJ_GROUPS / rows_pow2;        // 1, 2, 4 or 8
+    const int rows_per_pass = PROJ_GROUPS / nsplit;
+    const int rsub = k % nsplit;
     const int total = a.prefix[a.n_units];
     const int per = group_span(a, total);
-    for (int n = threadIdx.x >> 6; n < npad; n += 2) {
-      uint4 packed = make_uint4(0, 0, 0, 0);
-      if (n < a.n_q && a.keys[n] != 0) {
-        const int u = n / a.width, member = n % a.width;
-        const int rs = a.prefix[u], re = a.prefix[u + 1];
-        const int c0 = rs / per, c1 = (re - 1) / per;
-        if (c0 == c1) {
+    for (int n = k / nsplit; n < npad; n += rows_per_pass) {   // same trip count in every group
+      int kind = 0, u = 0, member = 0, c0 = 0, c1 = -1;         // 0: padding row, 1: no key, 2: whole, 3: split
+      if (n < a.n_q) {
+        kind = 1;
+        if (a.keys[n] != 0) {
+          u = n / a.width;
+          member = n % a.width;
+          c0 = a.prefix[u] / per;
+          c1 = (a.prefix[u + 1] - 1) / per;
+          kind = c0 == c1 ? 2 : 3;
+        }
+      }
+      float M = -CUDART_INF_F, L = 0.f, acc[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+      if (kind == 3) {
+        for (int c = c0 + rsub; c <= c1; c += PROJ_UNROLL * nsplit) {
+          float mq[PROJ_UNROLL], lq[PROJ_UNROLL], x[PROJ_UNROLL][8];
+#pragma unroll
+          for (int q = 0; q < PROJ_UNROLL; ++q) {
+            mq[q] = -CUDART_INF_F;
+            const int cq = c + q * nsplit;
+            if (cq <= c1) {
+              const int64_t sl = ((int64_t)u + cq) * a.width + member;
+              mq[q] = a.ws_ml[(sl * 2) * HEADS + h];
+              lq[q] = a.ws_ml[(sl * 2 + 1) * HEADS + h];
+              ld_global_v8(a.ws_o + ((sl * (RANK / 8) + g) * HEADS + h) * 8, x[q]);
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < PROJ_UNROLL; ++q) merge_piece(M, L, acc, mq[q], lq[q], x[q]);
+        }
+      }
+      if (nsplit > 1) {
+        float* mine = merge_s + (size_t)threadIdx.x * 10;
+        mine[0] = M;
+        mine[1] = L;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mine[2 + j] = acc[j];
+        __syncthreads();
+        if (rsub == 0 && kind == 3) {
+          for (int o = 1; o < nsplit; ++o) {
+            const float* other = merge_s + (size_t)(threadIdx.x + 64 * o) * 10;
+            float xo[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) xo[j] = other[2 + j];
+            merge_piece(M, L, acc, other[0], other[1], xo);
+          }
+        }
+        __syncthreads();
+      }
+      if (rsub == 0) {
+        uint4 packed = make_uint4(0, 0, 0, 0);
+        if (kind == 2) {
           // finished in place by its group: bf16 context (and lse) already written
           packed = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.ctx) +
                                                    (int64_t)n * a.ctx_row_stride + (int64_t)h * a.ctx_head_stride +
                                                    8 * g);
-        } else {
-          auto slot_of = [&](int c) -> int64_t { return ((int64_t)u + c) * a.width + member; };
-          float M = -CUDART_INF_F, L = 0.f;
-          for (int c = c0; c <= c1; ++c) M = fmaxf(M, a.ws_ml[(slot_of(c) * 2) * HEADS + h]);
-          float acc[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-          for (int c = c0; c <= c1; c += 4) {
-            float wc[4], x[4][8];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              wc[q] = 0.f;
-              if (c + q <= c1) {
-                const int64_t sl = slot_of(c + q);
-                const float mc = a.ws_ml[(sl * 2) * HEADS + h];
-                if (mc != -CUDART_INF_F) {
-                  wc[q] = exp2f(mc - M);
-                  L += wc[q] * a.ws_ml[(sl * 2 + 1) * HEADS + h];
-                }
-                ld_global_v8(a.ws_o + ((sl * (RANK / 8) + g) * HEADS + h) * 8, x[q]);
-              }
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-#pragma unroll
-              for (int j = 0; j < 8; ++j) acc[j] = (wc[q] != 0.f) ? fmaf(wc[q], x[q][j], acc[j]) : acc[j];
-          }
+        } else if (kind == 3) {
           const float inv = L > 0.f ? 1.f / L : 0.f;
           packed = make_uint4(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv),
                               pack_bf16x2(acc[4] * inv, acc[5] * inv), pack_bf16x2(acc[6] * inv, acc[7] * inv));
-          if (g == 0 && a.lse)
-            a.lse[(int64_t)n * HEADS + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -CUDART_INF_F;
         }
-      } else if (n < a.n_q && g == 0 && a.lse) {
-        a.lse[(int64_t)n * HEADS + h] = -CUDART_INF_F;   // no visible key: ctx 0, lse -inf
+        if (g == 0 && a.lse && (kind == 1 || kind == 3))
+          a.lse[(int64_t)n * HEADS + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -CUDART_INF_F;
+        *reinterpret_cast<uint4*>(sB + (g >> 3) * (npad * 128) + n * 128 + (((g & 7) ^ (n & 7)) << 4)) = packed;
       }
-      *reinterpret_cast<uint4*>(sB + (g >> 3) * (npad * 128) + n * 128 + (((g & 7) ^ (n & 7)) << 4)) = packed;
     }
   }
   fence_proxy_async_smem();   // generic-proxy writes of sB, read by the MMA
@@ -1091,9 +1138,12 @@ __global__ void __launch_bounds__(PROJ_THREADS) tc_combine_project_kernel(const 
   ok = mbar_wait_warp(&bar_mma, 0, kWaitLimit) && mma_ok_s != 0;
   tc_fence_after();
   if (ok) {
-    const uint32_t row_addr = tmem + ((uint32_t)(32 * warp) << 16);
-    const int j = 32 * warp + lane;
-    for (int c0 = 0; c0 < npad; c0 += 16) {
+    // warp w reads TMEM lanes 32 (w % 4) .. +31 (v rows) and columns
+    // (query rows) [16 (w / 4), +16), the blocks repeating every 64 columns
+    const int lq = warp & 3;
+    const uint32_t row_addr = tmem + ((uint32_t)(32 * lq) << 16);
+    const int j = 32 * lq + lane;
+    for (int c0 = 16 * (warp >> 2); c0 < npad; c0 += 16 * (PROJ_THREADS / 128)) {
       uint32_t r[16];
       tmem_ld16(row_addr + c0, r);
       tmem_wait_ld();
@@ -1253,7 +1303,7 @@ cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* works
     cudaFuncSetAttribute(tc_combine_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PROJ_SMEM_MAX);
     attr_tail = true;
   }
-  const size_t smem = 1024 + 8 * PROJ_BOX_BYTES + 8 * (size_t)p.npad * 128;
+  const size_t smem = 1024 + 8 * PROJ_BOX_BYTES + 8 * (size_t)p.npad * 128 + PROJ_MERGE_BYTES;
   e = launch_pdl(tc_combine_project_kernel, dim3(tail->heads), dim3(PROJ_THREADS), smem, stream, wmap, a, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
