@@ -61,6 +61,8 @@ typedef enum mla_dtype { MLA_DTYPE_F32 = 0, MLA_DTYPE_BF16 = 1 } mla_dtype;
 #define MLA_DEVICE_BAD_SELECTION_COUNT (1 << 1) /* a count of 0, < -1 or > k_max   */
 #define MLA_DEVICE_INDEX_OUT_OF_RANGE (1 << 4)  /* a position outside its window    */
 #define MLA_DEVICE_TIMEOUT (1 << 5)             /* a bounded device wait gave up    */
+#define MLA_DEVICE_LAYOUT (1 << 6)              /* shared memory not laid out as the
+                                                   kernel expects; nothing computed */
 
 /* Static, never NULL. */
 const char* mla_status_string(int status);

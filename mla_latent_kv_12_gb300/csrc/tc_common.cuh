@@ -299,6 +299,12 @@ __device__ __forceinline__ void ld_global_v8(const float* p, float (&v)[8]) {
                : "memory");
 }
 
+// L2 prefetch of the line holding `p` (no data returned: safe on memory that an
+// earlier grid may still be writing).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // wait::ld that also names the 32 destination registers of an earlier
 // tcgen05.ld, so the compiler cannot move a use of them above the wait (used
 // where further loads are in flight while earlier registers are consumed).

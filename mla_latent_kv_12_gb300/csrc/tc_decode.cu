@@ -51,7 +51,10 @@ constexpr int STAGE_BYTES = NCH * CHUNK_BYTES;
 constexpr int XH_BYTES = 128 * BN * 2;    // fp16 partial scores of one tile (one send / receive buffer)
 constexpr int HEADS = 128, RANK = 512, DV = 256;  // DV: latent dims per CTA
 constexpr int THREADS = 352;   // producer, score MMA, 4 softmax, 4 exchange, P.V MMA warps
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 4 * XH_BYTES;  // + send[2], receive[2]
+// Dynamic shared memory: the stage ring, then send[2] and receive[2].  The
+// 1024-byte alignment of the extern declaration places it on a 1024-byte
+// boundary after the static variables (checked at run time).
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4 * XH_BYTES;
 constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 400, TM_P = 464;  // TMEM columns (Q: 128 + 16)
 constexpr long long kWaitLimit = 1LL << 32;  // clock cycles (~2 s)
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
@@ -94,6 +97,10 @@ struct TcDecodeArgs {
   int32_t gather_tma;    // 1: selected rows come by TMA gather4 (else cp.async)
   int32_t lat_rows_per_batch, rope_rows_per_batch;  // batch stride in rows (gather maps)
   int32_t plan_in_kernel;  // 1: n_q <= kMaxRowsInKernelPlan, each CTA plans (CTA 0 also stores the plan)
+  // 1 inside a fused step: the launch before the decode kernel is the absorb
+  // kernel, which writes only the query and lets its dependants start only
+  // after its own wait, so every other input is complete when this grid starts.
+  int32_t early_inputs;
 };
 
 // ------------------------------------------------------------------ helpers
@@ -185,6 +192,44 @@ __device__ __forceinline__ int row_keys(const TcDecodeArgs& a, int n, bool flag)
   return keys;
 }
 
+// The split plan inside a kernel (n_q <= kMaxRowsInKernelPlan; called by every
+// thread of the block, blockDim >= n_q): visible entries per query row, then per
+// unit its tiles (the longest of its `width` rows) and their exclusive prefix,
+// scanned by warp 0 (four units per lane, in unit order).
+// With start_s / limit_s, also each row's first cache row and window limit.
+__device__ __forceinline__ void plan_rows(const TcDecodeArgs& a, int32_t* keys_s, int32_t* prefix_s, bool flag,
+                                          int32_t* start_s = nullptr, int32_t* limit_s = nullptr) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x < a.n_q) {
+    const int n = threadIdx.x;
+    keys_s[n] = row_keys(a, n, flag);
+    if (start_s) {
+      start_s[n] = a.kv_start ? a.kv_start[n / a.s_q] : 0;
+      limit_s[n] = row_limit(a, n);
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int carry = 0;
+    for (int j = 0; j < kMaxRowsInKernelPlan / 32; ++j) {
+      const int u = 32 * j + lane;
+      int tiles = 0;
+      if (u < a.n_units)
+        for (int i = 0; i < a.width; ++i) tiles = max(tiles, (keys_s[u * a.width + i] + BN - 1) / BN);
+      int v = tiles;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += x;
+      }
+      if (u < a.n_units) prefix_s[u] = carry + v - tiles;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) prefix_s[a.n_units] = carry;
+  }
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(1024) tc_plan_kernel(const __grid_constant__ TcDecodeArgs a) {
   pdl_wait();
   __shared__ int warp_sums[32];
@@ -239,7 +284,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                      const __grid_constant__ CUtensorMap lat_rows_map, const __grid_constant__ CUtensorMap rope_rows_map,
                      const __grid_constant__ TcDecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if ((smem_u32(smem_raw) & 1023u) != 0) {   // the same in every CTA: nothing waits on anything yet
+    if (threadIdx.x == 0 && a.status) atomicOr(a.status, MLA_DEVICE_LAYOUT);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   uint8_t* stages = smem;
   // Exchange buffers, each [8][128 heads][16 B] of fp16 scores: xin[b] is written
   // by the peer's bulk copy, xout[b] is staged here and copied to the peer.
@@ -253,6 +302,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   __shared__ volatile int abort_s;
   __shared__ int32_t plan_keys_s[kMaxRowsInKernelPlan];
   __shared__ int32_t plan_prefix_s[kMaxRowsInKernelPlan + 1];
+  __shared__ int32_t row_start_s[kMaxRowsInKernelPlan], row_limit_s[kMaxRowsInKernelPlan];
   auto aborted = [&]() -> bool { return __any_sync(0xffffffffu, abort_s != 0); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -279,7 +329,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     mbar_init(&s_free, 4);      // the exchange warps have read S
     mbar_init(&p_full, 4);      // one arrival per softmax warp
     mbar_init(&pv_done, 1);
-    mbar_init(&q_full, 4);
+    mbar_init(&q_full, 8);      // softmax warps (latent dims 0..127, rope) + exchange warps (128..255)
     mbar_init(&o_free, 4);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&x_full[b], 1);   // local expect_tx arrival + the peer's bulk-copy bytes
@@ -301,35 +351,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   cluster_sync();   // peer barriers initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
-  pdl_wait();       // the query (and the planner's prefix and counts) are complete
+  // Only the query is written by the launch before a fused step's decode: there
+  // the softmax warps alone wait (before their first query load), and the plan
+  // and the first cache loads start at once.
+  if (!a.early_inputs) pdl_wait();
 
   const int32_t* keys_p = a.keys;
   const int32_t* prefix_p = a.prefix;
   if (a.plan_in_kernel) {
-    // Visible entries per query row, then per unit its tiles (the longest of
-    // its `width` rows) and their exclusive prefix, scanned by warp 0 (at most
-    // 128 units, four per lane in unit order).
-    if (threadIdx.x < a.n_q) plan_keys_s[threadIdx.x] = row_keys(a, threadIdx.x, blockIdx.x == 0);
-    __syncthreads();
-    if (warp == 0) {
-      int carry = 0;
-      for (int j = 0; j < kMaxRowsInKernelPlan / 32; ++j) {
-        const int u = 32 * j + lane;
-        int tiles = 0;
-        if (u < a.n_units)
-          for (int i = 0; i < a.width; ++i) tiles = max(tiles, (plan_keys_s[u * a.width + i] + BN - 1) / BN);
-        int v = tiles;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int x = __shfl_up_sync(0xffffffffu, v, o);
-          if (lane >= o) v += x;
-        }
-        if (u < a.n_units) plan_prefix_s[u] = carry + v - tiles;
-        carry += __shfl_sync(0xffffffffu, v, 31);
-      }
-      if (lane == 0) plan_prefix_s[a.n_units] = carry;
-    }
-    __syncthreads();
+    plan_rows(a, plan_keys_s, plan_prefix_s, blockIdx.x == 0, row_start_s, row_limit_s);
     keys_p = plan_keys_s;
     prefix_p = plan_prefix_s;
     if (blockIdx.x == 0) {   // the combine kernel reads the plan from the workspace
@@ -353,13 +383,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     bool issued[STAGES];
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) issued[s] = false, issued_phase[s] = 0;
+    int fills = 0;   // the ring's first STAGES fills need no free slot
     int u, n, t0, t1;
     bool whole;
     while (!aborted() && it.next(u, t0, t1, whole)) {
       if (!member_segment(a, keys_p, u, member, n, t0, t1)) continue;
       const int b = n / a.s_q;
-      const int start = a.kv_start ? a.kv_start[b] : 0;
-      const int limit = row_limit(a, n);
+      const int start = a.plan_in_kernel ? row_start_s[n] : (a.kv_start ? a.kv_start[b] : 0);
+      const int limit = a.plan_in_kernel ? row_limit_s[n] : row_limit(a, n);
       const int keys = keys_p[n];
       const int zb = a.batch_in_map ? b : 0;
       const int32_t* list = (gather && a.sel_count[n] != -1) ? a.sel + (int64_t)n * a.k_max : nullptr;
@@ -371,7 +402,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
       }
       for (int t = t0; t < t1 && !aborted(); ++t) {
-        if (!mbar_wait_warp(&empty_bar[stage], phase ^ 1u, kWaitLimit)) { fail(); break; }
+        if (fills++ >= STAGES && !mbar_wait_warp(&empty_bar[stage], phase ^ 1u, kWaitLimit)) { fail(); break; }
         if (!gather) {
           if (lane == 0) {
             mbar_arrive_expect_tx(&full_bar[stage], nch * CHUNK_BYTES);
@@ -569,11 +600,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     uint32_t x_full_peer[2];
     x_full_peer[0] = mapa(smem_u32(&x_full[0]), peer);
     x_full_peer[1] = mapa(smem_u32(&x_full[1]), peer);
+    if (a.early_inputs) pdl_wait();   // the query comes from the launch before this one
     uint32_t tile = 0;
     int u, n, t0, t1;
     bool whole;
     while (!aborted() && it.next(u, t0, t1, whole)) {
       if (!member_segment(a, keys_p, u, member, n, t0, t1)) continue;
+      {
+        // Latent dims [dim_base+128, dim_base+256) of this head's query into
+        // TMEM columns 64..127 of Q.  Every score MMA of the previous segment
+        // has completed (its last scores were read here), so Q is free.
+        const uint4* qlat = reinterpret_cast<const uint4*>(a.q + (int64_t)n * a.q_row_stride +
+                                                           (int64_t)h * a.q_head_stride + dim_base + 128);
+        uint4 qv[16];
+#pragma unroll
+        for (int v = 0; v < 16; ++v) qv[v] = __ldg(qlat + v);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t r[32];
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            r[4 * v] = qv[8 * c + v].x, r[4 * v + 1] = qv[8 * c + v].y, r[4 * v + 2] = qv[8 * c + v].z,
+            r[4 * v + 3] = qv[8 * c + v].w;
+          tmem_st32(tmem + TM_Q + (2 + c) * 32 + lane_off, r);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_full);
+      }
       for (int t = t0; t < t1; ++t) {
         const uint32_t b = tile & 1u, use = tile >> 1;
         if (tile >= 2) {
@@ -620,6 +675,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
   } else {
     // ============================================================ softmax / epilogue
+    if (a.early_inputs) pdl_wait();   // the query comes from the launch before this one
     const int quarter = warp & 3;
     const int h = 32 * quarter + lane;                    // head = TMEM lane
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
@@ -642,34 +698,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         continue;
       }
       const int keys = keys_p[n];
-      const int limit = row_limit(a, n);
+      const int limit = a.plan_in_kernel ? row_limit_s[n] : row_limit(a, n);
       const int32_t* list = (gather && a.sel_count[n] != -1) ? a.sel + (int64_t)n * a.k_max : nullptr;
-      // ---- Q row of this head (this CTA's dims) into TMEM
+      // ---- Q row of this head (this CTA's dims) into TMEM: latent dims
+      // [dim_base, dim_base+128) and the rope half [32*rank, 32*rank+32) here,
+      // the other 128 latent dims by the exchange warps; all loads in flight at once.
       {
-        // Latent dims [dim_base, dim_base+256) as four 64-dim chunks, then the
-        // rope half [32*rank, 32*rank+32).  Two chunks in flight: chunk c+1's
-        // loads are issued before chunk c's TMEM store (a compiler barrier).
         const __nv_bfloat16* qrow = a.q + (int64_t)n * a.q_row_stride + (int64_t)h * a.q_head_stride;
         const uint4* qlat = reinterpret_cast<const uint4*>(qrow + dim_base);
         const uint4* qrope = reinterpret_cast<const uint4*>(qrow + RANK + 32 * (int)rank);
-        uint4 qa[8], qb[8];
+        uint4 qv[20];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) qa[v] = __ldg(qlat + v);
+        for (int v = 0; v < 16; ++v) qv[v] = __ldg(qlat + v);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int v = 0; v < 4; ++v) qv[16 + v] = __ldg(qrope + v);
 #pragma unroll
-          for (int v = 0; v < 8; ++v) qb[v] = (c < 3) ? __ldg(qlat + 8 * (c + 1) + v) : (v < 4 ? __ldg(qrope + v) : qa[v]);
+        for (int c = 0; c < 2; ++c) {
           uint32_t r[32];
 #pragma unroll
-          for (int v = 0; v < 8; ++v) r[4 * v] = qa[v].x, r[4 * v + 1] = qa[v].y, r[4 * v + 2] = qa[v].z, r[4 * v + 3] = qa[v].w;
+          for (int v = 0; v < 8; ++v)
+            r[4 * v] = qv[8 * c + v].x, r[4 * v + 1] = qv[8 * c + v].y, r[4 * v + 2] = qv[8 * c + v].z,
+            r[4 * v + 3] = qv[8 * c + v].w;
           tmem_st32(tmem + TM_Q + c * 32 + lane_off, r);
-#pragma unroll
-          for (int v = 0; v < 8; ++v) qa[v] = qb[v];
         }
         {
           uint32_t r[16];
 #pragma unroll
-          for (int v = 0; v < 4; ++v) r[4 * v] = qa[v].x, r[4 * v + 1] = qa[v].y, r[4 * v + 2] = qa[v].z, r[4 * v + 3] = qa[v].w;
+          for (int v = 0; v < 4; ++v)
+            r[4 * v] = qv[16 + v].x, r[4 * v + 1] = qv[16 + v].y, r[4 * v + 2] = qv[16 + v].z, r[4 * v + 3] = qv[16 + v].w;
           tmem_st16(tmem + TM_Q + 128 + lane_off, r);
         }
         tmem_wait_st();
@@ -992,6 +1048,8 @@ __global__ void __launch_bounds__(PROJ_THREADS) tc_combine_project_kernel(const 
   __shared__ __align__(8) uint64_t bar_mma;
   __shared__ uint32_t tmem_base_s;
   __shared__ int mma_ok_s;
+  __shared__ int32_t keys_s[kMaxRowsInKernelPlan];
+  __shared__ int32_t prefix_s[kMaxRowsInKernelPlan + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x;
   const int npad = p.npad;
@@ -1022,6 +1080,25 @@ __global__ void __launch_bounds__(PROJ_THREADS) tc_combine_project_kernel(const 
       tma_load_2d(sA + i * PROJ_BOX_BYTES, &wmap, &bar_full[i], 64 * i, row0);
     }
   }
+  // The split plan depends only on the step's inputs (complete, as above):
+  // recomputed here, the same way the decode kernel computes it, before the
+  // wait; the pieces' partial buffers are touched (L2 prefetch: address
+  // translation and lines) so that the loads after the wait hit.
+  plan_rows(a, keys_s, prefix_s, false);
+  {
+    const int per = group_span(a, prefix_s[a.n_units]);
+    for (int n = threadIdx.x >> 5; n < a.n_q; n += PROJ_THREADS / 32) {
+      if (keys_s[n] == 0) continue;
+      const int u = n / a.width, member = n % a.width;
+      const int c0 = prefix_s[u] / per, c1 = (prefix_s[u + 1] - 1) / per;
+      if (c0 == c1) continue;
+      for (int c = c0 + lane; c <= c1; c += 32) {
+        const int64_t sl = ((int64_t)u + c) * a.width + member;
+        prefetch_l2(a.ws_ml + sl * 2 * HEADS + h);
+        prefetch_l2(a.ws_o + sl * RANK * HEADS);
+      }
+    }
+  }
   pdl_wait();
 
   // ---- context rows of head h into sB (bf16, 128-byte swizzle: the 16-byte
@@ -1036,17 +1113,24 @@ __global__ void __launch_bounds__(PROJ_THREADS) tc_combine_project_kernel(const 
     const int nsplit = PROJ_GROUPS / rows_pow2;        // 1, 2, 4 or 8
     const int rows_per_pass = PROJ_GROUPS / nsplit;
     const int rsub = k % nsplit;
-    const int total = a.prefix[a.n_units];
-    const int per = group_span(a, total);
-    for (int n = k / nsplit; n < npad; n += rows_per_pass) {   // same trip count in every group
+    const int per = group_span(a, prefix_s[a.n_units]);
+    // the padding rows n_q .. npad-1 of the MMA's N are zero
+    for (int i = a.n_q * 64 + threadIdx.x; i < npad * 64; i += PROJ_THREADS) {
+      const int n = i >> 6, gg = i & 63;
+      *reinterpret_cast<uint4*>(sB + (gg >> 3) * (npad * 128) + n * 128 + (((gg & 7) ^ (n & 7)) << 4)) =
+          make_uint4(0, 0, 0, 0);
+    }
+    // rows in passes of rows_per_pass: the same trip count in every group
+    const int n_real = (a.n_q + rows_per_pass - 1) / rows_per_pass * rows_per_pass;
+    for (int n = k / nsplit; n < n_real; n += rows_per_pass) {
       int kind = 0, u = 0, member = 0, c0 = 0, c1 = -1;         // 0: padding row, 1: no key, 2: whole, 3: split
       if (n < a.n_q) {
         kind = 1;
-        if (a.keys[n] != 0) {
+        if (keys_s[n] != 0) {
           u = n / a.width;
           member = n % a.width;
-          c0 = a.prefix[u] / per;
-          c1 = (a.prefix[u + 1] - 1) / per;
+          c0 = prefix_s[u] / per;
+          c1 = (prefix_s[u + 1] - 1) / per;
           kind = c0 == c1 ? 2 : 3;
         }
       }
@@ -1071,7 +1155,7 @@ __global__ void __launch_bounds__(PROJ_THREADS) tc_combine_project_kernel(const 
           for (int q = 0; q < PROJ_UNROLL; ++q) merge_piece(M, L, acc, mq[q], lq[q], x[q]);
         }
       }
-      if (nsplit > 1) {
+      if (nsplit > 1) {   // uniform over the block: every thread reaches both barriers
         float* mine = merge_s + (size_t)threadIdx.x * 10;
         mine[0] = M;
         mine[1] = L;
@@ -1225,6 +1309,7 @@ cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* works
   a.min_tiles = kMinTilesPerGroup;
   a.batch_in_map = (g.latent_batch_stride != 0 || g.rope_batch_stride != 0) ? 1 : 0;
   a.plan_in_kernel = n_q <= kMaxRowsInKernelPlan ? 1 : 0;
+  a.early_inputs = (tail != nullptr && a.plan_in_kernel) ? 1 : 0;
 
   // Tensor maps over [B_buf, t_max, dims] (the batch axis has extent 1 for a
   // packed-flat cache whose batch stride is 0).

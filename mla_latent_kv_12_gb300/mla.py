@@ -20,6 +20,7 @@ F32, BF16 = 0, 1
 DEVICE_BAD_SELECTION_COUNT = 1 << 1
 DEVICE_INDEX_OUT_OF_RANGE = 1 << 4
 DEVICE_TIMEOUT = 1 << 5
+DEVICE_LAYOUT = 1 << 6
 
 _DT = {torch.float32: F32, torch.bfloat16: BF16}
 
