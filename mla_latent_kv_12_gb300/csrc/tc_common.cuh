@@ -61,6 +61,16 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
 }
 
+// Relaxed arrives for freeing a buffer that this thread's warp has just read:
+// `dep` must be a value computed from every datum read (so the warp has
+// received all of them before the arrive issues); no release fence is paid.
+__device__ __forceinline__ void mbar_arrive_relaxed_dep(uint64_t* bar, uint32_t dep) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)), "r"(dep) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote_relaxed_dep(uint32_t remote, uint32_t dep) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote), "r"(dep) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");

@@ -770,11 +770,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             }
           }
         }
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&xo_free[b]);
-          mbar_arrive_remote(x_free_peer[b]);
-        }
         // ---- online softmax (log2 domain) with lazy rescaling.  The scale is
         // positive, so the row maximum is taken on raw scores and scaled once;
         // each probability is ex2(fma(s, scale, -m)).  Independent partial
@@ -790,6 +785,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         for (int k = 8; k < BN; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], s[k]);
         const float mx = a.scale_log2 * fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        // Every score above fed mx, so the warp holds all of this tile's send
+        // and receive data: free both buffers with relaxed arrives ordered by
+        // that dependency (a release arrive costs a cluster-scope fence per tile).
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_relaxed_dep(&xo_free[b], __float_as_uint(mx));
+          mbar_arrive_remote_relaxed_dep(x_free_peer[b], __float_as_uint(mx));
+        }
         float alpha = 1.f;
         bool rescale = false;
         if (mx > m_used + kRescaleThreshold || m_used == -CUDART_INF_F) {
