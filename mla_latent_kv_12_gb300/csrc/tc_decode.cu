@@ -634,7 +634,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (tile >= 2) {
           // the peer has read our copy of tile-2 (so xout[b] is read too), and
           // our softmax warps have read their own half of it
-          if (!mbar_wait_cluster_warp(&x_free[b], (use - 1) & 1u, kWaitLimit)) { fail(); break; }
+          // (a signal only: the peer's reads of that buffer completed before its
+          // arrive, so a CTA-scope wait suffices)
+          if (!mbar_wait_warp(&x_free[b], (use - 1) & 1u, kWaitLimit)) { fail(); break; }
           if (!mbar_wait_warp(&xo_free[b], (use - 1) & 1u, kWaitLimit)) { fail(); break; }
         }
         if (!mbar_wait_warp(&s_full, tile & 1u, kWaitLimit)) { fail(); break; }
@@ -751,7 +753,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         // way in both CTAs (fp32 addition of the same two values)
         const uint32_t b = tile & 1u, use = tile >> 1;
         if (!mbar_wait_warp(&xo_full[b], use & 1u, kWaitLimit)) { fail(); break; }
-        if (!mbar_wait_cluster_warp(&x_full[b], use & 1u, kWaitLimit)) { fail(); break; }
+        // The peer's bulk copy completes as transaction bytes on this local
+        // barrier, which makes the data visible to the threads that observe the
+        // phase: a CTA-scope acquire, as for a TMA load.
+        if (!mbar_wait_warp(&x_full[b], use & 1u, kWaitLimit)) { fail(); break; }
         float s[BN];
         {
           const uint8_t* xo = xout + b * XH_BYTES;
