@@ -115,6 +115,69 @@ def rope_partial_interleaved(x: np.ndarray, position_offset, rotary_dims: int,
 
 
 # --------------------------------------------------------------------------
+# RMSNorm and the compressed-state append  (MLA page, rmsNormF32Mlx;
+# Glm52Mla.project and Glm52Mla.forward: the new tokens' latent is
+# RMS-normalised, their rope key rotated at the row's offset, and both are
+# appended to the row before attention)
+# --------------------------------------------------------------------------
+
+def rms_norm(x: np.ndarray, weight: np.ndarray, eps: float) -> np.ndarray:
+    """``x * (mean(x^2) + eps)^(-1/2) * weight`` over the last axis, float64.
+
+    The page computes it in f32 (square, mean, add eps, rsqrt, multiply by the
+    input, multiply by the weight); this is the same definition in float64.
+    """
+    x = np.asarray(x, dtype=F64)
+    w = np.asarray(weight, dtype=F64)
+    if w.shape != (x.shape[-1],):
+        raise ValueError("RMSNorm weight must match the feature axis")
+    if not np.isfinite(eps) or eps < 0:
+        raise ValueError("RMSNorm epsilon must be non-negative")
+    mean_sq = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(mean_sq + eps) * w
+
+
+def append_compressed(cache_latent: np.ndarray, cache_rope: np.ndarray, latent_raw: np.ndarray,
+                      rope_raw: np.ndarray, weight: np.ndarray, eps: float, theta: float,
+                      kv_start: Sequence[int], kv_len: Sequence[int],
+                      row_offsets: Optional[Sequence[int]] = None):
+    """Append ``S`` new tokens to every batch row of a compressed cache.
+
+    ``latent_raw [B, S, rank]`` and ``rope_raw [B, S, rope]`` (pair-interleaved)
+    are the new tokens' compressed projections.  Token ``t`` of row ``b`` is
+    RMS-normalised / rotated at position ``row_offsets[b] + t`` (default: the
+    row's current length ``kv_len[b]``, the page's right-aligned row offset)
+    and written to buffer row ``kv_start[b] + kv_len[b] + t``.  Returns new
+    float64 copies of the two cache buffers ``[B_buf, T_max, .]`` (a single
+    buffer row ``B_buf = 1`` is shared by all rows, the packed layout) and the
+    new lengths ``kv_len + S``.  A row whose new tokens would pass ``T_max`` is
+    left unchanged and reported in the returned ``overflow`` list.
+    """
+    lat = np.array(cache_latent, dtype=F64, copy=True)
+    rp = np.array(cache_rope, dtype=F64, copy=True)
+    latent_raw = np.asarray(latent_raw, dtype=F64)
+    rope_raw = np.asarray(rope_raw, dtype=F64)
+    B, S = latent_raw.shape[0], latent_raw.shape[1]
+    rope_dim = rope_raw.shape[-1]
+    offsets = np.asarray(kv_len if row_offsets is None else row_offsets, dtype=np.int64)
+    normed = rms_norm(latent_raw, weight, eps)
+    rotated = rope_partial_interleaved(rope_raw, offsets, rope_dim, theta)
+    t_max = lat.shape[1]
+    new_len = np.asarray(kv_len, dtype=np.int64).copy()
+    overflow = []
+    for b in range(B):
+        bb = b if lat.shape[0] > 1 else 0
+        first = int(kv_start[b]) + int(kv_len[b])
+        if first + S > t_max:
+            overflow.append(b)
+            continue
+        lat[bb, first:first + S] = normed[b]
+        rp[bb, first:first + S] = rotated[b]
+        new_len[b] += S
+    return lat, rp, new_len, overflow
+
+
+# --------------------------------------------------------------------------
 # kv_b_proj slicing (MLA page, attendReconstructed / attendAbsorbed)
 # --------------------------------------------------------------------------
 

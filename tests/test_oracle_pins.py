@@ -335,3 +335,62 @@ def test_gather_selected_is_indexing():
     assert np.all(g[0, 2] == 0)
     assert np.array_equal(g[1, 0], np.r_[lat[1, 1 + 8], rp[1, 9]])
     assert np.array_equal(g[1, 2], np.r_[lat[1, 5], rp[1, 5]])
+
+
+# ---------------------------------------------------------------- RMSNorm / append pins
+
+def test_rms_norm_closed_forms():
+    # eps = 0, unit weight: the output has unit root mean square whatever the input.
+    x = rng(40).standard_normal((3, 7, 512)) * 3.7
+    y = O.rms_norm(x, np.ones(512), 0.0)
+    assert np.allclose(np.sqrt(np.mean(y * y, axis=-1)), 1.0, rtol=1e-12)
+    # a constant row c with eps: every element is c / sqrt(c^2 + eps) * w_i
+    c, eps = -0.3, 1e-2
+    w = rng(41).standard_normal(16)
+    y = O.rms_norm(np.full((1, 16), c), w, eps)
+    assert np.allclose(y[0], c / math.sqrt(c * c + eps) * w, rtol=1e-13)
+    # scale invariance (eps = 0) and the weight acting elementwise
+    x = rng(42).standard_normal((4, 32))
+    w = rng(43).standard_normal(32)
+    assert np.allclose(O.rms_norm(5.5 * x, w, 0.0), O.rms_norm(x, w, 0.0), rtol=1e-12)
+    assert np.allclose(O.rms_norm(x, w, 0.0), O.rms_norm(x, np.ones(32), 0.0) * w, rtol=1e-13)
+    # a one-hot row: mean of squares is 1/n, so the hot entry becomes sqrt(n)
+    e = np.zeros((1, 64)); e[0, 9] = 1.0
+    assert np.isclose(O.rms_norm(e, np.ones(64), 0.0)[0, 9], 8.0, rtol=1e-14)
+    with pytest.raises(ValueError):
+        O.rms_norm(x, w, -1.0)
+    with pytest.raises(ValueError):
+        O.rms_norm(x, np.ones(31), 0.0)
+
+
+def test_append_places_normalised_and_rotated_rows():
+    r = rng(44)
+    B, S, T, rank, rope = 3, 2, 20, 16, 8
+    lat = r.standard_normal((B, T, rank))
+    rp = r.standard_normal((B, T, rope))
+    lat_raw = r.standard_normal((B, S, rank))
+    rope_raw = r.standard_normal((B, S, rope))
+    w = r.standard_normal(rank)
+    kv_start = [0, 3, 1]
+    kv_len = [5, 10, 18]          # row 2 overflows: 1 + 18 + 2 > 20
+    new_lat, new_rp, new_len, overflow = O.append_compressed(lat, rp, lat_raw, rope_raw, w, 1e-6, 10000.0,
+                                                             kv_start, kv_len)
+    assert overflow == [2] and list(new_len) == [7, 12, 18]
+    for b in range(2):
+        first = kv_start[b] + kv_len[b]
+        for t in range(S):
+            x = lat_raw[b, t]
+            want = x / math.sqrt(float(np.mean(x * x)) + 1e-6) * w
+            assert np.allclose(new_lat[b, first + t], want, rtol=1e-12)
+            # position kv_len[b] + t, checked against the pinned RoPE on one vector
+            want_r = O.rope_partial_interleaved(rope_raw[b, t].reshape(1, 1, rope), kv_len[b] + t, rope,
+                                                10000.0)[0, 0]
+            assert np.allclose(new_rp[b, first + t], want_r, rtol=1e-12)
+        # every other buffer row is untouched
+        keep = [i for i in range(T) if not first <= i < first + S]
+        assert np.array_equal(new_lat[b, keep], lat[b, keep]) and np.array_equal(new_rp[b, keep], rp[b, keep])
+    assert np.array_equal(new_lat[2], lat[2]) and np.array_equal(new_rp[2], rp[2])
+    # explicit row offsets move only the rotation, not the placement
+    _, rp2, _, _ = O.append_compressed(lat, rp, lat_raw, rope_raw, w, 1e-6, 10000.0, kv_start, kv_len,
+                                       row_offsets=[0, 0, 0])
+    assert np.allclose(rp2[0, 5], np.concatenate([rope_raw[0, 0, 0::2], rope_raw[0, 0, 1::2]]), rtol=0)
