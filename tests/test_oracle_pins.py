@@ -394,3 +394,18 @@ def test_append_places_normalised_and_rotated_rows():
     _, rp2, _, _ = O.append_compressed(lat, rp, lat_raw, rope_raw, w, 1e-6, 10000.0, kv_start, kv_len,
                                        row_offsets=[0, 0, 0])
     assert np.allclose(rp2[0, 5], np.concatenate([rope_raw[0, 0, 0::2], rope_raw[0, 0, 1::2]]), rtol=0)
+
+
+def test_append_exact_fit_and_packed_buffer():
+    # a row whose new tokens end exactly at T_max is appended; one token more is not
+    r = rng(45)
+    lat = r.standard_normal((1, 12, 8)); rp = r.standard_normal((1, 12, 4))
+    lat_raw = r.standard_normal((2, 2, 8)); rope_raw = r.standard_normal((2, 2, 4))
+    # packed layout: both rows share buffer row 0; row 0 = [0, 5), row 1 = [5, 10) + 2 new = 12 = T_max
+    new_lat, _, new_len, overflow = O.append_compressed(lat, rp, lat_raw, rope_raw, np.ones(8), 0.0, 10000.0,
+                                                        [0, 5], [3, 5])
+    assert overflow == [] and list(new_len) == [5, 7]
+    assert np.allclose(new_lat[0, 10:12], O.rms_norm(lat_raw[1], np.ones(8), 0.0))
+    assert np.allclose(new_lat[0, 3:5], O.rms_norm(lat_raw[0], np.ones(8), 0.0))
+    _, _, _, overflow = O.append_compressed(lat, rp, lat_raw, rope_raw, np.ones(8), 0.0, 10000.0, [0, 6], [3, 5])
+    assert overflow == [1]
