@@ -307,6 +307,28 @@ def ours(args):
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     e2e_value = w.n_q * world / (e2e_ms / 1e3)
 
+    # the cache append of the page's forward (RMSNorm + RoPE of one new token per
+    # batch row), timed alone over a scratch cache: one launch per call
+    ap_lat = torch.zeros(w.batch, 4, w.rank, dtype=one.dtype, device=dev)
+    ap_rope = torch.zeros(w.batch, 4, w.rope, dtype=one.dtype, device=dev)
+    ap_len = torch.zeros(w.batch, dtype=torch.int32, device=dev)
+    ap_in = inp.latent[:, :1].reshape(w.batch if inp.latent.shape[0] == w.batch else 1, 1, w.rank)
+    ap_in = ap_in.expand(w.batch, 1, w.rank).contiguous().to(dev)
+    ap_rin = torch.randn(w.batch, 1, w.rope, device=dev).to(one.dtype)
+    ap_w = torch.ones(w.rank, dtype=one.dtype, device=dev)
+    ap_calls = 200
+    for _ in range(3):
+        mla.append_compressed(ap_in, ap_rin, ap_w, 1e-6, w.theta, ap_lat, ap_rope, None, ap_len)
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(ap_calls):
+        mla.append_compressed(ap_in, ap_rin, ap_w, 1e-6, w.theta, ap_lat, ap_rope, None, ap_len)
+    a1.record(stream)
+    torch.cuda.synchronize()
+    append_us = a0.elapsed_time(a1) / ap_calls * 1e3
+    ap_bytes = w.batch * (w.rank + w.rope) * one.latent.element_size() * 2
+
     hbm, tf_burst, tf_sus, src = load_peaks()
     byts, flops = algorithmic(inp)
     ach_gbs = byts / (dec_ms / 1e3) / 1e9
@@ -345,6 +367,9 @@ def ours(args):
         "roofline": roof,
         "cpu_baseline": cpu,
         "cache_gbs": ach_gbs,
+        "append": {"us_per_call": append_us, "tokens_per_call": w.batch, "bytes_per_call": ap_bytes,
+                   "note": "mla_append_compressed (RMSNorm + RoPE of one new token per batch row), "
+                           "host-launched calls back to back"},
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -11,6 +11,9 @@
  *                                        -> mla_decode_attend
  *   - Glm52Mla.attendAbsorbed, latentContext @ Wv^T, heads concatenated
  *                                        -> mla_project_v
+ *   - rmsNormF32Mlx and the append of Glm52Mla.project / forward
+ *                                        -> mla_append_compressed
+ *   - the composition of the four decode operations -> mla_decode_step
  * and the causal verify window of "mlx-bun 0.4.0 -> 1.0.0, glm52.ts",
  * Glm52DecoderLayer.attend (token i of a block sees the prefix up to itself).
  *
@@ -222,6 +225,36 @@ int mla_project_v(const void* ctx, int64_t ctx_row_stride, int64_t ctx_head_stri
                   const void* kv_b_proj, int dtype, void* out, int64_t out_row_stride,
                   int out_dtype, int32_t n_q, int32_t heads, int32_t nope, int32_t v_dim,
                   int32_t rank, mla_stream_t stream);
+
+/*
+ * Append of new tokens' compressed state (MLA page: rmsNormF32Mlx, and
+ * Glm52Mla.project / Glm52Mla.forward, which normalise the latent part of the
+ * new tokens' kv_a projection, rotate its rope part at the row's position
+ * offset and append both to the cache before attending).
+ *
+ * Inputs: latent_raw[b*latent_raw_row_stride + t*latent_raw_token_stride +
+ * 0:rank] and the pair-interleaved rope_raw[b*.. + t*.. + 0:rope_dim] of new
+ * token t < s_new of batch row b, in `dtype`; norm_weight[rank] in `dtype`;
+ * eps >= 0.  Token t is written to buffer row r = kv_start[b] + kv_len[b] + t
+ * of the cache (layout as in mla_decode_attend; kv_start NULL means 0):
+ * latent[r] = x * (mean(x^2) + eps)^(-1/2) * weight, computed in f32, and
+ * rope[r] = the RoPE of mla_rope_partial_interleaved at position
+ * row_offsets[b] + t (row_offsets NULL: the row's current length kv_len[b]),
+ * in cache_dtype.  kv_len_out[b] (may be NULL, may alias kv_len) receives
+ * kv_len[b] + s_new.  A row whose new tokens would pass t_max (or with a
+ * negative length, start or offset) is left unchanged, keeps its length and
+ * sets MLA_DEVICE_INDEX_OUT_OF_RANGE.  Rows of a packed buffer must leave
+ * room after their windows: the call writes where it is told.
+ * rank <= 1024, rope_dim even and <= 256.
+ */
+int mla_append_compressed(const void* latent_raw, int64_t latent_raw_row_stride, int64_t latent_raw_token_stride,
+                          const void* rope_raw, int64_t rope_raw_row_stride, int64_t rope_raw_token_stride,
+                          int dtype, const void* norm_weight, float eps, float theta, const int32_t* row_offsets,
+                          void* latent, int64_t latent_row_stride, int64_t latent_batch_stride, void* rope,
+                          int64_t rope_row_stride, int64_t rope_batch_stride, int cache_dtype,
+                          const int32_t* kv_start, const int32_t* kv_len, int32_t* kv_len_out, int32_t batch,
+                          int32_t s_new, int32_t rank, int32_t rope_dim, int64_t t_max, int32_t* device_status,
+                          mla_stream_t stream);
 
 /*
  * One whole decode step of the attention layer in three launches: the four

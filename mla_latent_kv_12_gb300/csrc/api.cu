@@ -375,6 +375,60 @@ int mla_decode_step(const void* q_nope, int64_t q_nope_row_stride, int64_t q_nop
                      "decode_step: decode + combine/projection launch");
 }
 
+int mla_append_compressed(const void* latent_raw, int64_t latent_raw_row_stride, int64_t latent_raw_token_stride,
+                          const void* rope_raw, int64_t rope_raw_row_stride, int64_t rope_raw_token_stride,
+                          int dtype, const void* norm_weight, float eps, float theta, const int32_t* row_offsets,
+                          void* latent, int64_t latent_row_stride, int64_t latent_batch_stride, void* rope,
+                          int64_t rope_row_stride, int64_t rope_batch_stride, int cache_dtype,
+                          const int32_t* kv_start, const int32_t* kv_len, int32_t* kv_len_out, int32_t batch,
+                          int32_t s_new, int32_t rank, int32_t rope_dim, int64_t t_max, int32_t* device_status,
+                          mla_stream_t stream) {
+  g_detail[0] = 0;
+  MLA_CHECK(latent_raw && norm_weight && latent && kv_len && (rope_dim == 0 || (rope_raw && rope)),
+            "append: NULL pointer");
+  MLA_CHECK(valid_dtype(dtype) && valid_dtype(cache_dtype), "append: bad dtype");
+  MLA_CHECK(batch > 0 && s_new > 0 && rank > 0 && rope_dim >= 0 && t_max > 0, "append: sizes must be positive");
+  MLA_CHECK(rank <= kMaxAppendRank, "append: rank %d > %d", rank, kMaxAppendRank);
+  MLA_CHECK((rope_dim & 1) == 0 && rope_dim <= kMaxRotaryDims, "append: rope_dim must be even and <= %d",
+            kMaxRotaryDims);
+  MLA_CHECK(isfinite(eps) && eps >= 0.f, "append: RMSNorm epsilon must be non-negative");
+  MLA_CHECK(isfinite(theta) && theta > 0.f, "append: theta must be positive and finite");
+  MLA_CHECK(latent_raw_token_stride >= rank && latent_raw_row_stride >= 0 && latent_row_stride >= rank &&
+                latent_batch_stride >= 0,
+            "append: latent strides too small");
+  MLA_CHECK(rope_dim == 0 || (rope_raw_token_stride >= rope_dim && rope_raw_row_stride >= 0 &&
+                              rope_row_stride >= rope_dim && rope_batch_stride >= 0),
+            "append: rope strides too small");
+  AppendParams p;
+  memset(&p, 0, sizeof(p));
+  p.latent_raw = latent_raw;
+  p.lr_row_stride = latent_raw_row_stride;
+  p.lr_tok_stride = latent_raw_token_stride;
+  p.rope_raw = rope_raw;
+  p.rr_row_stride = rope_raw_row_stride;
+  p.rr_tok_stride = rope_raw_token_stride;
+  p.weight = norm_weight;
+  p.eps = eps;
+  p.row_offsets = row_offsets;
+  p.cache_latent = latent;
+  p.cl_row_stride = latent_row_stride;
+  p.cl_batch_stride = latent_batch_stride;
+  p.cache_rope = rope;
+  p.cr_row_stride = rope_row_stride;
+  p.cr_batch_stride = rope_batch_stride;
+  p.kv_start = kv_start;
+  p.kv_len = kv_len;
+  p.kv_len_out = kv_len_out;
+  p.batch = batch;
+  p.s_new = s_new;
+  p.rank = rank;
+  p.rope_dim = rope_dim;
+  p.t_max = t_max;
+  p.status = device_status;
+  if (rope_dim > 0) rope_inverse_frequencies(theta, rope_dim, p.inv_freq);
+  return cuda_status(launch_append(p, dtype, cache_dtype, (cudaStream_t)stream), "append launch");
+}
+
 int mla_project_v(const void* ctx, int64_t ctx_row_stride, int64_t ctx_head_stride,
                   const void* kv_b_proj, int dtype, void* out, int64_t out_row_stride,
                   int out_dtype, int32_t n_q, int32_t heads, int32_t nope, int32_t v_dim,

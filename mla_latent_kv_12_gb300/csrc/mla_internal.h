@@ -109,6 +109,30 @@ cudaError_t launch_tc_project(const ProjectParams& p, int out_dtype, cudaStream_
 
 cudaError_t launch_gather(const DecodeGeometry& g, int dtype, void* out, cudaStream_t stream);
 
+// Append of S new tokens per batch row (RMSNorm of the latent, RoPE of the key).
+constexpr int kMaxAppendRank = 1024;
+struct AppendParams {
+  const void* latent_raw;
+  int64_t lr_row_stride, lr_tok_stride;
+  const void* rope_raw;
+  int64_t rr_row_stride, rr_tok_stride;
+  const void* weight;
+  float eps;
+  const int32_t* row_offsets;
+  void* cache_latent;
+  int64_t cl_row_stride, cl_batch_stride;
+  void* cache_rope;
+  int64_t cr_row_stride, cr_batch_stride;
+  const int32_t* kv_start;
+  const int32_t* kv_len;
+  int32_t* kv_len_out;
+  int32_t batch, s_new, rank, rope_dim;
+  int64_t t_max;
+  int32_t* status;
+  float inv_freq[kMaxRotaryDims / 2];
+};
+cudaError_t launch_append(const AppendParams& p, int in_dtype, int cache_dtype, cudaStream_t stream);
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 

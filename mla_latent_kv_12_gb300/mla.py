@@ -29,7 +29,7 @@ EXPORTS = (
     "mla_rope_partial_interleaved", "mla_absorb_q", "mla_decode_attend",
     "mla_decode_workspace_size", "mla_decode_kernel_kind", "mla_project_v",
     "mla_gather_selected", "mla_decode_attend_no_alloc", "mla_decode_step",
-    "mla_decode_step_workspace_size",
+    "mla_decode_step_workspace_size", "mla_append_compressed",
 )
 
 
@@ -79,6 +79,10 @@ def _load() -> ctypes.CDLL:
     lib.mla_decode_step_workspace_size.restype = sz
     lib.mla_decode_step_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i64, i32, ctypes.c_int,
                                                    ctypes.c_int]
+    lib.mla_append_compressed.restype = ctypes.c_int
+    lib.mla_append_compressed.argtypes = [vp, i64, i64, vp, i64, i64, ctypes.c_int, vp, f32, f32, vp, vp, i64,
+                                          i64, vp, i64, i64, ctypes.c_int, vp, vp, vp, i32, i32, i32, i32, i64,
+                                          vp, vp]
     lib.mla_gather_selected.restype = ctypes.c_int
     lib.mla_gather_selected.argtypes = [vp, i64, i64, vp, i64, i64, ctypes.c_int, vp, vp, i32, i32, i32,
                                         i32, i64, vp, vp, i32, vp, vp, vp]
@@ -221,6 +225,24 @@ def decode_step(q_nope: torch.Tensor, q_rope: torch.Tensor, theta: float, kv_b_p
         _ptr(sel), _ptr(sel_count), k_max, float(softmax_scale), _ptr(out), out.stride(0), _dt(out),
         _ptr(lse_out), _ptr(workspace), workspace.numel(), _ptr(device_status), _stream(stream)))
     return out
+
+
+def append_compressed(latent_raw: torch.Tensor, rope_raw: torch.Tensor, norm_weight: torch.Tensor, eps: float,
+                      theta: float, latent: torch.Tensor, rope: torch.Tensor, kv_start, kv_len,
+                      kv_len_out: Optional[torch.Tensor] = None, row_offsets: Optional[torch.Tensor] = None,
+                      device_status: Optional[torch.Tensor] = None, stream=None):
+    """``latent_raw`` ``[B, S, rank]`` / ``rope_raw`` ``[B, S, rope]`` views (last dim contiguous); cache
+    views ``[B_buf, T_max, .]`` as for ``decode_attend`` (``B_buf == 1``: packed rows)."""
+    B, S, rank = latent_raw.shape
+    rope_dim = rope.shape[-1]
+    lat_bs = latent.stride(0) if latent.shape[0] > 1 else 0
+    rope_bs = rope.stride(0) if rope.shape[0] > 1 else 0
+    _check(lib.mla_append_compressed(
+        _ptr(latent_raw), latent_raw.stride(0), latent_raw.stride(1), _ptr(rope_raw), rope_raw.stride(0),
+        rope_raw.stride(1), _dt(latent_raw), _ptr(norm_weight), float(eps), float(theta), _ptr(row_offsets),
+        _ptr(latent), latent.stride(1), lat_bs, _ptr(rope), rope.stride(1), rope_bs, _dt(latent),
+        _ptr(kv_start), _ptr(kv_len), _ptr(kv_len_out), B, S, rank, rope_dim, latent.shape[1],
+        _ptr(device_status), _stream(stream)))
 
 
 def gather_selected(latent: torch.Tensor, rope: torch.Tensor, kv_start, kv_len, batch: int, s_q: int,

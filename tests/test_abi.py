@@ -108,3 +108,16 @@ def test_decode_step_validation(lib):
     assert L.mla_decode_step_workspace_size(1, 1, 128, 128, 128, 512, 64, 4096, 0, 0, 1) > 0
     assert L.mla_decode_step_workspace_size(1, 1, 64, 128, 128, 512, 64, 4096, 0, 0, 1) == 0
     assert L.mla_decode_step_workspace_size(1, 1, 128, 128, 128, 512, 64, 4096, 0, 0, 0) == 0
+
+
+def test_append_validation(lib):
+    L = lib.lib
+    # latent_raw, strides, rope_raw, strides, dtype, weight, eps, theta, offsets, latent, strides, rope, strides,
+    # cache dtype, kv_start, kv_len, kv_len_out, B, S, rank, rope, T, status, stream
+    args = [16, 512, 512, 16, 64, 64, 1, 16, 1e-6, 1e4, None, 16, 512, 0, 16, 64, 0, 1, None, 16, None,
+            1, 1, 512, 64, 128, None, None]
+    for i, v in [(0, None), (8, -1.0), (9, 0.0), (23, 2048), (24, 63), (21, 0), (19, None), (6, 5)]:
+        bad = list(args); bad[i] = v
+        assert L.mla_append_compressed(*bad) == 1, i
+    assert "epsilon" in (bad := list(args), bad.__setitem__(8, float("nan")), L.mla_append_compressed(*bad),
+                         L.mla_last_error_detail().decode())[3]

@@ -200,6 +200,90 @@ def test_decode_rescale_in_some_heads_only():
     assert np.max(np.abs(H.f64(lse) - want_lse)) <= 2e-2
 
 
+# ---------------------------------------------------------------- cache append (NEXT-3)
+
+def _append_case(dtype, cache_dtype, B=4, S=3, T=64, packed=False, offsets=None, seed=50):
+    g = torch.Generator().manual_seed(seed)
+    rank, rope_dim = 512, 64
+    bb = 1 if packed else B
+    lat = torch.randn(bb, T, rank, generator=g).to(cache_dtype)
+    rp = torch.randn(bb, T, rope_dim, generator=g).to(cache_dtype)
+    lat_raw = (torch.randn(B, S, rank, generator=g) * 2.0).to(dtype)
+    rope_raw = torch.randn(B, S, rope_dim, generator=g).to(dtype)
+    w = (1.0 + 0.1 * torch.randn(rank, generator=g)).to(dtype)
+    if packed:
+        kv_start = torch.tensor([0, 16, 32, 48][:B], dtype=torch.int32)
+        kv_len = torch.tensor([3, 13, 0, 16][:B], dtype=torch.int32)        # row 3: 48 + 16 + S > 64
+    else:
+        kv_start = torch.tensor([0, 2, 0, 1][:B], dtype=torch.int32)
+        kv_len = torch.tensor([5, 20, 0, 63][:B], dtype=torch.int32)        # row 3: 1 + 63 + S > 64
+    return lat, rp, lat_raw, rope_raw, w, kv_start, kv_len
+
+
+@pytest.mark.parametrize("dtype,cache_dtype,packed,S", [
+    (torch.bfloat16, torch.bfloat16, False, 3), (torch.bfloat16, torch.bfloat16, False, 1),
+    (torch.float32, torch.float32, False, 3), (torch.float32, torch.bfloat16, True, 3),
+    (torch.bfloat16, torch.float32, True, 2)])
+def test_append_matches_oracle(dtype, cache_dtype, packed, S):
+    lat, rp, lat_raw, rope_raw, w, kv_start, kv_len = _append_case(dtype, cache_dtype, S=S, packed=packed)
+    offsets = torch.tensor([7, 0, 100000, 3], dtype=torch.int32) if packed else None
+    d = {k: v.to(DEV) for k, v in dict(lat=lat, rp=rp, lat_raw=lat_raw, rope_raw=rope_raw, w=w,
+                                        kv_start=kv_start, kv_len=kv_len).items()}
+    out_len = torch.full_like(d["kv_len"], -7)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mla.append_compressed(d["lat_raw"], d["rope_raw"], d["w"], 1e-6, 10000.0, d["lat"], d["rp"], d["kv_start"],
+                          d["kv_len"], kv_len_out=out_len,
+                          row_offsets=offsets.to(DEV) if offsets is not None else None, device_status=st)
+    torch.cuda.synchronize()
+    want_lat, want_rp, want_len, overflow = O.append_compressed(
+        H.f64(lat), H.f64(rp), H.f64(lat_raw), H.f64(rope_raw), H.f64(w), 1e-6, 10000.0, kv_start.numpy(),
+        kv_len.numpy(), row_offsets=offsets.numpy() if offsets is not None else None)
+    assert overflow == [3]
+    assert int(st.item()) & mla.DEVICE_INDEX_OUT_OF_RANGE
+    assert out_len.cpu().tolist() == list(want_len)
+    tol = "f32" if cache_dtype == torch.float32 and dtype == torch.float32 else "bf16"
+    for b in range(4):
+        if b in overflow:
+            continue
+        bb = 0 if packed else b
+        first = int(kv_start[b] + kv_len[b])
+        H.assert_close(d["lat"][bb, first:first + S], want_lat[bb, first:first + S], tol, f"latent row {b}")
+        H.assert_close(d["rp"][bb, first:first + S], want_rp[bb, first:first + S], tol, f"rope row {b}")
+    # everything else in the cache is untouched, bit for bit
+    touched = torch.zeros(lat.shape[:2], dtype=torch.bool)
+    for b in range(4):
+        if b not in overflow:
+            bb = 0 if packed else b
+            first = int(kv_start[b] + kv_len[b])
+            touched[bb, first:first + S] = True
+    assert torch.equal(d["lat"].cpu()[~touched], lat[~touched])
+    assert torch.equal(d["rp"].cpu()[~touched], rp[~touched])
+
+
+def test_append_then_decode_matches_oracle():
+    # The page's forward: append the new token, then attend.  The cache is set
+    # up without its last key; the append writes it (normalised, rotated at its
+    # position) and updates kv_len in place; the decode step then matches the
+    # oracle over the full window.
+    w = dataclasses.replace(W.DENSE_BF16, t=700)
+    inp = W.make_inputs(w)
+    step = DecodeStep(inp, DEV)
+    last = int(inp.kv_len[0]) - 1
+    step.latent[0, last] = 3.0
+    step.rope[0, last] = -2.0
+    step.kv_len -= 1
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ones = torch.ones(w.rank, dtype=torch.bfloat16, device=DEV)
+    mla.append_compressed(inp.latent[:, last:last + 1].to(DEV), inp.rope_raw[:, last:last + 1].to(DEV), ones,
+                          1e-6, w.theta, step.latent, step.rope, step.kv_start, step.kv_len,
+                          kv_len_out=step.kv_len, device_status=st)
+    step.run()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and int(step.kv_len[0].item()) == last + 1
+    ref = H.oracle_reference(inp)
+    H.compare_step(step, ref, "bf16")
+
+
 # ---------------------------------------------------------------- edge cases
 
 def test_selection_edge_cases_flags_and_skips():
