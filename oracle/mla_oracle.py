@@ -178,6 +178,44 @@ def append_compressed(cache_latent: np.ndarray, cache_rope: np.ndarray, latent_r
 
 
 # --------------------------------------------------------------------------
+# Deterministic DSA top-k selection  ("mlx-bun ... glm52-dsa.ts",
+# selectGlm52DsaDevice and its two key kernels; the scores come from the
+# indexer, whose score function is not on the pages)
+# --------------------------------------------------------------------------
+
+def dsa_rank_keys(scores: np.ndarray) -> np.ndarray:
+    """The rank key of each f32 score: the order-preserving map of the f32 bits
+    to uint32 (negative values: all bits flipped; others: sign bit flipped),
+    complemented so that ascending keys are descending scores."""
+    bits = np.ascontiguousarray(scores, dtype=np.float32).view(np.uint32)
+    ascending = np.where(bits & np.uint32(0x80000000), ~bits, bits ^ np.uint32(0x80000000))
+    return (~ascending).astype(np.uint32)
+
+
+def select_topk(scores: np.ndarray, top_k: int) -> Optional[np.ndarray]:
+    """Positions selected from one row's scores, in the contract's order.
+
+    Stable ascending sort of the rank keys (equal scores keep ascending
+    positions), the first ``top_k`` positions, threshold = the minimum selected
+    score; the output lists the selected positions whose score is above the
+    threshold in ascending order, then the threshold ties in ascending order.
+    A row with at most ``top_k`` scores is dense: ``None``.
+    """
+    scores = np.ascontiguousarray(scores, dtype=np.float32)
+    if top_k <= 0:
+        raise ValueError("top_k must be positive")
+    if scores.shape[0] <= top_k:
+        return None
+    ranked = np.argsort(dsa_rank_keys(scores), kind="stable")
+    chosen = ranked[:top_k]
+    chosen_scores = scores[chosen]
+    threshold = np.min(chosen_scores)
+    order_class = np.where(chosen_scores > threshold, 0, 1)
+    order = np.lexsort((chosen, order_class))        # class first, then position
+    return chosen[order].astype(np.int64)
+
+
+# --------------------------------------------------------------------------
 # kv_b_proj slicing (MLA page, attendReconstructed / attendAbsorbed)
 # --------------------------------------------------------------------------
 

@@ -409,3 +409,59 @@ def test_append_exact_fit_and_packed_buffer():
     assert np.allclose(new_lat[0, 3:5], O.rms_norm(lat_raw[0], np.ones(8), 0.0))
     _, _, _, overflow = O.append_compressed(lat, rp, lat_raw, rope_raw, np.ones(8), 0.0, 10000.0, [0, 6], [3, 5])
     assert overflow == [1]
+
+
+# ---------------------------------------------------------------- DSA top-k pins
+
+def test_rank_keys_order_floats():
+    # the key order is the float order, descending, over signs, zeros and infinities
+    v = np.array([-np.inf, -3.5, -1e-30, -0.0, 0.0, 1e-30, 2.0, np.inf], dtype=np.float32)
+    k = O.dsa_rank_keys(v)
+    assert np.all(np.diff(k.astype(np.int64)) < 0)          # larger score -> smaller key
+    x = rng(60).standard_normal(1000).astype(np.float32)
+    assert np.array_equal(np.argsort(O.dsa_rank_keys(x), kind="stable"), np.argsort(-x, kind="stable"))
+
+
+def test_select_topk_distinct_scores_brute_force():
+    x = rng(61).permutation(5000).astype(np.float32) * 0.25 - 300.0     # distinct values
+    got = O.select_topk(x, 64)
+    want = np.sort(np.argsort(x)[::-1][:64])                           # the 64 largest, then ascending
+    # distinct: only the k-th is at the threshold, so it comes last
+    assert np.array_equal(np.sort(got), want)
+    thr_pos = int(np.argsort(x)[::-1][63])
+    assert got[-1] == thr_pos and np.array_equal(got[:-1], np.sort(want[want != thr_pos]))
+
+
+def test_select_topk_ties_and_order():
+    # all equal: the first k positions, ascending (equal scores keep ascending positions)
+    assert np.array_equal(O.select_topk(np.zeros(100, np.float32), 10), np.arange(10))
+    # a tie group straddling the boundary: above-threshold positions first, then the
+    # lowest-position members of the tie group, each ascending
+    x = np.zeros(20, np.float32)
+    x[[3, 17]] = 5.0                    # above
+    x[[1, 4, 9, 12, 18]] = 2.0          # the tie group at the threshold
+    got = O.select_topk(x, 5)
+    assert list(got) == [3, 17, 1, 4, 9]
+    # -inf and +inf take part like any value; -0.0 and +0.0 are equal scores
+    y = np.array([1.0, -np.inf, np.inf, 0.0, -0.0, -1.0], np.float32)
+    assert list(O.select_topk(y, 3)) == [0, 2, 3]
+    assert list(O.select_topk(y, 4)) == [0, 2, 3, 4]
+    # short rows are dense
+    assert O.select_topk(np.ones(8, np.float32), 8) is None
+    assert O.select_topk(np.ones(9, np.float32), 8) is not None
+    with pytest.raises(ValueError):
+        O.select_topk(np.ones(4, np.float32), 0)
+
+
+def test_select_topk_set_is_permutation_equivariant():
+    r = rng(62)
+    x = r.integers(0, 40, 3000).astype(np.float32)     # many ties
+    perm = r.permutation(3000)
+    inv = np.argsort(perm)
+    a = O.select_topk(x, 300)
+    b = O.select_topk(x[perm], 300)
+    # the above-threshold set is the same set of values' positions mapped through the permutation
+    thr = x[a].min()
+    assert set(a[x[a] > thr]) == set(perm[b][x[perm][b] > thr].tolist()) == set(np.nonzero(x > thr)[0].tolist())
+    assert len(a) == 300 and np.all(np.diff(a[x[a] > thr]) > 0) and np.all(np.diff(a[x[a] == thr]) > 0)
+    del inv
