@@ -316,18 +316,50 @@ def ours(args):
     ap_in = ap_in.expand(w.batch, 1, w.rank).contiguous().to(dev)
     ap_rin = torch.randn(w.batch, 1, w.rope, device=dev).to(one.dtype)
     ap_w = torch.ones(w.rank, dtype=one.dtype, device=dev)
-    ap_calls = 200
+    ap_per_graph, ap_reps = 20, 10
     for _ in range(3):
         mla.append_compressed(ap_in, ap_rin, ap_w, 1e-6, w.theta, ap_lat, ap_rope, None, ap_len)
     torch.cuda.synchronize()
+    g_ap = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g_ap, stream=cap):
+            for _ in range(ap_per_graph):
+                mla.append_compressed(ap_in, ap_rin, ap_w, 1e-6, w.theta, ap_lat, ap_rope, None, ap_len)
+    g_ap.replay()
+    torch.cuda.synchronize()
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a0.record(stream)
-    for _ in range(ap_calls):
-        mla.append_compressed(ap_in, ap_rin, ap_w, 1e-6, w.theta, ap_lat, ap_rope, None, ap_len)
+    for _ in range(ap_reps):
+        g_ap.replay()
     a1.record(stream)
     torch.cuda.synchronize()
-    append_us = a0.elapsed_time(a1) / ap_calls * 1e3
+    append_us = a0.elapsed_time(a1) / (ap_per_graph * ap_reps) * 1e3
     ap_bytes = w.batch * (w.rank + w.rope) * one.latent.element_size() * 2
+
+    # the DSA top-k selection (2048 positions per query row from f32 scores over
+    # the row's window), timed alone: 10 calls per CUDA graph, replayed
+    sel_k = 2048
+    sel_len = inp.kv_len.repeat_interleave(w.s_q).to(torch.int32).to(dev)
+    sel_scores = torch.randn(w.n_q, int(inp.kv_len.max()), device=dev)
+    sel_out = torch.empty(w.n_q, sel_k, dtype=torch.int32, device=dev)
+    sel_cnt = torch.empty(w.n_q, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        mla.select_topk(sel_scores, sel_len, sel_k, sel_out, sel_cnt)
+    torch.cuda.synchronize()
+    g_sel = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g_sel, stream=cap):
+            for _ in range(10):
+                mla.select_topk(sel_scores, sel_len, sel_k, sel_out, sel_cnt)
+    g_sel.replay()
+    torch.cuda.synchronize()
+    a0.record(stream)
+    for _ in range(5):
+        g_sel.replay()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    select_us = a0.elapsed_time(a1) / 50 * 1e3
+    sel_bytes = int(inp.kv_len.repeat_interleave(w.s_q).sum()) * 4
 
     hbm, tf_burst, tf_sus, src = load_peaks()
     byts, flops = algorithmic(inp)
@@ -369,7 +401,10 @@ def ours(args):
         "cache_gbs": ach_gbs,
         "append": {"us_per_call": append_us, "tokens_per_call": w.batch, "bytes_per_call": ap_bytes,
                    "note": "mla_append_compressed (RMSNorm + RoPE of one new token per batch row), "
-                           "host-launched calls back to back"},
+                           "20 calls per CUDA graph, replayed"},
+        "select_topk": {"us_per_call": select_us, "rows": w.n_q, "top_k": sel_k, "score_bytes": sel_bytes,
+                        "note": "mla_select_topk over f32 scores of each query row's window, "
+                                "10 calls per CUDA graph, replayed"},
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -14,6 +14,7 @@
  *   - rmsNormF32Mlx and the append of Glm52Mla.project / forward
  *                                        -> mla_append_compressed
  *   - the composition of the four decode operations -> mla_decode_step
+ * and "mlx-bun ... glm52-dsa.ts", selectGlm52DsaDevice -> mla_select_topk.
  * and the causal verify window of "mlx-bun 0.4.0 -> 1.0.0, glm52.ts",
  * Glm52DecoderLayer.attend (token i of a block sees the prefix up to itself).
  *
@@ -255,6 +256,29 @@ int mla_append_compressed(const void* latent_raw, int64_t latent_raw_row_stride,
                           const int32_t* kv_start, const int32_t* kv_len, int32_t* kv_len_out, int32_t batch,
                           int32_t s_new, int32_t rank, int32_t rope_dim, int64_t t_max, int32_t* device_status,
                           mla_stream_t stream);
+
+/*
+ * Deterministic DSA top-k selection ("mlx-bun ... glm52-dsa.ts",
+ * selectGlm52DsaDevice): the positions that mla_decode_attend's selected mode
+ * reads, from per-row f32 indexer scores (the score function itself is not
+ * on the pages).
+ *
+ * Row n has lengths[n] (device) scores at scores[n*score_row_stride + 0..);
+ * the caller promises lengths[n] <= score_row_stride.  A row with
+ * lengths[n] <= top_k is dense: counts[n] = -1 and its selection row is left
+ * as it was (a negative length also sets MLA_DEVICE_BAD_SELECTION_COUNT).
+ * Otherwise counts[n] = top_k and selected[n*selected_row_stride + 0..top_k)
+ * holds the top_k positions under the order (score descending, equal scores
+ * by ascending position) -- equal means equal f32 bits, with the order of
+ * the bits' monotone map to uint32 (+0 above -0; positive NaN above +inf,
+ * negative NaN below -inf) -- listed as: the selected positions whose score
+ * is above the threshold (the minimum selected score; NaN if any selected
+ * score is NaN) in ascending order, then the others in ascending order.
+ * The output is bit-exact and deterministic.
+ */
+int mla_select_topk(const float* scores, int64_t score_row_stride, const int32_t* lengths, int32_t n_rows,
+                    int32_t top_k, int32_t* selected, int64_t selected_row_stride, int32_t* counts,
+                    int32_t* device_status, mla_stream_t stream);
 
 /*
  * One whole decode step of the attention layer in three launches: the four

@@ -429,6 +429,18 @@ int mla_append_compressed(const void* latent_raw, int64_t latent_raw_row_stride,
   return cuda_status(launch_append(p, dtype, cache_dtype, (cudaStream_t)stream), "append launch");
 }
 
+int mla_select_topk(const float* scores, int64_t score_row_stride, const int32_t* lengths, int32_t n_rows,
+                    int32_t top_k, int32_t* selected, int64_t selected_row_stride, int32_t* counts,
+                    int32_t* device_status, mla_stream_t stream) {
+  g_detail[0] = 0;
+  MLA_CHECK(scores && lengths && selected && counts, "select_topk: NULL pointer");
+  MLA_CHECK(n_rows > 0 && top_k > 0, "select_topk: n_rows and top_k must be positive");
+  MLA_CHECK(score_row_stride >= 0 && selected_row_stride >= top_k, "select_topk: strides too small");
+  SelectParams p{scores, score_row_stride, lengths, n_rows, top_k, selected, selected_row_stride, counts,
+                 device_status};
+  return cuda_status(launch_select_topk(p, (cudaStream_t)stream), "select_topk launch");
+}
+
 int mla_project_v(const void* ctx, int64_t ctx_row_stride, int64_t ctx_head_stride,
                   const void* kv_b_proj, int dtype, void* out, int64_t out_row_stride,
                   int out_dtype, int32_t n_q, int32_t heads, int32_t nope, int32_t v_dim,

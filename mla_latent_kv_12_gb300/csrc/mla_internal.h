@@ -133,6 +133,19 @@ struct AppendParams {
 };
 cudaError_t launch_append(const AppendParams& p, int in_dtype, int cache_dtype, cudaStream_t stream);
 
+// Deterministic top-k selection of positions from per-row f32 scores.
+struct SelectParams {
+  const float* scores;
+  int64_t row_stride;
+  const int32_t* lengths;
+  int32_t n_rows, top_k;
+  int32_t* selected;
+  int64_t out_stride;
+  int32_t* counts;
+  int32_t* status;
+};
+cudaError_t launch_select_topk(const SelectParams& p, cudaStream_t stream);
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 

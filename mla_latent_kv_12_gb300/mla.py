@@ -29,7 +29,7 @@ EXPORTS = (
     "mla_rope_partial_interleaved", "mla_absorb_q", "mla_decode_attend",
     "mla_decode_workspace_size", "mla_decode_kernel_kind", "mla_project_v",
     "mla_gather_selected", "mla_decode_attend_no_alloc", "mla_decode_step",
-    "mla_decode_step_workspace_size", "mla_append_compressed",
+    "mla_decode_step_workspace_size", "mla_append_compressed", "mla_select_topk",
 )
 
 
@@ -83,6 +83,8 @@ def _load() -> ctypes.CDLL:
     lib.mla_append_compressed.argtypes = [vp, i64, i64, vp, i64, i64, ctypes.c_int, vp, f32, f32, vp, vp, i64,
                                           i64, vp, i64, i64, ctypes.c_int, vp, vp, vp, i32, i32, i32, i32, i64,
                                           vp, vp]
+    lib.mla_select_topk.restype = ctypes.c_int
+    lib.mla_select_topk.argtypes = [vp, i64, vp, i32, i32, vp, i64, vp, vp, vp]
     lib.mla_gather_selected.restype = ctypes.c_int
     lib.mla_gather_selected.argtypes = [vp, i64, i64, vp, i64, i64, ctypes.c_int, vp, vp, i32, i32, i32,
                                         i32, i64, vp, vp, i32, vp, vp, vp]
@@ -243,6 +245,16 @@ def append_compressed(latent_raw: torch.Tensor, rope_raw: torch.Tensor, norm_wei
         _ptr(latent), latent.stride(1), lat_bs, _ptr(rope), rope.stride(1), rope_bs, _dt(latent),
         _ptr(kv_start), _ptr(kv_len), _ptr(kv_len_out), B, S, rank, rope_dim, latent.shape[1],
         _ptr(device_status), _stream(stream)))
+
+
+def select_topk(scores: torch.Tensor, lengths: torch.Tensor, top_k: int, selected: torch.Tensor,
+                counts: torch.Tensor, device_status=None, stream=None):
+    """``scores`` ``[n_rows, >=max length]`` f32 (last dim contiguous); ``selected`` ``[n_rows, >=top_k]``
+    int32; ``counts`` ``[n_rows]`` int32."""
+    assert scores.dtype == torch.float32 and scores.stride(1) == 1 and selected.stride(1) == 1
+    _check(lib.mla_select_topk(_ptr(scores), scores.stride(0), _ptr(lengths), scores.shape[0], top_k,
+                               _ptr(selected), selected.stride(0), _ptr(counts), _ptr(device_status),
+                               _stream(stream)))
 
 
 def gather_selected(latent: torch.Tensor, rope: torch.Tensor, kv_start, kv_len, batch: int, s_q: int,

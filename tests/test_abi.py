@@ -121,3 +121,11 @@ def test_append_validation(lib):
         assert L.mla_append_compressed(*bad) == 1, i
     assert "epsilon" in (bad := list(args), bad.__setitem__(8, float("nan")), L.mla_append_compressed(*bad),
                          L.mla_last_error_detail().decode())[3]
+
+
+def test_select_validation(lib):
+    L = lib.lib
+    args = [16, 4096, 16, 2, 64, 16, 64, 16, None, None]
+    for i, v in [(0, None), (3, 0), (4, 0), (6, 32), (2, None)]:
+        bad = list(args); bad[i] = v
+        assert L.mla_select_topk(*bad) == 1, i

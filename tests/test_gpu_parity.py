@@ -284,6 +284,67 @@ def test_append_then_decode_matches_oracle():
     H.compare_step(step, ref, "bf16")
 
 
+# ---------------------------------------------------------------- DSA top-k selection (NEXT-2)
+
+def _select_and_compare(scores, lengths, top_k):
+    n = scores.shape[0]
+    sel = torch.full((n, top_k), -5, dtype=torch.int32, device=DEV)
+    cnt = torch.full((n,), -9, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mla.select_topk(scores.to(DEV), lengths.to(DEV), top_k, sel, cnt, device_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    sel, cnt = sel.cpu(), cnt.cpu()
+    for r in range(n):
+        want = O.select_topk(scores[r, :int(lengths[r])].numpy(), top_k)
+        if want is None:
+            assert int(cnt[r]) == -1 and torch.all(sel[r] == -5)
+        else:
+            assert int(cnt[r]) == top_k
+            assert np.array_equal(sel[r].numpy().astype(np.int64), want), f"row {r}"
+    return sel, cnt
+
+
+@pytest.mark.parametrize("top_k", [1, 7, 2048])
+def test_select_topk_bit_exact(top_k):
+    g = torch.Generator().manual_seed(70 + top_k)
+    T = 131072
+    lengths = torch.tensor([100, 5000, T, 2048, 2049, 1], dtype=torch.int32)
+    normal = torch.randn(6, T, generator=g)
+    _select_and_compare(normal, lengths, top_k)
+    ties = torch.randint(0, 10, (6, T), generator=g).to(torch.float32)     # heavy ties at the threshold
+    _select_and_compare(ties, lengths, top_k)
+
+
+def test_select_topk_special_values():
+    g = torch.Generator().manual_seed(80)
+    x = torch.randn(4, 3000, generator=g)
+    x[0, ::7] = float("inf")
+    x[0, 3::11] = float("-inf")
+    x[1, :] = 0.0
+    x[1, ::2] = -0.0                   # +0 ranks above -0
+    x[2, 100:110] = float("nan")       # positive NaN ranks first and makes the threshold NaN
+    x[3, 50:60] = -float("nan")        # negative NaN ranks last
+    lengths = torch.tensor([3000, 3000, 3000, 3000], dtype=torch.int32)
+    for k in (5, 64, 2999):
+        _select_and_compare(x, lengths, k)
+
+
+def test_select_then_sparse_decode():
+    # indexer-style scores -> device top-k -> selected-position decode, against
+    # the oracle over the oracle's selection (identical, bit for bit)
+    w = dataclasses.replace(W.SPARSE_BF16, top_k=256)
+    inp = W.make_inputs(w, rows=3, t_override=4000)
+    g = torch.Generator().manual_seed(90)
+    scores = torch.randn(3, 4000, generator=g)
+    lengths = inp.kv_len.clone()
+    lengths[1] = 200                                   # a short row: dense
+    sel, cnt = _select_and_compare(scores, lengths, 256)
+    inp2 = dataclasses.replace(inp, sel=sel.clone(), sel_count=cnt.clone())
+    inp2.kv_len[1] = 200
+    run_and_compare(inp2)
+
+
 # ---------------------------------------------------------------- edge cases
 
 def test_selection_edge_cases_flags_and_skips():
