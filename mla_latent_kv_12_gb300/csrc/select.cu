@@ -7,12 +7,14 @@
 //
 // One CTA (1024 threads) per row.  The rank key is the order-preserving map
 // of the f32 bits to uint32, complemented (ascending key = descending score).
-// A 4-pass radix select (8 bits per pass, shared-memory histograms) finds the
-// top_k-th smallest key K and how many entries equal to K are taken (the
-// lowest positions).  A counting pass gives the number of entries above the
-// threshold (0 when a selected score is NaN: the minimum is then NaN, as the
-// page's min is), and an ordered pass compacts the selection with block-wide
-// prefix sums, chunk by chunk in position order.
+// A 3-pass radix select (digits of 11, 11 and 10 bits, shared-memory
+// histograms with one atomic per distinct digit per warp) finds the top_k-th
+// smallest key K and how many entries equal to K are taken (the lowest
+// positions).  The compaction gives each warp a contiguous range of positions,
+// walked 32 at a time: a counting pass, one block-wide scan of the per-warp
+// counts, and an ordered write pass with in-warp ranks from ballots (nothing
+// is above the threshold when a selected score is NaN: the minimum is then
+// NaN, as the page's min is).
 #include <math.h>
 #include <stdint.h>
 
@@ -24,6 +26,8 @@ namespace {
 
 constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kBins = 2048;   // 11-bit digits
+constexpr int kUnroll = 8;    // independent loads in flight per thread
 
 __device__ __forceinline__ uint32_t rank_key(float s) {
   const uint32_t bits = __float_as_uint(s);
@@ -74,14 +78,15 @@ __device__ __forceinline__ void block_scan3(int (&v)[3], int (&excl)[3], int (&t
   __syncthreads();   // warp_sums is reused by the next call
 }
 
-__global__ void __launch_bounds__(kSelThreads) select_topk_kernel(const __grid_constant__ SelectParams p) {
+__global__ void __launch_bounds__(kSelThreads, 1) select_topk_kernel(const __grid_constant__ SelectParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  __shared__ int hist[256];
+  __shared__ int hist[kBins];
   __shared__ int warp_sums[kSelWarps][3];
   __shared__ uint32_t prefix_s;
   __shared__ int remaining_s;
   __shared__ int count_gt_s, nan_sel_s;
   const int row = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int L = p.lengths[row];
   const int k = p.top_k;
   const float* sc = p.scores + (int64_t)row * p.row_stride;
@@ -93,28 +98,47 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(const __grid_c
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     return;
   }
-  // ---- radix select of the k-th smallest key (1-based), 8 bits per pass
+  // ---- radix select of the k-th smallest key (1-based): digits of 11, 11 and
+  // 10 bits from the top; lanes of a warp holding the same digit add once
   if (threadIdx.x == 0) {
     prefix_s = 0;
     remaining_s = k;
   }
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = threadIdx.x; i < 256; i += kSelThreads) hist[i] = 0;
+  int hi_bits = 0;   // key bits fixed by earlier passes
+  for (int pass = 0; pass < 3; ++pass) {
+    const int width = pass < 2 ? 11 : 10;
+    const int shift = 32 - hi_bits - width;
+    const uint32_t mask = (1u << width) - 1u;
+    for (int i = threadIdx.x; i < kBins; i += kSelThreads) hist[i] = 0;
     __syncthreads();
     const uint32_t prefix = prefix_s;
-    for (int i = threadIdx.x; i < L; i += kSelThreads) {
-      const uint32_t key = rank_key(sc[i]);
-      const bool match = pass == 0 || (key >> (shift + 8)) == prefix;
-      if (match) atomicAdd(&hist[(key >> shift) & 255u], 1);
+    for (int base = 0; base < L; base += kSelThreads * kUnroll) {
+      float v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {   // kUnroll independent loads in flight
+        const int i = base + u * kSelThreads + threadIdx.x;
+        v[u] = i < L ? sc[i] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int i = base + u * kSelThreads + threadIdx.x;
+        const uint32_t key = rank_key(v[u]);
+        const bool match = i < L && (hi_bits == 0 || (key >> (32 - hi_bits)) == prefix);
+        const uint32_t digit = (key >> shift) & mask;
+        const uint32_t active = __ballot_sync(0xffffffffu, match);
+        if (match) {
+          const uint32_t same = __match_any_sync(active, digit);
+          if ((__ffs(same) - 1) == lane) atomicAdd(&hist[digit], __popc(same));
+        }
+      }
     }
     __syncthreads();
-    if (threadIdx.x < 32) {
-      // lane j owns bins 8j..8j+7: local sums, a warp scan, then the bin
-      const int lane = threadIdx.x;
-      int local[8], sum = 0;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) local[q] = hist[8 * lane + q], sum += local[q];
+    if (warp == 0) {
+      // lane j owns bins [64j, 64j+64): local sums, a warp scan, then the bin
+      const int nb = 1 << width;
+      const int per = nb / 32;
+      int sum = 0;
+      for (int q = 0; q < per; ++q) sum += hist[per * lane + q];
       int incl = sum;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -125,77 +149,99 @@ __global__ void __launch_bounds__(kSelThreads) select_topk_kernel(const __grid_c
       const int rem = remaining_s;
       if (before < rem && rem <= incl) {  // exactly one lane
         int cum = before;
-        for (int q = 0; q < 8; ++q) {
-          if (rem <= cum + local[q]) {
-            prefix_s = (prefix << 8) | (uint32_t)(8 * lane + q);
+        for (int q = 0; q < per; ++q) {
+          const int c = hist[per * lane + q];
+          if (rem <= cum + c) {
+            prefix_s = (prefix << width) | (uint32_t)(per * lane + q);
             remaining_s = rem - cum;
             break;
           }
-          cum += local[q];
+          cum += c;
         }
       }
     }
     __syncthreads();
+    hi_bits += width;
   }
   const uint32_t kth = prefix_s;        // the k-th smallest key
   const int take_ties = remaining_s;    // entries equal to kth that are taken (lowest positions)
   const float thr = key_score(kth);
-  // ---- entries above the threshold; a NaN among the selected makes the
-  // threshold NaN (nothing is above it)
-  if (threadIdx.x == 0) count_gt_s = 0, nan_sel_s = isnan(thr) ? 1 : 0;
-  __syncthreads();
-  int gt = 0, nan_sel = 0;
-  for (int i = threadIdx.x; i < L; i += kSelThreads) {
-    const float s = sc[i];
-    gt += s > thr ? 1 : 0;
-    nan_sel |= (isnan(s) && rank_key(s) < kth) ? 1 : 0;
-  }
+  // ---- compaction: warp w owns positions [w*span, (w+1)*span), walked 32 at a
+  // time (coalesced).  Pass 1 counts, per warp, the entries above the
+  // threshold, the other smaller keys and the ties, and whether a selected
+  // score is NaN (then the threshold -- the minimum selected score -- is NaN
+  // and nothing is above it).
+  const int span = ((L + kSelWarps - 1) / kSelWarps + 31) & ~31;
+  const int lo = min(L, warp * span), hi = min(L, lo + span);
+  const uint32_t lt = (1u << lane) - 1u;
+  int c_above = 0, c_less = 0, c_tie = 0;
+  bool nan_sel = isnan(thr);
+  for (int base0 = lo; base0 < hi; base0 += 32 * kUnroll) {
+    float vv[kUnroll];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    gt += __shfl_xor_sync(0xffffffffu, gt, o);
-    nan_sel |= __shfl_xor_sync(0xffffffffu, nan_sel, o);
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = base0 + 32 * u + lane;
+      vv[u] = i < hi ? sc[i] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = base0 + 32 * u + lane;
+      const bool in = i < hi;
+      const float s = vv[u];
+      const uint32_t key = in ? rank_key(s) : 0xffffffffu;
+      c_above += __popc(__ballot_sync(0xffffffffu, in && s > thr));
+      c_less += __popc(__ballot_sync(0xffffffffu, in && key < kth && !(s > thr)));
+      c_tie += __popc(__ballot_sync(0xffffffffu, in && key == kth));
+      nan_sel |= __any_sync(0xffffffffu, in && isnan(s) && key < kth);
+    }
   }
-  if ((threadIdx.x & 31) == 0) {
-    atomicAdd(&count_gt_s, gt);
+  if (threadIdx.x == 0) count_gt_s = 0, nan_sel_s = 0;
+  __syncthreads();
+  if (lane == 0) {
+    atomicAdd(&count_gt_s, c_above);
     if (nan_sel) atomicOr(&nan_sel_s, 1);
   }
-  __syncthreads();
+  // exclusive prefix of the per-warp counts (one value per warp: lanes > 0 add 0)
+  int v[3] = {lane == 0 ? c_above : 0, lane == 0 ? c_less : 0, lane == 0 ? c_tie : 0}, ex[3], tot[3];
+  block_scan3(v, ex, tot, warp_sums);   // its barriers also publish count_gt_s / nan_sel_s
+  ex[0] = __shfl_sync(0xffffffffu, ex[0], 0);
+  ex[1] = __shfl_sync(0xffffffffu, ex[1], 0);
+  ex[2] = __shfl_sync(0xffffffffu, ex[2], 0);
   const bool thr_nan = nan_sel_s != 0;
   const int n_above = thr_nan ? 0 : count_gt_s;
-  // ---- ordered compaction: above-threshold positions, then the rest, ascending
-  int carry[3] = {0, 0, 0};   // above, other selected, ties seen (key == kth)
+  // Pass 2 writes: above-threshold entries at [0, n_above) in position order,
+  // the other selected ones (smaller keys not above it, then the first
+  // take_ties ties) after them in position order.  With a NaN threshold every
+  // selected entry is in the second list.  (The ties taken before this range
+  // are the first min(ties before, take_ties).)
+  int o_above = ex[0], o_rest = ex[1] + min(ex[2], take_ties) + (thr_nan ? ex[0] : 0), t_seen = ex[2];
   int32_t* out = p.selected + (int64_t)row * p.out_stride;
-  for (int base = 0; base < L; base += kSelThreads) {
-    const int i = base + threadIdx.x;
-    int v[3] = {0, 0, 0};
-    bool sel = false, above = false;
-    uint32_t key = 0;
-    float s = 0.f;
-    if (i < L) {
-      s = sc[i];
-      key = rank_key(s);
-      v[2] = key == kth ? 1 : 0;
-    }
-    int ex[3], tot[3];
-    // first the tie ranks (a tie is taken if fewer than take_ties ties precede it)
-    int vt[3] = {0, 0, v[2]};
-    block_scan3(vt, ex, tot, warp_sums);
-    if (i < L) {
-      sel = key < kth || (key == kth && carry[2] + ex[2] < take_ties);
-      above = !thr_nan && s > thr;
-      v[0] = (sel && above) ? 1 : 0;
-      v[1] = (sel && !above) ? 1 : 0;
-    }
-    const int tie_total = tot[2];
-    int vs[3] = {v[0], v[1], 0};
-    block_scan3(vs, ex, tot, warp_sums);
+  for (int base0 = lo; base0 < hi; base0 += 32 * kUnroll) {
+   float vv[kUnroll];
+#pragma unroll
+   for (int u = 0; u < kUnroll; ++u) {
+     const int i = base0 + 32 * u + lane;
+     vv[u] = i < hi ? sc[i] : 0.f;
+   }
+#pragma unroll
+   for (int u = 0; u < kUnroll; ++u) {
+    const int i = base0 + 32 * u + lane;
+    const bool in = i < hi;
+    const float s = vv[u];
+    const uint32_t key = in ? rank_key(s) : 0xffffffffu;
+    const uint32_t tie_mask = __ballot_sync(0xffffffffu, in && key == kth);
+    const bool sel = in && (key < kth || (key == kth && t_seen + __popc(tie_mask & lt) < take_ties));
+    t_seen += __popc(tie_mask);
+    const bool above = sel && !thr_nan && s > thr;
+    const uint32_t a_mask = __ballot_sync(0xffffffffu, above);
+    const uint32_t r_mask = __ballot_sync(0xffffffffu, sel && !above);
     if (sel) {
-      const int slot = above ? carry[0] + ex[0] : n_above + carry[1] + ex[1];
+      const int slot = above ? o_above + __popc(a_mask & lt) : n_above + o_rest + __popc(r_mask & lt);
       if (slot < k) out[slot] = i;
     }
-    carry[0] += tot[0];
-    carry[1] += tot[1];
-    carry[2] += tie_total;
+    o_above += __popc(a_mask);
+    o_rest += __popc(r_mask);
+   }
   }
   if (threadIdx.x == 0) p.counts[row] = k;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
