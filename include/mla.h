@@ -322,6 +322,19 @@ size_t mla_decode_step_workspace_size(int32_t batch, int32_t s_q, int32_t heads,
                                       int selected, int dtype);
 
 /*
+ * Failure-detection self-test (no counterpart on the pages).  Every device
+ * wait of the library is bounded: a wait that gives up sets
+ * MLA_DEVICE_TIMEOUT, the kernel drains what it started and returns, and the
+ * CUDA context stays usable.  This call launches one warp that waits on a
+ * barrier nothing ever completes, through the same bounded wait, for at most
+ * limit_cycles SM clock cycles (0 < limit <= 2^32; the kernels use 2^32,
+ * about 2 s): afterwards *device_status has MLA_DEVICE_TIMEOUT set and
+ * *waited_cycles (device, may be NULL) holds the cycles waited.
+ */
+int mla_selftest_bounded_wait(int64_t limit_cycles, int32_t* device_status, int64_t* waited_cycles,
+                              mla_stream_t stream);
+
+/*
  * Test hook: the selected-position gather of attendAbsorbed (takeAxis on
  * latent and rope), bit-exact.  out[n, j, 0:rank+rope_dim] = latent || rope of
  * window key selected_positions[n*k_max + j] of query row n, for j < count;

@@ -441,6 +441,17 @@ int mla_select_topk(const float* scores, int64_t score_row_stride, const int32_t
   return cuda_status(launch_select_topk(p, (cudaStream_t)stream), "select_topk launch");
 }
 
+int mla_selftest_bounded_wait(int64_t limit_cycles, int32_t* device_status, int64_t* waited_cycles,
+                              mla_stream_t stream) {
+  g_detail[0] = 0;
+  MLA_CHECK(device_status, "selftest: NULL device_status");
+  MLA_CHECK(limit_cycles > 0 && limit_cycles <= ((int64_t)1 << 32),
+            "selftest: limit must be in (0, 2^32] cycles");
+  return cuda_status(launch_bounded_wait((long long)limit_cycles, device_status,
+                                         reinterpret_cast<long long*>(waited_cycles), (cudaStream_t)stream),
+                     "selftest launch");
+}
+
 int mla_project_v(const void* ctx, int64_t ctx_row_stride, int64_t ctx_head_stride,
                   const void* kv_b_proj, int dtype, void* out, int64_t out_row_stride,
                   int out_dtype, int32_t n_q, int32_t heads, int32_t nope, int32_t v_dim,

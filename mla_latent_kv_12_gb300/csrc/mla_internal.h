@@ -146,6 +146,9 @@ struct SelectParams {
 };
 cudaError_t launch_select_topk(const SelectParams& p, cudaStream_t stream);
 
+// Failure-detection self-test (a bounded wait on a barrier that never completes).
+cudaError_t launch_bounded_wait(long long limit_cycles, int32_t* status, long long* waited, cudaStream_t stream);
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 

@@ -30,6 +30,7 @@ EXPORTS = (
     "mla_decode_workspace_size", "mla_decode_kernel_kind", "mla_project_v",
     "mla_gather_selected", "mla_decode_attend_no_alloc", "mla_decode_step",
     "mla_decode_step_workspace_size", "mla_append_compressed", "mla_select_topk",
+    "mla_selftest_bounded_wait",
 )
 
 
@@ -85,6 +86,8 @@ def _load() -> ctypes.CDLL:
                                           vp, vp]
     lib.mla_select_topk.restype = ctypes.c_int
     lib.mla_select_topk.argtypes = [vp, i64, vp, i32, i32, vp, i64, vp, vp, vp]
+    lib.mla_selftest_bounded_wait.restype = ctypes.c_int
+    lib.mla_selftest_bounded_wait.argtypes = [i64, vp, vp, vp]
     lib.mla_gather_selected.restype = ctypes.c_int
     lib.mla_gather_selected.argtypes = [vp, i64, i64, vp, i64, i64, ctypes.c_int, vp, vp, i32, i32, i32,
                                         i32, i64, vp, vp, i32, vp, vp, vp]
@@ -255,6 +258,11 @@ def select_topk(scores: torch.Tensor, lengths: torch.Tensor, top_k: int, selecte
     _check(lib.mla_select_topk(_ptr(scores), scores.stride(0), _ptr(lengths), scores.shape[0], top_k,
                                _ptr(selected), selected.stride(0), _ptr(counts), _ptr(device_status),
                                _stream(stream)))
+
+
+def selftest_bounded_wait(limit_cycles: int, device_status: torch.Tensor,
+                          waited: Optional[torch.Tensor] = None, stream=None) -> None:
+    _check(lib.mla_selftest_bounded_wait(int(limit_cycles), _ptr(device_status), _ptr(waited), _stream(stream)))
 
 
 def gather_selected(latent: torch.Tensor, rope: torch.Tensor, kv_start, kv_len, batch: int, s_q: int,

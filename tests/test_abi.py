@@ -129,3 +129,10 @@ def test_select_validation(lib):
     for i, v in [(0, None), (3, 0), (4, 0), (6, 32), (2, None)]:
         bad = list(args); bad[i] = v
         assert L.mla_select_topk(*bad) == 1, i
+
+
+def test_selftest_validation(lib):
+    L = lib.lib
+    assert L.mla_selftest_bounded_wait(1000, None, None, None) == 1
+    assert L.mla_selftest_bounded_wait(0, 16, None, None) == 1
+    assert L.mla_selftest_bounded_wait((1 << 32) + 1, 16, None, None) == 1
