@@ -72,6 +72,10 @@ __global__ void __launch_bounds__(128) tc_absorb_kernel(const __grid_constant__ 
   const uint32_t tmem = tmem_base_s;
   bool ok = true;
   pdl_wait();
+  // Dependants may launch now: they wait for this grid before reading its
+  // output, and the decode kernel's CTAs (a whole SM each) start on the SMs
+  // these CTAs leave, overlapping their prologue with this grid's tail.
+  pdl_trigger();
 
   if (threadIdx.x == 0) {
     const uint32_t bytes = 2 * 16384 + 2 * npad * 128;
