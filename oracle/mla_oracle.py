@@ -15,6 +15,9 @@ Source pages (cited by page title, function and section):
   loop of ``Glm52Mla.forward`` (row windows, per-row nullable selections).
 * "mlx-bun 0.2.0 -> 0.4.0 / package/src/model/glm52-mla.ts" hunk (called *pad
   hunk*): the left-pad mask added to ``attendReconstructed``.
+* "mlx-bun 0.2.0 -> 0.4.0 / package/src/model/glm52-cache.ts":
+  ``Glm52Cache.specRoundRollback``, ``filter`` and ``mergeRows``, the row
+  operations of the right-aligned compressed cache.
 * "mlx-bun 0.4.0 -> 1.0.0 / package/src/model/glm52.ts" (deleted file),
   ``Glm52DecoderLayer.attend``: the sparse verify window evaluates query token
   ``i`` after appending tokens ``0..i``, each with its own selection.
@@ -432,3 +435,84 @@ def gather_selected(latent, rope, kv_start, kv_len, s_q: int, sel, sel_count, k_
         out[n, :keys.size, :latent.shape[-1]] = latent[bb][keys]
         out[n, :keys.size, latent.shape[-1]:] = rope[bb][keys]
     return out
+
+
+# --------------------------------------------------------------------------
+# Row operations of the right-aligned compressed cache  ("mlx-bun 0.2.0 ->
+# 0.4.0 / package/src/model/glm52-cache.ts", Glm52Cache.specRoundRollback,
+# Glm52Cache.filter and Glm52Cache.mergeRows).  Every state array has shape
+# [B, width, features]; row b holds row_offsets[b] valid tokens in columns
+# left_pad[b] .. width - 1, so left_pad[b] + row_offsets[b] == width.
+# --------------------------------------------------------------------------
+
+def rollback_right_aligned(arrays, left_pad, row_offsets, before_offsets, keep):
+    """Undo the rejected part of a speculative round, keeping rows right-aligned.
+
+    Row ``b`` had ``before_offsets[b]`` tokens when the round began and keeps
+    ``keep[b]`` of the tokens appended since; the rest (``rejected[b]``) are
+    dropped.  Each row is rotated right by its rejected count (column ``c``
+    takes column ``(c - rejected + width) mod width``), which carries the
+    rejected tail round to the front, and the leading columns that are pad in
+    every row afterwards are cut.  Returns ``(new arrays, new width, new
+    row_offsets, new left_pad)``.  The uniform case (the page hands it to
+    ``trim``, whose body is not on the pages) goes through the same rotation.
+    """
+    left_pad = np.asarray(left_pad, dtype=np.int64)
+    offsets = np.asarray(row_offsets, dtype=np.int64)
+    next_offsets = np.asarray(before_offsets, dtype=np.int64) + np.asarray(keep, dtype=np.int64)
+    rejected = offsets - next_offsets
+    if np.any(rejected < 0) or np.any(next_offsets < 0):
+        raise ValueError("rollback keeps more tokens than the round appended")
+    B, width = np.asarray(arrays[0]).shape[:2]
+    pads = left_pad + rejected
+    removable = int(pads.min())
+    columns = np.arange(width)
+    index = (columns[None, :] - rejected[:, None] + width) % width     # [B, width]
+    out = []
+    for a in arrays:
+        a = np.asarray(a)
+        shifted = np.take_along_axis(a, index[:, :, None], axis=1)
+        out.append(shifted[:, removable:].copy())
+    return out, width - removable, next_offsets, pads - removable
+
+
+def filter_right_aligned(arrays, left_pad, row_offsets, keep_rows):
+    """Keep the rows ``keep_rows`` (in that order) and cut the leading columns
+    that are pad in every kept row.  Returns ``(arrays, width, row_offsets,
+    left_pad)``."""
+    keep_rows = np.asarray(keep_rows, dtype=np.int64)
+    if keep_rows.size == 0:
+        raise ValueError("filter keeps no row")
+    pads = np.asarray(left_pad, dtype=np.int64)[keep_rows]
+    removable = int(pads.min())
+    width = np.asarray(arrays[0]).shape[1]
+    out = [np.asarray(a)[keep_rows, removable:].copy() for a in arrays]
+    return out, width - removable, np.asarray(row_offsets, dtype=np.int64)[keep_rows], pads - removable
+
+
+def merge_right_aligned(caches):
+    """Concatenate the rows of several right-aligned caches into one.
+
+    ``caches`` is a list of ``(arrays, left_pad, row_offsets)``.  Each row's
+    valid tokens (its ``fetchRow``) are placed right-aligned in a common width
+    equal to the largest row offset; pad columns are zero (the pages build
+    empty rows from zeros; the pad content of longer merges is not shown).
+    Returns ``(arrays, width, row_offsets, left_pad)``.
+    """
+    rows = []
+    for arrays, left_pad, row_offsets in caches:
+        for b in range(len(row_offsets)):
+            pad, off = int(left_pad[b]), int(row_offsets[b])
+            rows.append(([np.asarray(a)[b, pad:pad + off] for a in arrays], off))
+    width = max(off for _, off in rows)
+    n_arrays = len(caches[0][0])
+    out = []
+    for k in range(n_arrays):
+        proto = np.asarray(caches[0][0][k])
+        merged = np.zeros((len(rows), width, proto.shape[2]), dtype=proto.dtype)
+        for i, (tokens, off) in enumerate(rows):
+            if off:
+                merged[i, width - off:] = tokens[k]
+        out.append(merged)
+    offsets = np.array([off for _, off in rows], dtype=np.int64)
+    return out, width, offsets, width - offsets

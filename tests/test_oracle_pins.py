@@ -465,3 +465,115 @@ def test_select_topk_set_is_permutation_equivariant():
     assert set(a[x[a] > thr]) == set(perm[b][x[perm][b] > thr].tolist()) == set(np.nonzero(x > thr)[0].tolist())
     assert len(a) == 300 and np.all(np.diff(a[x[a] > thr]) > 0) and np.all(np.diff(a[x[a] == thr]) > 0)
     del inv
+
+
+# ---------------------------------------------------------------- right-aligned cache row operations
+
+def _tagged_cache(offsets, width, features=3, fill=-1.0):
+    """A right-aligned cache whose valid token j of row b holds (b, j, b*1000+j)
+    and whose pad holds ``fill``: every token says where it came from."""
+    B = len(offsets)
+    a = np.full((B, width, features), fill)
+    pad = np.array([width - o for o in offsets])
+    for b, o in enumerate(offsets):
+        for j in range(o):
+            a[b, pad[b] + j] = [b, j, b * 1000 + j][:features]
+    return a, pad, np.array(offsets)
+
+
+def _valid_tokens(a, pad, b):
+    return a[b, pad[b]:]
+
+
+def test_rollback_keeps_each_rows_accepted_prefix_in_order():
+    before = [5, 2, 7, 0]
+    appended = 4
+    offsets = [o + appended for o in before]
+    a, pad, offs = _tagged_cache(offsets, width=12)
+    keep = [4, 0, 2, 1]
+    (out,), width, new_off, new_pad = O.rollback_right_aligned([a], pad, offs, before, keep)
+    assert list(new_off) == [9, 2, 9, 1]
+    # the width loses the columns that are pad in every row afterwards
+    assert width == 12 - min(pad[b] + (offsets[b] - new_off[b]) for b in range(4)) == 9
+    assert np.all(new_pad + new_off == width)
+    for b in range(4):
+        tokens = _valid_tokens(out, new_pad, b)
+        assert tokens.shape[0] == new_off[b]
+        assert np.array_equal(tokens[:, 0], np.full(new_off[b], b))           # the row's own tokens
+        assert np.array_equal(tokens[:, 1], np.arange(new_off[b]))            # its first tokens, in order
+
+
+def test_rollback_uniform_rejection_drops_the_last_columns():
+    # every row rejects r tokens and one row fills the width: the result is the
+    # cache without its last r columns (what trimming the tail gives)
+    before = [6, 3]
+    offsets = [9, 6]
+    a = rng(70).standard_normal((2, 9, 4))
+    _, pad, offs = _tagged_cache(offsets, 9)
+    (out,), width, new_off, new_pad = O.rollback_right_aligned([a], pad, offs, before, [1, 1])
+    assert width == 7 and list(new_off) == [7, 4] and list(new_pad) == [0, 3]
+    assert np.array_equal(out, a[:, :7])
+    # nothing rejected and a full row: identity
+    (same,), w2, off2, pad2 = O.rollback_right_aligned([a], pad, offs, before, [3, 3])
+    assert w2 == 9 and np.array_equal(same, a) and list(off2) == offsets and list(pad2) == list(pad)
+
+
+def test_rollback_rejects_more_than_was_appended():
+    a, pad, offs = _tagged_cache([4, 4], 4)
+    with pytest.raises(ValueError):
+        O.rollback_right_aligned([a], pad, offs, [2, 2], [3, 0])
+    # a row may go back to empty
+    (out,), width, new_off, new_pad = O.rollback_right_aligned([a], pad, offs, [0, 2], [0, 0])
+    assert list(new_off) == [0, 2] and width == 2 and list(new_pad) == [2, 0]
+    assert np.array_equal(out[1, :, 1], [0, 1])
+
+
+def test_rollback_then_attention_equals_attention_over_the_accepted_prefix():
+    # decode over the rolled-back cache attends exactly to each row's accepted prefix
+    r = rng(71)
+    before, offsets, keep = [3, 5], [6, 8], [2, 1]
+    width, rank, rope_dim, H = 10, 8, 4, 2
+    lat = r.standard_normal((2, width, rank)); rp = r.standard_normal((2, width, rope_dim))
+    pad = np.array([width - o for o in offsets])
+    q_lat = r.standard_normal((2, H, rank)); q_rope = r.standard_normal((2, H, rope_dim))
+    (lat2, rp2), w2, off2, pad2 = O.rollback_right_aligned([lat, rp], pad, offsets, before, keep)
+    got, _ = O.attend_latent(q_lat, q_rope, lat2, rp2, pad2, off2, 1, None, None, 0.5)
+    want, _ = O.attend_latent(q_lat, q_rope, lat, rp, pad, np.add(before, keep), 1, None, None, 0.5)
+    assert np.allclose(got, want, rtol=1e-13, atol=1e-13)
+
+
+def test_filter_keeps_rows_and_cuts_the_common_pad():
+    a, pad, offs = _tagged_cache([3, 7, 5, 1], 9)
+    (out,), width, new_off, new_pad = O.filter_right_aligned([a], pad, offs, [2, 0, 3])
+    assert width == 5 == max(5, 3, 1)                     # the longest kept row now fills the width
+    assert list(new_off) == [5, 3, 1] and list(new_pad) == [0, 2, 4]
+    for i, src in enumerate([2, 0, 3]):
+        assert np.array_equal(_valid_tokens(out, new_pad, i), _valid_tokens(a, pad, src))
+    with pytest.raises(ValueError):
+        O.filter_right_aligned([a], pad, offs, [])
+
+
+def test_merge_right_aligns_rows_in_the_longest_width():
+    a, pad_a, off_a = _tagged_cache([2, 4], 6, fill=7.0)        # width above its longest row
+    b, pad_b, off_b = _tagged_cache([5, 0], 5, fill=7.0)
+    (out,), width, offs, pads = O.merge_right_aligned([([a], pad_a, off_a), ([b], pad_b, off_b)])
+    assert width == 5 and list(offs) == [2, 4, 5, 0] and list(pads) == [3, 1, 0, 5]
+    assert np.array_equal(_valid_tokens(out, pads, 0), _valid_tokens(a, pad_a, 0))
+    assert np.array_equal(_valid_tokens(out, pads, 1), _valid_tokens(a, pad_a, 1))
+    assert np.array_equal(_valid_tokens(out, pads, 2), _valid_tokens(b, pad_b, 0))
+    for i in range(4):
+        assert np.all(out[i, :pads[i]] == 0.0)                      # pad columns are zero
+
+
+def test_filter_then_merge_round_trip():
+    r = rng(72)
+    offsets = [4, 9, 6, 2, 9]
+    width = 9
+    a = r.standard_normal((5, width, 3))
+    pad = np.array([width - o for o in offsets])
+    for b in range(5):
+        a[b, :pad[b]] = 0.0
+    parts = [O.filter_right_aligned([a], pad, offsets, rows) for rows in ([0, 1], [2], [3, 4])]
+    (out,), w, offs, pads = O.merge_right_aligned([(arrs, p, o) for arrs, _, o, p in parts])
+    assert w == width and list(offs) == offsets and list(pads) == list(pad)
+    assert np.array_equal(out, a)
