@@ -207,6 +207,7 @@ def reference_arm(args):
 
 
 def ours(args):
+    import numpy as np
     import torch
     import torch.distributed as dist
 
@@ -361,6 +362,42 @@ def ours(args):
     select_us = a0.elapsed_time(a1) / 50 * 1e3
     sel_bytes = int(inp.kv_len.repeat_interleave(w.s_q).sum()) * 4
 
+    # the speculative-round rollback of a right-aligned cache (8 rows x 65536
+    # tokens of latent || rope, the verify batch's cache): one row-gather launch
+    # per state array, 2 x 0.6 GB moved per call, larger than L2
+    rb_B, rb_W = 8, 65536
+    rb_lat = torch.randn(rb_B, rb_W, w.rank, device=dev).to(one.dtype)
+    rb_rope = torch.randn(rb_B, rb_W, w.rope, device=dev).to(one.dtype)
+    rb_off = np.full(rb_B, rb_W - 7)
+    rb_off[::2] = rb_W                                     # half the rows fill the width
+    rb_keep = np.arange(rb_B) % 5                          # 0..4 of 4 appended tokens kept (4 = all)
+    rb_keep = np.minimum(rb_keep, 4)
+    rb_shift, _, _, rb_w = mla.plan_rollback(rb_W - rb_off, rb_off, rb_off - 4, rb_keep, rb_W)
+    rb_shift = rb_shift.to(dev)
+    rb_dst = [torch.empty(rb_B, rb_w, a.shape[2], dtype=a.dtype, device=dev) for a in (rb_lat, rb_rope)]
+
+    def rollback_call():
+        for a, d in zip((rb_lat, rb_rope), rb_dst):
+            mla.cache_shift_rows(a, d, shift=rb_shift)
+    for _ in range(3):
+        rollback_call()
+    torch.cuda.synchronize()
+    g_rb = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g_rb, stream=cap):
+            for _ in range(5):
+                rollback_call()
+    g_rb.replay()
+    torch.cuda.synchronize()
+    a0.record(stream)
+    for _ in range(4):
+        g_rb.replay()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    rollback_us = a0.elapsed_time(a1) / 20 * 1e3
+    rb_bytes = 2 * rb_B * rb_w * (w.rank + w.rope) * rb_lat.element_size()
+    del rb_lat, rb_rope, rb_dst
+
     hbm, tf_burst, tf_sus, src = load_peaks()
     byts, flops = algorithmic(inp)
     ach_gbs = byts / (dec_ms / 1e3) / 1e9
@@ -405,6 +442,12 @@ def ours(args):
         "select_topk": {"us_per_call": select_us, "rows": w.n_q, "top_k": sel_k, "score_bytes": sel_bytes,
                         "note": "mla_select_topk over f32 scores of each query row's window, "
                                 "10 calls per CUDA graph, replayed"},
+        "rollback": {"us_per_call": rollback_us, "bytes_per_call": rb_bytes,
+                     "gbs": rb_bytes / (rollback_us * 1e-6) / 1e9,
+                     "frac_of_measured_hbm": rb_bytes / (rollback_us * 1e-6) / 1e9 / hbm,
+                     "note": "right-aligned rollback (mla_plan_rollback + two mla_cache_shift_rows) of "
+                             "8 x 65536 tokens of latent || rope, read + write bytes, 5 calls per CUDA "
+                             "graph, replayed"},
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

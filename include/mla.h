@@ -14,7 +14,10 @@
  *   - rmsNormF32Mlx and the append of Glm52Mla.project / forward
  *                                        -> mla_append_compressed
  *   - the composition of the four decode operations -> mla_decode_step
- * and "mlx-bun ... glm52-dsa.ts", selectGlm52DsaDevice -> mla_select_topk.
+ * and "mlx-bun ... glm52-dsa.ts", selectGlm52DsaDevice -> mla_select_topk,
+ * and "mlx-bun 0.2.0 -> 0.4.0, glm52-cache.ts", Glm52Cache.specRoundRollback,
+ * filter and mergeRows -> mla_plan_rollback / mla_plan_filter /
+ * mla_plan_merge + mla_cache_shift_rows, and mla_rollback_lengths,
  * and the causal verify window of "mlx-bun 0.4.0 -> 1.0.0, glm52.ts",
  * Glm52DecoderLayer.attend (token i of a block sees the prefix up to itself).
  *
@@ -333,6 +336,85 @@ size_t mla_decode_step_workspace_size(int32_t batch, int32_t s_q, int32_t heads,
  */
 int mla_selftest_bounded_wait(int64_t limit_cycles, int32_t* device_status, int64_t* waited_cycles,
                               mla_stream_t stream);
+
+/*
+ * Row operations of the compressed cache ("mlx-bun 0.2.0 -> 0.4.0,
+ * package/src/model/glm52-cache.ts": Glm52Cache.specRoundRollback, filter and
+ * mergeRows).
+ *
+ * Right-aligned layout (the pages' own): every state array (latent, rope, an
+ * indexer key cache, ...) is [B, width, features]; row b holds row_offsets[b]
+ * valid tokens in columns left_pad[b] .. width-1, so left_pad[b] +
+ * row_offsets[b] == width.  Each operation is a host plan (integer
+ * bookkeeping on host arrays, no device work) plus one mla_cache_shift_rows
+ * call per state array, which writes a new array of the planned width:
+ *   - rollback (specRoundRollback): row b began the round with
+ *     before_offsets[b] tokens and keeps keep[b] of the tokens appended
+ *     since.  Each row is rotated right by its rejected count (column c takes
+ *     column (c - rejected + width) mod width) and the columns that are pad in
+ *     every row afterwards are cut: shift[b] = removable - rejected[b] with
+ *     removable = min_b(left_pad[b] + rejected[b]); the new width is width -
+ *     removable.  The uniform case (the page hands it to trim) is the same
+ *     rotation.
+ *   - filter: the rows keep_rows[0..n_keep) in that order, less the leading
+ *     columns that are pad in every kept row; src_row = keep_rows, shift[i] =
+ *     that common pad.
+ *   - merge (mergeRows): the rows of several caches, listed in merge order,
+ *     right-aligned in a width equal to the largest row offset; pad columns
+ *     are zero (zero_below[i] = the row's new pad).  Call mla_cache_shift_rows
+ *     once per source cache, with dst advanced to that source's first row and
+ *     the plan arrays sliced to its rows (src_row = the row's index in its
+ *     source).
+ * The plans take and return HOST int32 arrays of the row count, return
+ * MLA_ERR_INVALID_ARGUMENT (writing nothing) for a row that is not
+ * right-aligned, a kept row outside [0, batch) or a rollback that keeps more
+ * tokens than the round appended, and never touch the device.
+ *
+ * Per-row window layout (kv_start, kv_len; the decode entry points'): no data
+ * moves in a rollback; mla_rollback_lengths sets each row's length back to
+ * its accepted prefix, and the rejected tokens are overwritten by the next
+ * append.
+ */
+int mla_plan_rollback(int32_t batch, int32_t width, const int32_t* left_pad, const int32_t* row_offsets,
+                      const int32_t* before_offsets, const int32_t* keep, int32_t* shift, int32_t* new_left_pad,
+                      int32_t* new_row_offsets, int32_t* new_width);
+int mla_plan_filter(int32_t batch, int32_t width, const int32_t* left_pad, const int32_t* row_offsets,
+                    const int32_t* keep_rows, int32_t n_keep, int32_t* shift, int32_t* new_left_pad,
+                    int32_t* new_row_offsets, int32_t* new_width);
+int mla_plan_merge(int32_t n_rows, const int32_t* source_width, const int32_t* left_pad,
+                   const int32_t* row_offsets, int32_t* shift, int32_t* zero_below, int32_t* new_left_pad,
+                   int32_t* new_width);
+
+/*
+ * The gather behind the three row operations, bit-exact for any dtype:
+ *   dst[i, c, :] = c < zero_below[i] ? 0
+ *                : src[src_row[i], (c + shift[i]) mod src_width, :]
+ * for rows i < n_rows (<= 65535) and columns c < dst_width.  src is [src_batch,
+ * src_width, features] and dst [n_rows, dst_width, features], strides in
+ * elements (token stride >= features; feature axis contiguous).  src_row,
+ * shift and zero_below are DEVICE int32 arrays of n_rows (NULL: row i, 0, 0);
+ * shift may be negative.  dst must not overlap src (MLA_ERR_INVALID_ARGUMENT:
+ * the rotation is not done in place) and its rows must not overlap each
+ * other.  dst_width 0 launches nothing.  A src_row outside [0, src_batch) or
+ * a zero_below outside [0, dst_width] sets MLA_DEVICE_INDEX_OUT_OF_RANGE and
+ * leaves that destination row unwritten.  src_width may be 0 (an empty
+ * cache; src may then be NULL) when every row is all zero (zero_below[i] ==
+ * dst_width); a row that would read it is flagged the same way.
+ */
+int mla_cache_shift_rows(const void* src, int64_t src_token_stride, int64_t src_batch_stride, int32_t src_batch,
+                         int32_t src_width, void* dst, int64_t dst_token_stride, int64_t dst_batch_stride,
+                         int32_t dst_width, int32_t features, int dtype, const int32_t* src_row,
+                         const int32_t* shift, const int32_t* zero_below, int32_t n_rows, int32_t* device_status,
+                         mla_stream_t stream);
+
+/*
+ * Rollback in the per-row window layout: kv_len_out[b] = kv_len_before[b] +
+ * keep[b] (device int32 arrays of batch; kv_len_out may alias kv_len).  A row
+ * with a negative entry or that would keep more than kv_len[b] tokens keeps
+ * kv_len[b] and sets MLA_DEVICE_INDEX_OUT_OF_RANGE.
+ */
+int mla_rollback_lengths(const int32_t* kv_len_before, const int32_t* keep, const int32_t* kv_len,
+                         int32_t* kv_len_out, int32_t batch, int32_t* device_status, mla_stream_t stream);
 
 /*
  * Test hook: the selected-position gather of attendAbsorbed (takeAxis on

@@ -3,6 +3,7 @@
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
+#include <stdint.h>
 
 #include "mla_internal.h"
 
@@ -489,6 +490,145 @@ int mla_gather_selected(const void* latent, int64_t latent_row_stride, int64_t l
   g.sel_count = selected_counts;
   g.k_max = k_max;
   return cuda_status(launch_gather(g, dtype, out, (cudaStream_t)stream), "gather launch");
+}
+
+// ------------------------------------------------------------ cache row operations
+
+int mla_plan_rollback(int32_t batch, int32_t width, const int32_t* left_pad, const int32_t* row_offsets,
+                      const int32_t* before_offsets, const int32_t* keep, int32_t* shift, int32_t* new_left_pad,
+                      int32_t* new_row_offsets, int32_t* new_width) {
+  g_detail[0] = 0;
+  MLA_CHECK(left_pad && row_offsets && before_offsets && keep && shift && new_left_pad && new_row_offsets &&
+                new_width,
+            "plan_rollback: NULL pointer");
+  MLA_CHECK(batch > 0 && width >= 0, "plan_rollback: batch must be positive and width non-negative");
+  int64_t removable = INT64_MAX;
+  for (int32_t b = 0; b < batch; ++b) {
+    MLA_CHECK(left_pad[b] >= 0 && row_offsets[b] >= 0 && (int64_t)left_pad[b] + row_offsets[b] == width,
+              "plan_rollback: row %d is not right-aligned (pad %d + offset %d != width %d)", b, left_pad[b],
+              row_offsets[b], width);
+    const int64_t next = (int64_t)before_offsets[b] + keep[b];
+    MLA_CHECK(before_offsets[b] >= 0 && keep[b] >= 0 && next <= row_offsets[b],
+              "plan_rollback: row %d keeps %lld tokens of %d", b, (long long)next, row_offsets[b]);
+    const int64_t pad = (int64_t)left_pad[b] + (row_offsets[b] - next);
+    if (pad < removable) removable = pad;
+  }
+  for (int32_t b = 0; b < batch; ++b) {
+    const int32_t next = before_offsets[b] + keep[b];
+    const int32_t rejected = row_offsets[b] - next;
+    shift[b] = (int32_t)(removable - rejected);
+    new_left_pad[b] = (int32_t)(left_pad[b] + rejected - removable);
+    new_row_offsets[b] = next;
+  }
+  *new_width = (int32_t)(width - removable);
+  return MLA_OK;
+}
+
+int mla_plan_filter(int32_t batch, int32_t width, const int32_t* left_pad, const int32_t* row_offsets,
+                    const int32_t* keep_rows, int32_t n_keep, int32_t* shift, int32_t* new_left_pad,
+                    int32_t* new_row_offsets, int32_t* new_width) {
+  g_detail[0] = 0;
+  MLA_CHECK(left_pad && row_offsets && keep_rows && shift && new_left_pad && new_row_offsets && new_width,
+            "plan_filter: NULL pointer");
+  MLA_CHECK(batch > 0 && width >= 0 && n_keep > 0, "plan_filter: batch and n_keep must be positive");
+  int32_t removable = INT32_MAX;
+  for (int32_t i = 0; i < n_keep; ++i) {
+    const int32_t b = keep_rows[i];
+    MLA_CHECK(b >= 0 && b < batch, "plan_filter: kept row %d outside [0, %d)", b, batch);
+    MLA_CHECK(left_pad[b] >= 0 && row_offsets[b] >= 0 && (int64_t)left_pad[b] + row_offsets[b] == width,
+              "plan_filter: row %d is not right-aligned", b);
+    if (left_pad[b] < removable) removable = left_pad[b];
+  }
+  for (int32_t i = 0; i < n_keep; ++i) {
+    shift[i] = removable;
+    new_left_pad[i] = left_pad[keep_rows[i]] - removable;
+    new_row_offsets[i] = row_offsets[keep_rows[i]];
+  }
+  *new_width = width - removable;
+  return MLA_OK;
+}
+
+int mla_plan_merge(int32_t n_rows, const int32_t* source_width, const int32_t* left_pad,
+                   const int32_t* row_offsets, int32_t* shift, int32_t* zero_below, int32_t* new_left_pad,
+                   int32_t* new_width) {
+  g_detail[0] = 0;
+  MLA_CHECK(source_width && left_pad && row_offsets && shift && zero_below && new_left_pad && new_width,
+            "plan_merge: NULL pointer");
+  MLA_CHECK(n_rows > 0, "plan_merge: n_rows must be positive");
+  int32_t width = 0;
+  for (int32_t i = 0; i < n_rows; ++i) {
+    MLA_CHECK(left_pad[i] >= 0 && row_offsets[i] >= 0 &&
+                  (int64_t)left_pad[i] + row_offsets[i] == source_width[i],
+              "plan_merge: row %d is not right-aligned in its source", i);
+    if (row_offsets[i] > width) width = row_offsets[i];
+  }
+  for (int32_t i = 0; i < n_rows; ++i) {
+    const int32_t pad = width - row_offsets[i];
+    shift[i] = left_pad[i] - pad;
+    zero_below[i] = pad;
+    new_left_pad[i] = pad;
+  }
+  *new_width = width;
+  return MLA_OK;
+}
+
+int mla_cache_shift_rows(const void* src, int64_t src_token_stride, int64_t src_batch_stride, int32_t src_batch,
+                         int32_t src_width, void* dst, int64_t dst_token_stride, int64_t dst_batch_stride,
+                         int32_t dst_width, int32_t features, int dtype, const int32_t* src_row,
+                         const int32_t* shift, const int32_t* zero_below, int32_t n_rows, int32_t* device_status,
+                         mla_stream_t stream) {
+  g_detail[0] = 0;
+  MLA_CHECK(dst && (src || src_width == 0), "shift_rows: NULL pointer");
+  MLA_CHECK(valid_dtype(dtype), "shift_rows: bad dtype %d", dtype);
+  MLA_CHECK(features > 0 && src_batch > 0 && src_width >= 0 && dst_width >= 0 && n_rows > 0,
+            "shift_rows: sizes must be positive (widths non-negative)");
+  MLA_CHECK(n_rows <= 65535, "shift_rows: at most 65535 rows per call");
+  MLA_CHECK(src_token_stride >= features && dst_token_stride >= features && src_batch_stride >= 0 &&
+                dst_batch_stride >= 0,
+            "shift_rows: strides too small");
+  MLA_CHECK(n_rows == 1 || dst_batch_stride >= (int64_t)dst_width * dst_token_stride,
+            "shift_rows: destination rows overlap");
+  if (dst_width == 0) return MLA_OK;
+  const int64_t elem = dtype == MLA_DTYPE_F32 ? 4 : 2;
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), d0 = reinterpret_cast<uintptr_t>(dst);
+  const uintptr_t s1 = s0 + (uintptr_t)(((int64_t)(src_batch - 1) * src_batch_stride +
+                                         (int64_t)(src_width - 1) * src_token_stride + features) * elem);
+  const uintptr_t d1 = d0 + (uintptr_t)(((int64_t)(n_rows - 1) * dst_batch_stride +
+                                         (int64_t)(dst_width - 1) * dst_token_stride + features) * elem);
+  MLA_CHECK(src_width == 0 || d1 <= s0 || s1 <= d0,
+            "shift_rows: source and destination overlap (the gather is not in place)");
+  ShiftRowsParams p;
+  memset(&p, 0, sizeof(p));
+  p.src = src;
+  p.src_col_bytes = src_token_stride * elem;
+  p.src_batch_bytes = src_batch_stride * elem;
+  p.src_batch = src_batch;
+  p.src_width = src_width;
+  p.dst = dst;
+  p.dst_col_bytes = dst_token_stride * elem;
+  p.dst_batch_bytes = dst_batch_stride * elem;
+  p.dst_width = dst_width;
+  p.n_rows = n_rows;
+  p.row_bytes = (int64_t)features * elem;
+  p.src_row = src_row;
+  p.shift = shift;
+  p.zero_below = zero_below;
+  p.status = device_status;
+  int vec = 16;
+  while (vec > 2 && ((s0 | d0) % vec || p.src_col_bytes % vec || p.dst_col_bytes % vec ||
+                     p.src_batch_bytes % vec || p.dst_batch_bytes % vec || p.row_bytes % vec))
+    vec >>= 1;
+  return cuda_status(launch_shift_rows(p, vec, (cudaStream_t)stream), "shift_rows launch");
+}
+
+int mla_rollback_lengths(const int32_t* kv_len_before, const int32_t* keep, const int32_t* kv_len,
+                         int32_t* kv_len_out, int32_t batch, int32_t* device_status, mla_stream_t stream) {
+  g_detail[0] = 0;
+  MLA_CHECK(kv_len_before && keep && kv_len && kv_len_out, "rollback_lengths: NULL pointer");
+  MLA_CHECK(batch > 0, "rollback_lengths: batch must be positive");
+  return cuda_status(launch_rollback_lengths(kv_len_before, keep, kv_len, kv_len_out, batch, device_status,
+                                             (cudaStream_t)stream),
+                     "rollback_lengths launch");
 }
 
 }  // extern "C"

@@ -146,6 +146,27 @@ struct SelectParams {
 };
 cudaError_t launch_select_topk(const SelectParams& p, cudaStream_t stream);
 
+// Row gather of a right-aligned cache state array (rollback, filter, merge):
+// dst[i, c] = c < zero_below[i] ? 0 : src[src_row[i], (c + shift[i]) mod src_width].
+// Sizes and strides in bytes.
+struct ShiftRowsParams {
+  const void* src;
+  int64_t src_col_bytes, src_batch_bytes;
+  int32_t src_batch, src_width;
+  void* dst;
+  int64_t dst_col_bytes, dst_batch_bytes;
+  int32_t dst_width, n_rows;
+  int64_t row_bytes;
+  const int32_t* src_row;     // NULL: row i
+  const int32_t* shift;       // NULL: 0
+  const int32_t* zero_below;  // NULL: 0
+  int32_t* status;
+  int32_t units_per_col, cols_per_cta;  // set by the launcher
+};
+cudaError_t launch_shift_rows(const ShiftRowsParams& p, int vec_bytes, cudaStream_t stream);
+cudaError_t launch_rollback_lengths(const int32_t* before, const int32_t* keep, const int32_t* kv_len,
+                                    int32_t* kv_len_out, int32_t batch, int32_t* status, cudaStream_t stream);
+
 // Failure-detection self-test (a bounded wait on a barrier that never completes).
 cudaError_t launch_bounded_wait(long long limit_cycles, int32_t* status, long long* waited, cudaStream_t stream);
 

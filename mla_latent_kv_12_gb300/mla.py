@@ -30,7 +30,8 @@ EXPORTS = (
     "mla_decode_workspace_size", "mla_decode_kernel_kind", "mla_project_v",
     "mla_gather_selected", "mla_decode_attend_no_alloc", "mla_decode_step",
     "mla_decode_step_workspace_size", "mla_append_compressed", "mla_select_topk",
-    "mla_selftest_bounded_wait",
+    "mla_selftest_bounded_wait", "mla_plan_rollback", "mla_plan_filter", "mla_plan_merge",
+    "mla_cache_shift_rows", "mla_rollback_lengths",
 )
 
 
@@ -88,6 +89,14 @@ def _load() -> ctypes.CDLL:
     lib.mla_select_topk.argtypes = [vp, i64, vp, i32, i32, vp, i64, vp, vp, vp]
     lib.mla_selftest_bounded_wait.restype = ctypes.c_int
     lib.mla_selftest_bounded_wait.argtypes = [i64, vp, vp, vp]
+    for name, args in (("mla_plan_rollback", [i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]),
+                       ("mla_plan_filter", [i32, i32, vp, vp, vp, i32, vp, vp, vp, vp]),
+                       ("mla_plan_merge", [i32, vp, vp, vp, vp, vp, vp, vp]),
+                       ("mla_cache_shift_rows", [vp, i64, i64, i32, i32, vp, i64, i64, i32, i32,
+                                                 ctypes.c_int, vp, vp, vp, i32, vp, vp]),
+                       ("mla_rollback_lengths", [vp, vp, vp, vp, i32, vp, vp])):
+        getattr(lib, name).restype = ctypes.c_int
+        getattr(lib, name).argtypes = args
     lib.mla_gather_selected.restype = ctypes.c_int
     lib.mla_gather_selected.argtypes = [vp, i64, i64, vp, i64, i64, ctypes.c_int, vp, vp, i32, i32, i32,
                                         i32, i64, vp, vp, i32, vp, vp, vp]
@@ -274,6 +283,70 @@ def gather_selected(latent: torch.Tensor, rope: torch.Tensor, kv_start, kv_len, 
         _ptr(latent), latent.stride(1), lat_bs, _ptr(rope), rope.stride(1), rope_bs, _dt(latent),
         _ptr(kv_start), _ptr(kv_len), batch, s_q, latent.shape[-1], rope.shape[-1], latent.shape[1],
         _ptr(sel), _ptr(sel_count), k_max, _ptr(out), _ptr(device_status), _stream(stream)))
+    return out
+
+
+# ---------------------------------------------------------------- cache row operations
+
+def _host_i32(values) -> torch.Tensor:
+    t = torch.as_tensor(values, dtype=torch.int32, device="cpu").contiguous()
+    return t
+
+
+def plan_rollback(left_pad, row_offsets, before_offsets, keep, width: int):
+    """Host plan of a speculative-round rollback of a right-aligned cache.
+    Returns ``(shift, new_left_pad, new_row_offsets, new_width)`` (CPU int32 tensors, int)."""
+    lp, ro, bo, kp = (_host_i32(x) for x in (left_pad, row_offsets, before_offsets, keep))
+    B = lp.numel()
+    shift, pad, off = (torch.empty(B, dtype=torch.int32) for _ in range(3))
+    w = ctypes.c_int32(0)
+    _check(lib.mla_plan_rollback(B, int(width), _ptr(lp), _ptr(ro), _ptr(bo), _ptr(kp), _ptr(shift), _ptr(pad),
+                                 _ptr(off), ctypes.addressof(w)))
+    return shift, pad, off, w.value
+
+
+def plan_filter(left_pad, row_offsets, keep_rows, width: int):
+    """Host plan of a row filter. Returns ``(shift, new_left_pad, new_row_offsets, new_width)``."""
+    lp, ro, kr = (_host_i32(x) for x in (left_pad, row_offsets, keep_rows))
+    n = kr.numel()
+    shift, pad, off = (torch.empty(n, dtype=torch.int32) for _ in range(3))
+    w = ctypes.c_int32(0)
+    _check(lib.mla_plan_filter(lp.numel(), int(width), _ptr(lp), _ptr(ro), _ptr(kr), n, _ptr(shift), _ptr(pad),
+                               _ptr(off), ctypes.addressof(w)))
+    return shift, pad, off, w.value
+
+
+def plan_merge(source_width, left_pad, row_offsets):
+    """Host plan of a merge of rows listed in merge order (each with its source's width).
+    Returns ``(shift, zero_below, new_left_pad, new_width)``."""
+    sw, lp, ro = (_host_i32(x) for x in (source_width, left_pad, row_offsets))
+    n = lp.numel()
+    shift, zero, pad = (torch.empty(n, dtype=torch.int32) for _ in range(3))
+    w = ctypes.c_int32(0)
+    _check(lib.mla_plan_merge(n, _ptr(sw), _ptr(lp), _ptr(ro), _ptr(shift), _ptr(zero), _ptr(pad),
+                              ctypes.addressof(w)))
+    return shift, zero, pad, w.value
+
+
+def cache_shift_rows(src: torch.Tensor, dst: torch.Tensor, shift: Optional[torch.Tensor] = None,
+                     src_row: Optional[torch.Tensor] = None, zero_below: Optional[torch.Tensor] = None,
+                     device_status=None, stream=None) -> torch.Tensor:
+    """``dst[i, c] = c < zero_below[i] ? 0 : src[src_row[i], (c + shift[i]) mod width]`` on views
+    ``[B, width, F]`` (last dim contiguous); the index arrays are device int32 ``[dst rows]``."""
+    assert src.dtype == dst.dtype and src.stride(-1) == 1 and dst.stride(-1) == 1
+    _check(lib.mla_cache_shift_rows(_ptr(src), src.stride(1), src.stride(0), src.shape[0], src.shape[1],
+                                    _ptr(dst), dst.stride(1), dst.stride(0), dst.shape[1], src.shape[2],
+                                    _dt(src), _ptr(src_row), _ptr(shift), _ptr(zero_below), dst.shape[0],
+                                    _ptr(device_status), _stream(stream)))
+    return dst
+
+
+def rollback_lengths(kv_len_before: torch.Tensor, keep: torch.Tensor, kv_len: torch.Tensor,
+                     kv_len_out: Optional[torch.Tensor] = None, device_status=None, stream=None) -> torch.Tensor:
+    """Per-row window layout: ``kv_len_out = kv_len_before + keep`` (in place when ``kv_len_out`` is None)."""
+    out = kv_len if kv_len_out is None else kv_len_out
+    _check(lib.mla_rollback_lengths(_ptr(kv_len_before), _ptr(keep), _ptr(kv_len), _ptr(out), kv_len.numel(),
+                                    _ptr(device_status), _stream(stream)))
     return out
 
 

@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -136,3 +137,95 @@ def test_selftest_validation(lib):
     assert L.mla_selftest_bounded_wait(1000, None, None, None) == 1
     assert L.mla_selftest_bounded_wait(0, 16, None, None) == 1
     assert L.mla_selftest_bounded_wait((1 << 32) + 1, 16, None, None) == 1
+
+
+def test_shift_rows_and_rollback_lengths_validation(lib):
+    L = lib.lib
+    # src, token stride, batch stride, src batch, src width, dst, token stride, batch stride, dst width,
+    # features, dtype, src_row, shift, zero_below, n_rows, status, stream
+    MB = 1 << 20
+    args = [16 * MB, 512, 512 * 64, 2, 64, 64 * MB, 512, 512 * 64, 60, 512, 1, None, None, None, 2, None, None]
+    for i, v in [(0, None), (5, None), (10, 5), (9, 0), (14, 0), (14, 70000), (1, 256), (6, 256), (7, 512),
+                 (4, -1), (8, -1), (5, 16 * MB + 4096)]:          # the last one: destination overlaps source
+        bad = list(args); bad[i] = v
+        assert L.mla_cache_shift_rows(*bad) == 1, i
+    assert "overlap" in L.mla_last_error_detail().decode()
+    zero_width = list(args); zero_width[8] = 0                    # nothing to write: no launch, ok
+    assert L.mla_cache_shift_rows(*zero_width) == 0
+    assert L.mla_rollback_lengths(None, 16, 16, 16, 4, None, None) == 1
+    assert L.mla_rollback_lengths(16, 16, 16, 16, 0, None, None) == 1
+
+
+# ------------------------------------------------ host plans of the cache row operations
+
+def _right_aligned(rng_, B, width, lo=0):
+    offs = rng_.integers(lo, width + 1, B)
+    return width - offs, offs
+
+
+def _apply_plan(a, width_out, shift, src_row=None, zero_below=None):
+    """The gather the row kernel performs, per its contract, on a host array."""
+    B_out = len(shift)
+    out = np.zeros((B_out, width_out, a.shape[2]), a.dtype)
+    for i in range(B_out):
+        r = i if src_row is None else src_row[i]
+        for c in range(width_out):
+            if zero_below is not None and c < zero_below[i]:
+                continue
+            out[i, c] = a[r, (c + int(shift[i])) % a.shape[1]]
+    return out
+
+
+def test_rollback_plan_matches_the_oracle(lib):
+    from oracle import mla_oracle as O
+    r = np.random.default_rng(80)
+    for trial in range(20):
+        B, appended = int(r.integers(1, 6)), int(r.integers(0, 5))
+        width = int(r.integers(appended, 20))
+        pad, offs = _right_aligned(r, B, width, lo=appended)
+        before = offs - appended
+        keep = r.integers(0, appended + 1, B)
+        a = r.standard_normal((B, width, 3))
+        shift, new_pad, new_off, new_width = lib.plan_rollback(pad, offs, before, keep, width)
+        (want,), w, off_o, pad_o = O.rollback_right_aligned([a], pad, offs, before, keep)
+        assert new_width == w and list(new_off) == list(off_o) and list(new_pad) == list(pad_o)
+        assert np.array_equal(_apply_plan(a, new_width, shift.numpy()), want)
+
+
+def test_filter_and_merge_plans_match_the_oracle(lib):
+    from oracle import mla_oracle as O
+    r = np.random.default_rng(81)
+    for trial in range(20):
+        B, width = int(r.integers(1, 6)), int(r.integers(1, 16))
+        pad, offs = _right_aligned(r, B, width)
+        a = r.standard_normal((B, width, 2))
+        for b in range(B):
+            a[b, :pad[b]] = 0.0
+        keep = r.integers(0, B, int(r.integers(1, B + 2)))
+        shift, new_pad, new_off, new_width = lib.plan_filter(pad, offs, keep, width)
+        (want,), w, off_o, pad_o = O.filter_right_aligned([a], pad, offs, keep)
+        assert new_width == w and list(new_off) == list(off_o) and list(new_pad) == list(pad_o)
+        assert np.array_equal(_apply_plan(a, new_width, shift.numpy(), src_row=keep), want)
+        # merge this cache with a second one of another width
+        B2, width2 = int(r.integers(1, 4)), int(r.integers(1, 24))
+        pad2, offs2 = _right_aligned(r, B2, width2)
+        a2 = r.standard_normal((B2, width2, 2))
+        shift, zero, new_pad, w_m = lib.plan_merge([width] * B + [width2] * B2, list(pad) + list(pad2),
+                                                   list(offs) + list(offs2))
+        (want,), w, off_o, pad_o = O.merge_right_aligned([([a], pad, offs), ([a2], pad2, offs2)])
+        assert w_m == w and list(new_pad) == list(pad_o)
+        if w:
+            got = np.concatenate([_apply_plan(a, w, shift[:B].numpy(), zero_below=zero[:B].numpy()),
+                                  _apply_plan(a2, w, shift[B:].numpy(), zero_below=zero[B:].numpy())])
+            assert np.array_equal(got, want)
+
+
+def test_row_plans_reject_bad_bookkeeping(lib):
+    with pytest.raises(lib.MLAError, match="right-aligned"):
+        lib.plan_rollback([1, 0], [3, 3], [1, 1], [0, 0], 4)             # 0 + 3 != 4
+    with pytest.raises(lib.MLAError, match="keeps"):
+        lib.plan_rollback([0, 1], [4, 3], [2, 2], [3, 0], 4)             # keeps 5 of 4
+    with pytest.raises(lib.MLAError, match="outside"):
+        lib.plan_filter([0, 1], [4, 3], [2], 4)
+    with pytest.raises(lib.MLAError, match="right-aligned"):
+        lib.plan_merge([4, 5], [0, 1], [4, 3])
