@@ -14,6 +14,8 @@
  *   - rmsNormF32Mlx and the append of Glm52Mla.project / forward
  *                                        -> mla_append_compressed
  *   - the composition of the four decode operations -> mla_decode_step
+ *   - Glm52Mla.attendReconstructed (prefill: per-head K/V materialised)
+ *                                        -> mla_reconstruct_kv + mla_prefill_attend
  * and "mlx-bun ... glm52-dsa.ts", selectGlm52DsaDevice -> mla_select_topk,
  * and "mlx-bun 0.2.0 -> 0.4.0, glm52-cache.ts", Glm52Cache.specRoundRollback,
  * filter and mergeRows -> mla_plan_rollback / mla_plan_filter /
@@ -415,6 +417,55 @@ int mla_cache_shift_rows(const void* src, int64_t src_token_stride, int64_t src_
  */
 int mla_rollback_lengths(const int32_t* kv_len_before, const int32_t* keep, const int32_t* kv_len,
                          int32_t* kv_len_out, int32_t batch, int32_t* device_status, mla_stream_t stream);
+
+/*
+ * Reconstructed prefill (the MLA page, Glm52Mla.attendReconstructed, with the
+ * left-pad mask of the "mlx-bun 0.2.0 -> 0.4.0" hunk).  For a long block of
+ * new tokens the per-head keys and values are materialised once and
+ * attention runs in its plain form.
+ *
+ * mla_reconstruct_kv: for rows t < n_rows of latent [n_rows, rank] (row
+ * stride in elements) and head h < heads,
+ *   k_nope[t, h, :] = latent[t, :] . W_UK_h^T   (W_UK_h = kv_b_proj rows
+ *                                                h*(nope+v_dim) .. +nope)
+ *   v[t, h, :]      = latent[t, :] . W_UV_h^T   (the next v_dim rows)
+ * kv_b_proj is [heads*(nope+v_dim), rank] contiguous.  k_nope / v element
+ * (t, h, d) sits at t*row_stride + h*head_stride + d.  bf16 in and out, f32
+ * accumulation.  Served: bf16, nope = v_dim = 128, rank a multiple of 64 up
+ * to 1024, 16-byte aligned pointers and strides; other requests return
+ * MLA_ERR_UNSUPPORTED.  The rope part of the keys is not materialised: it is
+ * the cache's rope key, shared by all heads.
+ *
+ * mla_prefill_attend: query token i < s_q of batch row b (query row n =
+ * b*s_q + i) attends, for every head, to the window keys t <= kv_len[b] -
+ * s_q + i of buffer rows kv_start[b] + t (the block's own tokens are the
+ * window's last s_q keys; kv_start is the page's left pad), with
+ *   score = (q_nope[n,h,:] . k_nope[row,h,:] + q_rope[n,h,:] . rope[row,:]) * softmax_scale
+ * and writes out[n, h*v_dim + d] = sum_t softmax(score)_t v[row, h, d]
+ * (heads concatenated, out_dtype) and lse_out[n*heads + h] (natural log of
+ * the softmax denominator, may be NULL).  q_rope must already be rotated
+ * (mla_rope_partial_interleaved).  Buffer rows of batch row b start at
+ * b*t_max, or all batch rows share rows 0..t_max-1 when `packed` is
+ * non-zero; k_nope, v and rope are indexed by the same buffer row.  A query
+ * token with no visible key (kv_len < s_q) gets zeros and lse = -inf.  A
+ * window outside [0, t_max) sets MLA_DEVICE_INDEX_OUT_OF_RANGE and that
+ * batch row is skipped.  Served: bf16 with nope 128, rope 64, v_dim 128,
+ * 16-byte aligned pointers and strides (out_row_stride a multiple of 8);
+ * other requests return MLA_ERR_UNSUPPORTED.
+ */
+int mla_reconstruct_kv(const void* latent, int64_t latent_row_stride, int64_t n_rows, const void* kv_b_proj,
+                       int32_t heads, int32_t nope, int32_t v_dim, int32_t rank, void* k_nope,
+                       int64_t k_row_stride, int64_t k_head_stride, void* v, int64_t v_row_stride,
+                       int64_t v_head_stride, int dtype, int32_t* device_status, mla_stream_t stream);
+
+int mla_prefill_attend(const void* q_nope, int64_t q_nope_row_stride, int64_t q_nope_head_stride,
+                       const void* q_rope, int64_t q_rope_row_stride, int64_t q_rope_head_stride,
+                       const void* k_nope, int64_t k_row_stride, int64_t k_head_stride, const void* v,
+                       int64_t v_row_stride, int64_t v_head_stride, const void* rope, int64_t rope_row_stride,
+                       int packed, int dtype, const int32_t* kv_start, const int32_t* kv_len, int32_t batch,
+                       int32_t s_q, int32_t heads, int32_t nope, int32_t rope_dim, int32_t v_dim, int64_t t_max,
+                       float softmax_scale, void* out, int64_t out_row_stride, int out_dtype, float* lse_out,
+                       int32_t* device_status, mla_stream_t stream);
 
 /*
  * Test hook: the selected-position gather of attendAbsorbed (takeAxis on

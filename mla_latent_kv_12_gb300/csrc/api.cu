@@ -631,4 +631,97 @@ int mla_rollback_lengths(const int32_t* kv_len_before, const int32_t* keep, cons
                      "rollback_lengths launch");
 }
 
+// ------------------------------------------------------------ reconstructed prefill
+
+int mla_reconstruct_kv(const void* latent, int64_t latent_row_stride, int64_t n_rows, const void* kv_b_proj,
+                       int32_t heads, int32_t nope, int32_t v_dim, int32_t rank, void* k_nope,
+                       int64_t k_row_stride, int64_t k_head_stride, void* v, int64_t v_row_stride,
+                       int64_t v_head_stride, int dtype, int32_t* device_status, mla_stream_t stream) {
+  g_detail[0] = 0;
+  MLA_CHECK(latent && kv_b_proj && k_nope && v, "reconstruct: NULL pointer");
+  MLA_CHECK(valid_dtype(dtype), "reconstruct: bad dtype %d", dtype);
+  MLA_CHECK(n_rows > 0 && heads > 0 && nope > 0 && v_dim > 0 && rank > 0, "reconstruct: sizes must be positive");
+  MLA_CHECK(n_rows < ((int64_t)1 << 31), "reconstruct: at most 2^31 - 1 rows");
+  MLA_CHECK(latent_row_stride >= rank && k_head_stride >= nope && v_head_stride >= v_dim && k_row_stride >= 0 &&
+                v_row_stride >= 0,
+            "reconstruct: strides too small");
+  if (!(dtype == MLA_DTYPE_BF16 && nope == 128 && v_dim == 128 && rank % 64 == 0 && rank <= 1024 &&
+        heads <= 65535))
+    return fail(MLA_ERR_UNSUPPORTED, "reconstruct: served for bf16, nope = v = 128, rank a multiple of 64 "
+                                     "up to 1024");
+  MLA_CHECK(aligned16(latent) && aligned16(kv_b_proj) && aligned16(k_nope) && aligned16(v) &&
+                latent_row_stride % 8 == 0 && k_row_stride % 8 == 0 && k_head_stride % 8 == 0 &&
+                v_row_stride % 8 == 0 && v_head_stride % 8 == 0,
+            "reconstruct: pointers and strides must be 16-byte aligned");
+  ReconstructParams p{latent, latent_row_stride, n_rows, kv_b_proj, heads, nope, v_dim, rank, k_nope,
+                      k_row_stride, k_head_stride, v, v_row_stride, v_head_stride, device_status};
+  return cuda_status(launch_tc_reconstruct(p, (cudaStream_t)stream), "reconstruct launch");
+}
+
+int mla_prefill_attend(const void* q_nope, int64_t q_nope_row_stride, int64_t q_nope_head_stride,
+                       const void* q_rope, int64_t q_rope_row_stride, int64_t q_rope_head_stride,
+                       const void* k_nope, int64_t k_row_stride, int64_t k_head_stride, const void* v,
+                       int64_t v_row_stride, int64_t v_head_stride, const void* rope, int64_t rope_row_stride,
+                       int packed, int dtype, const int32_t* kv_start, const int32_t* kv_len, int32_t batch,
+                       int32_t s_q, int32_t heads, int32_t nope, int32_t rope_dim, int32_t v_dim, int64_t t_max,
+                       float softmax_scale, void* out, int64_t out_row_stride, int out_dtype, float* lse_out,
+                       int32_t* device_status, mla_stream_t stream) {
+  g_detail[0] = 0;
+  MLA_CHECK(q_nope && q_rope && k_nope && v && rope && kv_start && kv_len && out, "prefill: NULL pointer");
+  MLA_CHECK(valid_dtype(dtype) && valid_dtype(out_dtype), "prefill: bad dtype");
+  MLA_CHECK(batch > 0 && s_q > 0 && heads > 0 && nope > 0 && rope_dim > 0 && v_dim > 0 && t_max > 0,
+            "prefill: sizes must be positive");
+  MLA_CHECK(isfinite(softmax_scale) && softmax_scale > 0.f, "prefill: softmax scale must be positive and finite");
+  MLA_CHECK(q_nope_head_stride >= nope && q_rope_head_stride >= rope_dim && k_head_stride >= nope &&
+                v_head_stride >= v_dim && rope_row_stride >= rope_dim && q_nope_row_stride >= 0 &&
+                q_rope_row_stride >= 0 && k_row_stride >= 0 && v_row_stride >= 0 &&
+                out_row_stride >= (int64_t)heads * v_dim,
+            "prefill: strides too small");
+  const int64_t buf_rows = packed ? t_max : (int64_t)batch * t_max;
+  MLA_CHECK(buf_rows < ((int64_t)1 << 31) && (int64_t)batch * s_q < ((int64_t)1 << 31),
+            "prefill: at most 2^31 - 1 buffer rows and query rows");
+  if (!(dtype == MLA_DTYPE_BF16 && nope == 128 && rope_dim == 64 && v_dim == 128 && heads <= 65535 &&
+        batch <= 65535))
+    return fail(MLA_ERR_UNSUPPORTED, "prefill: served for bf16 with nope 128, rope 64, v 128");
+  MLA_CHECK(aligned16(q_nope) && aligned16(q_rope) && aligned16(k_nope) && aligned16(v) && aligned16(rope) &&
+                aligned16(out) && q_nope_row_stride % 8 == 0 && q_nope_head_stride % 8 == 0 &&
+                q_rope_row_stride % 8 == 0 && q_rope_head_stride % 8 == 0 && k_row_stride % 8 == 0 &&
+                k_head_stride % 8 == 0 && v_row_stride % 8 == 0 && v_head_stride % 8 == 0 &&
+                rope_row_stride % 8 == 0 && out_row_stride % 8 == 0,
+            "prefill: pointers and strides must be 16-byte aligned");
+  PrefillParams p;
+  memset(&p, 0, sizeof(p));
+  p.q_nope = q_nope;
+  p.qn_row_stride = q_nope_row_stride;
+  p.qn_head_stride = q_nope_head_stride;
+  p.q_rope = q_rope;
+  p.qr_row_stride = q_rope_row_stride;
+  p.qr_head_stride = q_rope_head_stride;
+  p.k_nope = k_nope;
+  p.k_row_stride = k_row_stride;
+  p.k_head_stride = k_head_stride;
+  p.v = v;
+  p.v_row_stride = v_row_stride;
+  p.v_head_stride = v_head_stride;
+  p.rope = rope;
+  p.rope_row_stride = rope_row_stride;
+  p.kv_start = kv_start;
+  p.kv_len = kv_len;
+  p.t_max = t_max;
+  p.packed = packed ? 1 : 0;
+  p.batch = batch;
+  p.s_q = s_q;
+  p.heads = heads;
+  p.nope = nope;
+  p.rope_dim = rope_dim;
+  p.v_dim = v_dim;
+  p.softmax_scale = softmax_scale;
+  p.out = out;
+  p.out_row_stride = out_row_stride;
+  p.out_dtype = out_dtype;
+  p.lse = lse_out;
+  p.status = device_status;
+  return cuda_status(launch_tc_prefill(p, (cudaStream_t)stream), "prefill launch");
+}
+
 }  // extern "C"

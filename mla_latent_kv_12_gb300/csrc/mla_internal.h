@@ -167,6 +167,46 @@ cudaError_t launch_shift_rows(const ShiftRowsParams& p, int vec_bytes, cudaStrea
 cudaError_t launch_rollback_lengths(const int32_t* before, const int32_t* keep, const int32_t* kv_len,
                                     int32_t* kv_len_out, int32_t batch, int32_t* status, cudaStream_t stream);
 
+// Reconstruction of per-head keys and values from latent rows (prefill).
+struct ReconstructParams {
+  const void* latent;
+  int64_t latent_row_stride, n_rows;
+  const void* kv_b_proj;
+  int32_t heads, nope, v_dim, rank;
+  void* k_nope;
+  int64_t k_row_stride, k_head_stride;
+  void* v;
+  int64_t v_row_stride, v_head_stride;
+  int32_t* status;
+};
+cudaError_t launch_tc_reconstruct(const ReconstructParams& p, cudaStream_t stream);
+
+// Causal prefill attention over materialised per-head keys / values.
+struct PrefillParams {
+  const void* q_nope;
+  int64_t qn_row_stride, qn_head_stride;
+  const void* q_rope;
+  int64_t qr_row_stride, qr_head_stride;
+  const void* k_nope;
+  int64_t k_row_stride, k_head_stride;
+  const void* v;
+  int64_t v_row_stride, v_head_stride;
+  const void* rope;
+  int64_t rope_row_stride;
+  const int32_t* kv_start;
+  const int32_t* kv_len;
+  int64_t t_max;
+  int32_t packed;
+  int32_t batch, s_q, heads, nope, rope_dim, v_dim;
+  float softmax_scale;
+  void* out;
+  int64_t out_row_stride;
+  int32_t out_dtype;
+  float* lse;
+  int32_t* status;
+};
+cudaError_t launch_tc_prefill(const PrefillParams& p, cudaStream_t stream);
+
 // Failure-detection self-test (a bounded wait on a barrier that never completes).
 cudaError_t launch_bounded_wait(long long limit_cycles, int32_t* status, long long* waited, cudaStream_t stream);
 

@@ -1,0 +1,611 @@
+// Reconstructed prefill attention on tcgen05 ("glm52-mla.ts",
+// Glm52Mla.attendReconstructed, with the left-pad mask of the 0.2.0 -> 0.4.0
+// hunk): for a long block of new tokens the per-head keys and values are
+// materialised once and attention runs in its plain form, which costs
+// 2*H*(nope+rope+v) flops per (query, key) pair instead of the absorbed
+// form's 2*H*(2*rank+rope).
+//
+//   tc_reconstruct_kernel  K_nope[t,h,:] = latent[t,:] . W_UK_h^T,
+//                          V[t,h,:]      = latent[t,:] . W_UV_h^T
+//     grid (row tiles of 128, heads), one tcgen05 MMA chain M=128 tokens x
+//     N=256 (head h's 256 rows of kv_b_proj) x K=rank, fed by a 4-stage TMA
+//     ring; the f32 accumulator is rounded to bf16 into swizzled shared memory
+//     and written with TMA tensor stores.
+//
+//   tc_prefill_kernel      causal flash attention, one CTA per (128 query
+//     rows, head, batch row).  Q (nope || rotated rope, 192 features) stays
+//     in shared memory; each 128-key tile brings K_nope, the cache's shared
+//     rope key and V by TMA (two stages).  Warp 1 issues S(j+1) = Q.K^T into
+//     one of two TMEM score buffers while the four softmax warps (one query
+//     row per thread) turn S(j) into bf16 P in place; then it issues
+//     O += P.V with P read from TMEM.  The running maximum is only moved when
+//     it grows by more than 2^8 (the accumulated O and sum are then rescaled
+//     in TMEM), so most tiles skip the correction.
+#include <cuda_bf16.h>
+#include <math.h>
+#include <string.h>
+
+#include "mla_internal.h"
+#include "tc_common.cuh"
+#include "tc_host.h"
+
+namespace mla {
+namespace {
+
+using namespace tc;
+
+constexpr long long kWaitLimit = 1LL << 32;  // clock cycles (~2 s)
+constexpr int kChunk = 128 * 128;            // 128 rows x 64 bf16 (one 128-byte swizzle atom column)
+
+__device__ __forceinline__ void tma_store_3d(const void* tmap, const void* src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+               ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Offset of 16-byte unit u of row r in a 128-byte-swizzled chunk.
+__device__ __forceinline__ uint32_t sw128(int r, int u) { return (uint32_t)(r * 128 + ((u ^ (r & 7)) << 4)); }
+
+// ------------------------------------------------------------------ reconstruct
+
+constexpr int RC_STAGES = 4;
+constexpr int RC_A_BYTES = kChunk;          // 128 tokens x 64 latent features
+constexpr int RC_B_BYTES = 2 * kChunk;      // 256 weight rows x 64 latent features
+constexpr int RC_STAGE_BYTES = RC_A_BYTES + RC_B_BYTES;
+constexpr int RC_SMEM = 1024 + RC_STAGES * RC_STAGE_BYTES;
+constexpr int RC_THREADS = 192;
+
+struct ReconArgs {
+  int32_t k_chunks;     // rank / 64
+  int32_t head_rows;    // nope + v rows of kv_b_proj per head
+  int32_t* status;
+};
+
+__global__ void __launch_bounds__(RC_THREADS, 1)
+    tc_reconstruct_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__ CUtensorMap w_map,
+                          const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
+                          const __grid_constant__ ReconArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full_bar[RC_STAGES], empty_bar[RC_STAGES], mma_done;
+  __shared__ uint32_t tmem_s;
+  __shared__ volatile int abort_s;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row0 = blockIdx.x * 128, h = blockIdx.y;
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&lat_map);
+    tma_prefetch_desc(&w_map);
+    tma_prefetch_desc(&k_map);
+    tma_prefetch_desc(&v_map);
+    for (int s = 0; s < RC_STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(&mma_done, 1);
+    abort_s = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_s, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_s;
+  auto fail = [&]() {
+    abort_s = 1;
+    if (a.status) atomicOr(a.status, MLA_DEVICE_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    bool issued[RC_STAGES] = {false, false, false, false};
+    uint32_t issued_phase[RC_STAGES] = {0, 0, 0, 0};
+    if (lane == 0) {
+      for (int kc = 0; kc < a.k_chunks && !abort_s; ++kc) {
+        const int s = kc % RC_STAGES;
+        const uint32_t ph = (uint32_t)(kc / RC_STAGES) & 1u;
+        if (kc >= RC_STAGES && !mbar_wait(&empty_bar[s], ph ^ 1u, kWaitLimit)) { fail(); break; }
+        uint8_t* st = smem + s * RC_STAGE_BYTES;
+        mbar_arrive_expect_tx(&full_bar[s], RC_STAGE_BYTES);
+        tma_load_2d(st, &lat_map, &full_bar[s], kc * 64, row0);
+        tma_load_2d(st + RC_A_BYTES, &w_map, &full_bar[s], kc * 64, h * a.head_rows);
+        issued[s] = true;
+        issued_phase[s] = ph;
+      }
+      for (int s = 0; s < RC_STAGES; ++s)
+        if (issued[s]) mbar_wait(&full_bar[s], issued_phase[s], kWaitLimit);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    const uint32_t idesc = idesc_bf16_f32(128, 256, 0, 0);
+    for (int kc = 0; kc < a.k_chunks; ++kc) {
+      const int s = kc % RC_STAGES;
+      if (!mbar_wait_warp(&full_bar[s], (uint32_t)(kc / RC_STAGES) & 1u, kWaitLimit)) { fail(); break; }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t a0 = smem_u32(smem + s * RC_STAGE_BYTES), b0 = a0 + RC_A_BYTES;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ss(tmem, smem_desc(a0 + k * 32, 16, 1024, kSwizzle128B), smem_desc(b0 + k * 32, 16, 1024, kSwizzle128B),
+                 idesc, (kc | k) != 0);
+        mma_commit(&empty_bar[s]);
+      }
+      __syncwarp();
+    }
+    if (lane == 0) mma_commit(&mma_done);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ epilogue (warps 2..5)
+    const int quarter = warp & 3;
+    const int r = 32 * quarter + lane;                     // token row of the tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
+    const bool ok = mbar_wait_warp(&mma_done, 0, kWaitLimit);
+    if (!ok) fail();
+    if (ok && !abort_s) {
+      tc_fence_after();
+      // Chunks 0,1 = K_nope features 0..63, 64..127; chunks 2,3 = V.
+#pragma unroll 1
+      for (int p = 0; p < 8; ++p) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + p * 32, v);
+        tmem_wait_ld();
+        uint8_t* chunk = smem + (p >> 1) * kChunk;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1]));
+          w.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3]));
+          w.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5]));
+          w.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7]));
+          *reinterpret_cast<uint4*>(chunk + sw128(r, (p & 1) * 4 + u)) = w;
+        }
+      }
+      fence_proxy_async_smem();
+    }
+    named_sync(1, 128);
+    if (ok && !abort_s && warp == 2 && lane == 0) {
+      tma_store_3d(&k_map, smem, 0, h, row0);
+      tma_store_3d(&k_map, smem + kChunk, 64, h, row0);
+      tma_store_3d(&v_map, smem + 2 * kChunk, 0, h, row0);
+      tma_store_3d(&v_map, smem + 3 * kChunk, 64, h, row0);
+      bulk_commit();
+      bulk_wait_all();
+    }
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// ------------------------------------------------------------------ prefill attention
+
+constexpr int PF_STAGES = 2;
+constexpr int PF_Q_BYTES = 3 * kChunk;        // nope 0..63 | nope 64..127 | rope
+constexpr int PF_STAGE_BYTES = 5 * kChunk;    // K_nope x2 | rope | V x2
+constexpr int PF_SMEM = 1024 + PF_Q_BYTES + PF_STAGES * PF_STAGE_BYTES;
+constexpr int PF_THREADS = 192;
+constexpr uint32_t PF_TM_O = 256;             // TMEM: S0 at 0, S1 at 128, O at 256
+constexpr float kRescaleLog2 = 8.f;
+
+struct PrefillArgs {
+  const int32_t* kv_start;
+  const int32_t* kv_len;
+  int64_t t_max;         // buffer rows of one batch row (the packed buffer's rows when packed)
+  int32_t packed;        // all batch rows share one buffer row range
+  int32_t batch, s_q, n_qtiles;
+  float scale_log2;      // softmax scale * log2(e)
+  void* out;
+  int64_t out_row_stride;
+  int32_t v_dim, out_f32;
+  float* lse;
+  int32_t* status;
+};
+
+__global__ void __launch_bounds__(PF_THREADS, 1)
+    tc_prefill_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_constant__ CUtensorMap qr_map,
+                      const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap r_map,
+                      const __grid_constant__ CUtensorMap v_map, const __grid_constant__ PrefillArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* stages = smem + PF_Q_BYTES;
+  __shared__ __align__(8) uint64_t q_full, full_bar[PF_STAGES], empty_bar[PF_STAGES], s_full[2], p_full, pv_done,
+      mma_drain;
+  __shared__ uint32_t tmem_s;
+  __shared__ volatile int abort_s;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = a.n_qtiles - 1 - (int)blockIdx.x;       // longest causal rows first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int i0 = qt * 128;
+
+  const int64_t start = a.kv_start[b], len = a.kv_len[b];
+  if (start < 0 || len < 0 || start + len > a.t_max) {
+    if (threadIdx.x == 0 && a.status) atomicOr(a.status, MLA_DEVICE_INDEX_OUT_OF_RANGE);
+    return;
+  }
+  // Token i of the block sits at window position len - s_q + i and sees the
+  // keys at or before it.
+  const int64_t offs = len - a.s_q;
+  const int64_t i_hi = min((int64_t)i0 + 127, (int64_t)a.s_q - 1);
+  const int64_t key_end = min(len, offs + i_hi + 1);
+  const int n_kt = key_end > 0 ? (int)((key_end + 127) / 128) : 0;
+  const int64_t ybase = (a.packed ? 0 : (int64_t)b * a.t_max) + start;
+  const int q_row0 = b * a.s_q + i0;
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&qn_map);
+    tma_prefetch_desc(&qr_map);
+    tma_prefetch_desc(&k_map);
+    tma_prefetch_desc(&r_map);
+    tma_prefetch_desc(&v_map);
+    mbar_init(&q_full, 1);
+    for (int s = 0; s < PF_STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
+    mbar_init(&p_full, 128);
+    mbar_init(&pv_done, 1);
+    mbar_init(&mma_drain, 1);
+    abort_s = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_s, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_s;
+  auto fail = [&]() {
+    abort_s = 1;
+    if (a.status) atomicOr(a.status, MLA_DEVICE_TIMEOUT);
+  };
+  auto aborted = [&]() -> bool { return __any_sync(0xffffffffu, abort_s != 0); };
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    bool issued[PF_STAGES] = {false, false};
+    uint32_t issued_phase[PF_STAGES] = {0, 0};
+    bool q_issued = false;
+    if (lane == 0 && n_kt > 0) {
+      mbar_arrive_expect_tx(&q_full, PF_Q_BYTES);
+      tma_load_3d(sQ, &qn_map, &q_full, 0, h, q_row0);
+      tma_load_3d(sQ + kChunk, &qn_map, &q_full, 64, h, q_row0);
+      tma_load_3d(sQ + 2 * kChunk, &qr_map, &q_full, 0, h, q_row0);
+      q_issued = true;
+      for (int kt = 0; kt < n_kt && !abort_s; ++kt) {
+        const int s = kt % PF_STAGES;
+        const uint32_t ph = (uint32_t)(kt / PF_STAGES) & 1u;
+        if (kt >= PF_STAGES && !mbar_wait(&empty_bar[s], ph ^ 1u, kWaitLimit)) { fail(); break; }
+        uint8_t* st = stages + s * PF_STAGE_BYTES;
+        const int y = (int)(ybase + (int64_t)kt * 128);
+        mbar_arrive_expect_tx(&full_bar[s], PF_STAGE_BYTES);
+        tma_load_3d(st, &k_map, &full_bar[s], 0, h, y);
+        tma_load_3d(st + kChunk, &k_map, &full_bar[s], 64, h, y);
+        tma_load_2d(st + 2 * kChunk, &r_map, &full_bar[s], 0, y);
+        tma_load_3d(st + 3 * kChunk, &v_map, &full_bar[s], 0, h, y);
+        tma_load_3d(st + 4 * kChunk, &v_map, &full_bar[s], 64, h, y);
+        issued[s] = true;
+        issued_phase[s] = ph;
+      }
+      // Every issued copy lands before the CTA may exit.
+      if (q_issued) mbar_wait(&q_full, 0, kWaitLimit);
+      for (int s = 0; s < PF_STAGES; ++s)
+        if (issued[s]) mbar_wait(&full_bar[s], issued_phase[s], kWaitLimit);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+    const uint32_t idesc_pv = idesc_bf16_f32(128, 128, 0, 1);
+    auto issue_s = [&](int j) -> bool {
+      const int s = j % PF_STAGES;
+      if (!mbar_wait_warp(&full_bar[s], (uint32_t)(j / PF_STAGES) & 1u, kWaitLimit)) return false;
+      uint8_t* st = stages + s * PF_STAGE_BYTES;
+      const int64_t valid = len - (int64_t)j * 128;
+      if (valid < 128) {
+        // Tail tile: clear the V rows past the window, so that P = 0 never
+        // meets a non-finite value of rows this call does not own.
+        const int v0 = valid < 0 ? 0 : (int)valid;
+        for (int q = lane; q < (128 - v0) * 16; q += 32) {
+          const int c = q / ((128 - v0) * 8), rem = q % ((128 - v0) * 8);
+          *reinterpret_cast<uint4*>(st + (3 + c) * kChunk + (v0 + rem / 8) * 128 + (rem % 8) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(st);
+#pragma unroll
+        for (int c = 0; c < 3; ++c)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tmem + (uint32_t)((j & 1) * 128),
+                   smem_desc(q0 + c * kChunk + k * 32, 16, 1024, kSwizzle128B),
+                   smem_desc(k0 + c * kChunk + k * 32, 16, 1024, kSwizzle128B), idesc_s, (c | k) != 0);
+        mma_commit(&s_full[j & 1]);
+      }
+      __syncwarp();
+      return true;
+    };
+    bool ok = n_kt == 0 || mbar_wait_warp(&q_full, 0, kWaitLimit);
+    if (ok && n_kt > 0) ok = issue_s(0);
+    for (int j = 0; ok && j < n_kt; ++j) {
+      if (j + 1 < n_kt && !issue_s(j + 1)) { ok = false; break; }
+      if (!mbar_wait_warp(&p_full, (uint32_t)j & 1u, kWaitLimit)) { ok = false; break; }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t v0 = smem_u32(stages + (j % PF_STAGES) * PF_STAGE_BYTES + 3 * kChunk);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ts(tmem + PF_TM_O, tmem + (uint32_t)((j & 1) * 128 + k * 8),
+                 smem_desc(v0 + k * 2048, kChunk, 1024, kSwizzle128B), idesc_pv, (j | k) != 0);
+        mma_commit(&empty_bar[j % PF_STAGES]);
+        mma_commit(&pv_done);
+      }
+      __syncwarp();
+      if (aborted()) { ok = false; break; }
+    }
+    if (!ok) fail();
+    // No MMA may be in flight when TMEM is released.
+    if (lane == 0) mma_commit(&mma_drain);
+    __syncwarp();
+    mbar_wait_warp(&mma_drain, 0, kWaitLimit);
+  } else {
+    // ------------------------------------------------ softmax + epilogue (warps 2..5)
+    const int quarter = warp & 3;
+    const int r = 32 * quarter + lane;
+    const int i = i0 + r;
+    const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
+    const int64_t limit = i < a.s_q ? offs + i : -1;       // last visible window position
+    const int64_t min_limit = offs + i0;                   // the tile's first row
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kt; ++j) {
+      if (!mbar_wait_warp(&s_full[j & 1], (uint32_t)(j >> 1) & 1u, kWaitLimit)) { ok = false; break; }
+      tc_fence_after();
+      float x[128];
+      {
+        uint32_t v[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(tmem + lane_off + (uint32_t)((j & 1) * 128 + c * 32), v);
+          tmem_wait_ld_regs(v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[e]) * a.scale_log2;
+        }
+      }
+      const int64_t kbase = (int64_t)j * 128;
+      const bool full = (kbase + 127 <= min_limit) && (kbase + 127 < len);
+      if (!full) {
+#pragma unroll
+        for (int e = 0; e < 128; ++e)
+          if (kbase + e > limit) x[e] = -INFINITY;
+      }
+      float mx = x[0];
+#pragma unroll
+      for (int e = 1; e < 128; ++e) mx = fmaxf(mx, x[e]);
+      // Move the running maximum only when it grows by more than 2^8.
+      const bool move = mx > m_used + kRescaleLog2;
+      float alpha = 1.f;
+      if (move) {
+        alpha = (m_used == -INFINITY) ? 0.f : ex2_approx(m_used - mx);
+        m_used = mx;
+        l *= alpha;
+      }
+      uint32_t pk[64];
+      float sum = 0.f;
+      if (m_used == -INFINITY) {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) pk[e] = 0u;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+          const float p0 = ex2_approx(x[2 * e] - m_used), p1 = ex2_approx(x[2 * e + 1] - m_used);
+          sum += p0 + p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+      }
+      l += sum;
+      // O holds P(0..j-1).V once the previous P.V is done; correct it in place
+      // (warp-uniform: tcgen05.ld/st are collective).
+      if (j > 0) {
+        if (!mbar_wait_warp(&pv_done, (uint32_t)(j - 1) & 1u, kWaitLimit)) { ok = false; break; }
+        if (__any_sync(0xffffffffu, move)) {
+          tc_fence_after();
+          const float f = move ? alpha : 1.f;
+          uint32_t v[32];
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld32(tmem + lane_off + PF_TM_O + c * 32, v);
+            tmem_wait_ld_regs(v);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * f);
+            tmem_st32(tmem + lane_off + PF_TM_O + c * 32, v);
+          }
+        }
+      }
+      {
+        uint32_t (&p0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
+        uint32_t (&p1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
+        tmem_st32(tmem + lane_off + (uint32_t)((j & 1) * 128), p0);
+        tmem_st32(tmem + lane_off + (uint32_t)((j & 1) * 128 + 32), p1);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&p_full);
+      if (aborted()) { ok = false; break; }
+    }
+    if (ok && n_kt > 0) {
+      ok = mbar_wait_warp(&pv_done, (uint32_t)(n_kt - 1) & 1u, kWaitLimit);
+      if (!ok) fail();
+    } else if (!ok) {
+      fail();
+    }
+    // Epilogue: O / l, heads concatenated; lse in natural log.
+    const bool visible = l > 0.f;
+    const float inv = visible ? 1.f / l : 0.f;
+    const bool write = i < a.s_q;
+    const int64_t n = (int64_t)b * a.s_q + i;
+    if (ok && n_kt > 0) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + PF_TM_O + c * 32, v);
+        tmem_wait_ld_regs(v);
+        if (write) {
+          if (a.out_f32) {
+            float* o = static_cast<float*>(a.out) + n * a.out_row_stride + (int64_t)h * a.v_dim + c * 32;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4*>(o + e) =
+                  make_float4(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv,
+                              __uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
+          } else {
+            __nv_bfloat16* o =
+                static_cast<__nv_bfloat16*>(a.out) + n * a.out_row_stride + (int64_t)h * a.v_dim + c * 32;
+#pragma unroll
+            for (int e = 0; e < 32; e += 8) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv);
+              *reinterpret_cast<uint4*>(o + e) = w;
+            }
+          }
+        }
+      }
+    } else if (ok && write) {
+      // No visible key (a row shorter than its block): zeros.
+      for (int d = 0; d < a.v_dim; ++d) {
+        if (a.out_f32) static_cast<float*>(a.out)[n * a.out_row_stride + (int64_t)h * a.v_dim + d] = 0.f;
+        else static_cast<__nv_bfloat16*>(a.out)[n * a.out_row_stride + (int64_t)h * a.v_dim + d] = __float2bfloat16_rn(0.f);
+      }
+    }
+    if (ok && write && a.lse)
+      a.lse[n * gridDim.y + h] = visible ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_tc_reconstruct(const ReconstructParams& p, cudaStream_t stream) {
+  CUtensorMap lat_map, w_map, k_map, v_map;
+  {
+    const uint64_t dims[2] = {(uint64_t)p.rank, (uint64_t)p.n_rows};
+    const uint64_t strides[1] = {(uint64_t)p.latent_row_stride * 2};
+    const uint32_t box[2] = {64, 128};
+    if (!encode_tmap_bf16(&lat_map, p.latent, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)p.rank, (uint64_t)p.heads * (p.nope + p.v_dim)};
+    const uint64_t strides[1] = {(uint64_t)p.rank * 2};
+    const uint32_t box[2] = {64, 256};
+    if (!encode_tmap_bf16(&w_map, p.kv_b_proj, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)p.nope, (uint64_t)p.heads, (uint64_t)p.n_rows};
+    const uint64_t strides[2] = {(uint64_t)p.k_head_stride * 2, (uint64_t)p.k_row_stride * 2};
+    const uint32_t box[3] = {64, 1, 128};
+    if (!encode_tmap_bf16(&k_map, p.k_nope, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)p.v_dim, (uint64_t)p.heads, (uint64_t)p.n_rows};
+    const uint64_t strides[2] = {(uint64_t)p.v_head_stride * 2, (uint64_t)p.v_row_stride * 2};
+    const uint32_t box[3] = {64, 1, 128};
+    if (!encode_tmap_bf16(&v_map, p.v, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(tc_reconstruct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RC_SMEM);
+    attr = true;
+  }
+  ReconArgs a{p.rank / 64, p.nope + p.v_dim, p.status};
+  const dim3 grid((unsigned)((p.n_rows + 127) / 128), (unsigned)p.heads);
+  tc_reconstruct_kernel<<<grid, RC_THREADS, RC_SMEM, stream>>>(lat_map, w_map, k_map, v_map, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_prefill(const PrefillParams& p, cudaStream_t stream) {
+  CUtensorMap qn_map, qr_map, k_map, r_map, v_map;
+  const uint64_t n_q = (uint64_t)p.batch * p.s_q;
+  const uint64_t buf_rows = p.packed ? (uint64_t)p.t_max : (uint64_t)p.batch * p.t_max;
+  {
+    const uint64_t dims[3] = {(uint64_t)p.nope, (uint64_t)p.heads, n_q};
+    const uint64_t strides[2] = {(uint64_t)p.qn_head_stride * 2, (uint64_t)p.qn_row_stride * 2};
+    const uint32_t box[3] = {64, 1, 128};
+    if (!encode_tmap_bf16(&qn_map, p.q_nope, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)p.rope_dim, (uint64_t)p.heads, n_q};
+    const uint64_t strides[2] = {(uint64_t)p.qr_head_stride * 2, (uint64_t)p.qr_row_stride * 2};
+    const uint32_t box[3] = {64, 1, 128};
+    if (!encode_tmap_bf16(&qr_map, p.q_rope, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)p.nope, (uint64_t)p.heads, buf_rows};
+    const uint64_t strides[2] = {(uint64_t)p.k_head_stride * 2, (uint64_t)p.k_row_stride * 2};
+    const uint32_t box[3] = {64, 1, 128};
+    if (!encode_tmap_bf16(&k_map, p.k_nope, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)p.rope_dim, buf_rows};
+    const uint64_t strides[1] = {(uint64_t)p.rope_row_stride * 2};
+    const uint32_t box[2] = {64, 128};
+    if (!encode_tmap_bf16(&r_map, p.rope, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)p.v_dim, (uint64_t)p.heads, buf_rows};
+    const uint64_t strides[2] = {(uint64_t)p.v_head_stride * 2, (uint64_t)p.v_row_stride * 2};
+    const uint32_t box[3] = {64, 1, 128};
+    if (!encode_tmap_bf16(&v_map, p.v, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(tc_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM);
+    attr = true;
+  }
+  PrefillArgs a;
+  memset(&a, 0, sizeof(a));
+  a.kv_start = p.kv_start;
+  a.kv_len = p.kv_len;
+  a.t_max = p.t_max;
+  a.packed = p.packed;
+  a.batch = p.batch;
+  a.s_q = p.s_q;
+  a.n_qtiles = (p.s_q + 127) / 128;
+  a.scale_log2 = p.softmax_scale * 1.4426950408889634f;
+  a.out = p.out;
+  a.out_row_stride = p.out_row_stride;
+  a.v_dim = p.v_dim;
+  a.out_f32 = p.out_dtype == MLA_DTYPE_F32 ? 1 : 0;
+  a.lse = p.lse;
+  a.status = p.status;
+  const dim3 grid((unsigned)a.n_qtiles, (unsigned)p.heads, (unsigned)p.batch);
+  tc_prefill_kernel<<<grid, PF_THREADS, PF_SMEM, stream>>>(qn_map, qr_map, k_map, r_map, v_map, a);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

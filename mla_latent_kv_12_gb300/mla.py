@@ -31,7 +31,7 @@ EXPORTS = (
     "mla_gather_selected", "mla_decode_attend_no_alloc", "mla_decode_step",
     "mla_decode_step_workspace_size", "mla_append_compressed", "mla_select_topk",
     "mla_selftest_bounded_wait", "mla_plan_rollback", "mla_plan_filter", "mla_plan_merge",
-    "mla_cache_shift_rows", "mla_rollback_lengths",
+    "mla_cache_shift_rows", "mla_rollback_lengths", "mla_reconstruct_kv", "mla_prefill_attend",
 )
 
 
@@ -94,7 +94,12 @@ def _load() -> ctypes.CDLL:
                        ("mla_plan_merge", [i32, vp, vp, vp, vp, vp, vp, vp]),
                        ("mla_cache_shift_rows", [vp, i64, i64, i32, i32, vp, i64, i64, i32, i32,
                                                  ctypes.c_int, vp, vp, vp, i32, vp, vp]),
-                       ("mla_rollback_lengths", [vp, vp, vp, vp, i32, vp, vp])):
+                       ("mla_rollback_lengths", [vp, vp, vp, vp, i32, vp, vp]),
+                       ("mla_reconstruct_kv", [vp, i64, i64, vp, i32, i32, i32, i32, vp, i64, i64, vp, i64, i64,
+                                               ctypes.c_int, vp, vp]),
+                       ("mla_prefill_attend", [vp, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64,
+                                               ctypes.c_int, ctypes.c_int, vp, vp, i32, i32, i32, i32, i32, i32,
+                                               i64, f32, vp, i64, ctypes.c_int, vp, vp, vp])):
         getattr(lib, name).restype = ctypes.c_int
         getattr(lib, name).argtypes = args
     lib.mla_gather_selected.restype = ctypes.c_int
@@ -347,6 +352,34 @@ def rollback_lengths(kv_len_before: torch.Tensor, keep: torch.Tensor, kv_len: to
     out = kv_len if kv_len_out is None else kv_len_out
     _check(lib.mla_rollback_lengths(_ptr(kv_len_before), _ptr(keep), _ptr(kv_len), _ptr(out), kv_len.numel(),
                                     _ptr(device_status), _stream(stream)))
+    return out
+
+
+# ---------------------------------------------------------------- reconstructed prefill
+
+def reconstruct_kv(latent: torch.Tensor, kv_b_proj: torch.Tensor, k_nope: torch.Tensor, v: torch.Tensor,
+                   heads: int, nope: int, v_dim: int, device_status=None, stream=None):
+    """``latent`` ``[rows, rank]`` view; ``k_nope`` ``[rows, H, nope]`` and ``v`` ``[rows, H, v]`` views."""
+    assert latent.stride(-1) == 1 and k_nope.stride(-1) == 1 and v.stride(-1) == 1
+    assert kv_b_proj.is_contiguous()
+    _check(lib.mla_reconstruct_kv(_ptr(latent), latent.stride(0), latent.shape[0], _ptr(kv_b_proj), heads, nope,
+                                  v_dim, latent.shape[1], _ptr(k_nope), k_nope.stride(0), k_nope.stride(1), _ptr(v),
+                                  v.stride(0), v.stride(1), _dt(latent), _ptr(device_status), _stream(stream)))
+
+
+def prefill_attend(q_nope: torch.Tensor, q_rope: torch.Tensor, k_nope: torch.Tensor, v: torch.Tensor,
+                   rope: torch.Tensor, kv_start, kv_len, batch: int, s_q: int, t_max: int, packed: bool,
+                   softmax_scale: float, out: torch.Tensor, lse_out: Optional[torch.Tensor] = None,
+                   device_status=None, stream=None) -> torch.Tensor:
+    """``q_nope`` ``[n_q, H, nope]`` / ``q_rope`` ``[n_q, H, rope]`` (rotated) views; ``k_nope`` / ``v``
+    ``[buffer rows, H, .]``; ``rope`` ``[buffer rows, rope]``; ``out`` ``[n_q, H*v]``."""
+    _, heads, nope = q_nope.shape
+    _check(lib.mla_prefill_attend(
+        _ptr(q_nope), q_nope.stride(0), q_nope.stride(1), _ptr(q_rope), q_rope.stride(0), q_rope.stride(1),
+        _ptr(k_nope), k_nope.stride(0), k_nope.stride(1), _ptr(v), v.stride(0), v.stride(1), _ptr(rope),
+        rope.stride(0), 1 if packed else 0, _dt(q_nope), _ptr(kv_start), _ptr(kv_len), batch, s_q, heads, nope,
+        q_rope.shape[-1], v.shape[-1], int(t_max), float(softmax_scale), _ptr(out), out.stride(0), _dt(out),
+        _ptr(lse_out), _ptr(device_status), _stream(stream)))
     return out
 
 

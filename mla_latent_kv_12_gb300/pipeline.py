@@ -134,3 +134,68 @@ class DecodeStep:
                                            self.latent.shape[1], k_max, self.sel is not None,
                                            self.dtype)
         return 2 if nbytes > 0 else 1
+
+
+class PrefillStep:
+    """Reconstructed prefill of one attention layer ("glm52-mla.ts",
+    Glm52Mla.attendReconstructed): the block's ``S_q`` new tokens are the last
+    keys of each row's window (appended before attending), RoPE rotates the
+    query rope part at each row's offset, ``kv_b_proj`` materialises the
+    per-head no-PE keys and values of every buffer row, and causal attention
+    reads them with the cache's shared rope key.  Three launches per ``run``.
+    """
+
+    def __init__(self, inp: DecodeInputs, device="cuda", out_dtype: Optional[torch.dtype] = None):
+        w = inp.w
+        self.w, self.inp = w, inp
+        dt = DTYPES[w.dtype]
+        self.dtype = dt
+        self.out_dtype = out_dtype or dt
+        dev = torch.device(device)
+        n_q, H = w.n_q, w.heads
+        self.kv_start = inp.kv_start.to(dev)
+        self.kv_len = inp.kv_len.to(dev)
+        self.q_offset = inp.q_offset.to(dev)
+        self.latent = inp.latent.to(dev)
+        rope_raw = inp.rope_raw.to(dev)
+        self.rope = torch.empty_like(rope_raw)
+        rotate_cache_keys(inp, rope_raw, self.rope, inp.kv_start, inp.kv_len, w.theta)
+        del rope_raw
+        self.kv_b_proj = inp.kv_b_proj.to(dev).contiguous()
+        self.q_nope = inp.q_nope.to(dev).reshape(n_q, H, w.nope)
+        self.q_rope_raw = inp.q_rope_raw.to(dev)                          # [B, S, H, rope]
+        self.q_rope = torch.empty(w.batch, w.s_q, H, w.rope, dtype=dt, device=dev)
+        self.t_max = self.latent.shape[1]
+        rows = self.latent.shape[0] * self.t_max
+        self.kv = torch.empty(rows, H, w.nope + w.v, dtype=dt, device=dev)
+        self.k_nope = self.kv[..., :w.nope]
+        self.v = self.kv[..., w.nope:]
+        self.out = torch.empty(n_q, H * w.v, dtype=self.out_dtype, device=dev)
+        self.lse = torch.empty(n_q, H, dtype=torch.float32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.scale = mla.default_scale(w.nope, w.rope)
+
+    def rope_q(self, stream=None):
+        mla.rope_partial_interleaved(self.q_rope_raw, self.q_rope, self.w.rope, self.w.theta,
+                                     row_offsets=self.q_offset, stream=stream)
+
+    def reconstruct(self, stream=None):
+        w = self.w
+        mla.reconstruct_kv(self.latent.view(-1, w.rank), self.kv_b_proj, self.k_nope, self.v, w.heads, w.nope,
+                           w.v, device_status=self.status, stream=stream)
+
+    def attend(self, stream=None):
+        w = self.w
+        mla.prefill_attend(self.q_nope, self.q_rope.view(w.n_q, w.heads, w.rope), self.k_nope, self.v,
+                           self.rope.view(-1, w.rope), self.kv_start, self.kv_len, w.batch, w.s_q, self.t_max,
+                           self.inp.packed_flat, self.scale, self.out, self.lse, device_status=self.status,
+                           stream=stream)
+
+    def run(self, stream=None) -> torch.Tensor:
+        self.rope_q(stream)
+        self.reconstruct(stream)
+        self.attend(stream)
+        return self.out
+
+    def launches_per_step(self) -> int:
+        return 3

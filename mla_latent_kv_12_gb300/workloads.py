@@ -70,6 +70,11 @@ VERIFY_BF16 = Workload("verify_bf16_b8_sq4_t65536_h128", 8, 4, 65536, 128, 512, 
 VERIFY_SPARSE_BF16 = dataclasses.replace(VERIFY_BF16, name="verify_sparse_bf16_b8_sq4_t65536_top2048_h128",
                                          top_k=2048)
 
+# Reconstructed prefill (the pages' second workload: a dense long prompt block,
+# causal, appended before attending): one row, 4096 new tokens, no earlier cache.
+PREFILL_BF16 = Workload("prefill_bf16_b1_s4096_h128", 1, 4096, 4096, 128, 512, 128, 64, 128,
+                        10000.0, "bf16", 5)
+
 ALL = (TINY_F32, DENSE_BF16, RAGGED_BF16, SPARSE_BF16, VERIFY_BF16, VERIFY_SPARSE_BF16)
 
 

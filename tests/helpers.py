@@ -159,3 +159,17 @@ def oracle_reference_out_only(inp, rows, heads=None):
                                     rows=rows, head_subset=heads,
                                     batch_buffer_rows=batch_buffer_rows(inp))
     return out
+
+
+def oracle_prefill(inp, rows, heads):
+    """The reconstructed definition (``attendReconstructed``) for sampled query rows and heads
+    of a prefill block: ``out [n_q, len(heads), v]`` and ``lse`` (float64; unsampled rows NaN)."""
+    w = inp.w
+    brows = sorted({n // w.s_q for n in rows})
+    rope = oracle_rotated_cache_rope(inp, brows, inp.latent.dtype)
+    q_rope = oracle_rotated_q_rope(inp)
+    q_nope = inp.q_nope.to(torch.float64).numpy().reshape(w.n_q, w.heads, w.nope)
+    wkv = inp.kv_b_proj.to(torch.float64).numpy()
+    return O.attend_reconstructed(q_nope, q_rope, Rows(inp.latent), rope, wkv, inp.kv_start.numpy(),
+                                  inp.kv_len.numpy(), w.heads, w.nope, w.v, w.s_q, rows=list(rows),
+                                  head_subset=list(heads), batch_buffer_rows=batch_buffer_rows(inp))
