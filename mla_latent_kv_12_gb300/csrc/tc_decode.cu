@@ -524,10 +524,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (gather && !a.gather_tma) fence_proxy_async_smem();
         if (tile > 0 && !mbar_wait_warp(&s_free, (tile - 1) & 1u, kWaitLimit)) { fail(); break; }
         tc_fence_after();
-        if (lane == 0) {
-          // 16 latent K-steps, then this CTA's two rope K-steps.  Descriptors
-          // differ only in the start address (16-byte units, low bits).
-          const uint64_t d0 = smem_desc(smem_u32(stages + stage * STAGE_BYTES), 16, 1024, kSwizzle128B);
+        // 16 latent K-steps, then this CTA's two rope K-steps.  Descriptors
+        // differ only in the start address (16-byte units, low bits); one
+        // elected lane of the converged warp issues them with constant
+        // offsets (a lane-0 branch with per-MMA descriptor arithmetic issues
+        // the N=64 MMAs at about half the rate).
+        const uint64_t d0 = smem_desc(smem_u32(stages + stage * STAGE_BYTES), 16, 1024, kSwizzle128B);
+        const uint64_t d_rope = d0 + (uint64_t)((4 * CHUNK_BYTES + 2 * (int)rank * 32) >> 4);
+        if (elect_one()) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
 #pragma unroll
@@ -537,8 +541,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           }
 #pragma unroll
           for (int k = 0; k < 2; ++k)
-            mma_ts(tmem + TM_S, tmem + TM_Q + 128 + k * 8,
-                   d0 + (uint64_t)((4 * CHUNK_BYTES + (2 * (int)rank + k) * 32) >> 4), idesc_s, 1u);
+            mma_ts(tmem + TM_S, tmem + TM_Q + 128 + k * 8, d_rope + (uint64_t)((k * 32) >> 4), idesc_s, 1u);
           mma_commit(&s_full);
         }
         __syncwarp();
@@ -568,12 +571,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (first && seg > 0 && !mbar_wait_warp(&o_free, (seg - 1) & 1u, kWaitLimit)) { fail(); break; }
         if (!mbar_wait_warp(&p_full, tile & 1u, kWaitLimit)) { fail(); break; }
         tc_fence_after();
-        if (lane == 0) {
-          const uint64_t d0 = smem_desc(smem_u32(stages + stage * STAGE_BYTES), CHUNK_BYTES, 1024, kSwizzle128B);
+        const uint64_t d0 = smem_desc(smem_u32(stages + stage * STAGE_BYTES), CHUNK_BYTES, 1024, kSwizzle128B);
+        const uint32_t acc0 = first ? 0u : 1u;
+        if (elect_one()) {
 #pragma unroll
           for (int k = 0; k < BN / 16; ++k)
             mma_ts(tmem + TM_O, tmem + TM_P + k * 8, d0 + (uint64_t)((k * 2048) >> 4), idesc_pv,
-                   (first && k == 0) ? 0u : 1u);
+                   k == 0 ? acc0 : 1u);
           mma_commit(&empty_bar[stage]);
           mma_commit(&pv_done);
         }

@@ -8,17 +8,21 @@
 //   tc_reconstruct_kernel  K_nope[t,h,:] = latent[t,:] . W_UK_h^T,
 //                          V[t,h,:]      = latent[t,:] . W_UV_h^T
 //     grid (row tiles of 128, heads), one tcgen05 MMA chain M=128 tokens x
-//     N=256 (head h's 256 rows of kv_b_proj) x K=rank, fed by a 4-stage TMA
-//     ring; the f32 accumulator is rounded to bf16 into swizzled shared memory
+//     N=256 (head h's 256 rows of kv_b_proj) x K=rank, fed by a 2-stage TMA
+//     ring (two CTAs per SM); the f32 accumulator is rounded to bf16 into swizzled shared memory
 //     and written with TMA tensor stores.
 //
 //   tc_prefill_kernel      causal flash attention, one CTA per (128 query
-//     rows, head, batch row).  Q (nope || rotated rope, 192 features) stays
-//     in shared memory; each 128-key tile brings K_nope, the cache's shared
-//     rope key and V by TMA (two stages).  Warp 1 issues S(j+1) = Q.K^T into
-//     one of two TMEM score buffers while the four softmax warps (one query
-//     row per thread) turn S(j) into bf16 P in place; then it issues
-//     O += P.V with P read from TMEM.  The running maximum is only moved when
+//     rows, head, batch row).  Q (nope || rotated rope, 192 features) is
+//     loaded once into TMEM (the score MMAs read A from there, which issues
+//     faster than from shared memory); each 128-key tile brings K_nope and the
+//     cache's shared rope key (one ring, freed when the tile's scores are
+//     done) and V
+//     (a second ring, freed when its P.V is done) by TMA.  Warp 1 issues
+//     S(j+1) = Q.K^T into one of two TMEM score buffers while eight softmax
+//     warps (two per quarter of the query rows, 64 score columns each) turn
+//     S(j) into bf16 P in place; then it issues O += P.V with P read from
+//     TMEM.  The running maximum is only moved when
 //     it grows by more than 2^8 (the accumulated O and sum are then rescaled
 //     in TMEM), so most tiles skip the correction.
 #include <cuda_bf16.h>
@@ -49,7 +53,7 @@ __device__ __forceinline__ uint32_t sw128(int r, int u) { return (uint32_t)(r * 
 
 // ------------------------------------------------------------------ reconstruct
 
-constexpr int RC_STAGES = 4;
+constexpr int RC_STAGES = 2;       // two CTAs per SM: one's epilogue overlaps the other's MMAs
 constexpr int RC_A_BYTES = kChunk;          // 128 tokens x 64 latent features
 constexpr int RC_B_BYTES = 2 * kChunk;      // 256 weight rows x 64 latent features
 constexpr int RC_STAGE_BYTES = RC_A_BYTES + RC_B_BYTES;
@@ -62,7 +66,7 @@ struct ReconArgs {
   int32_t* status;
 };
 
-__global__ void __launch_bounds__(RC_THREADS, 1)
+__global__ void __launch_bounds__(RC_THREADS, 2)
     tc_reconstruct_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__ CUtensorMap w_map,
                           const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                           const __grid_constant__ ReconArgs a) {
@@ -102,8 +106,8 @@ __global__ void __launch_bounds__(RC_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
-    bool issued[RC_STAGES] = {false, false, false, false};
-    uint32_t issued_phase[RC_STAGES] = {0, 0, 0, 0};
+    bool issued[RC_STAGES] = {};
+    uint32_t issued_phase[RC_STAGES] = {};
     if (lane == 0) {
       for (int kc = 0; kc < a.k_chunks && !abort_s; ++kc) {
         const int s = kc % RC_STAGES;
@@ -127,12 +131,13 @@ __global__ void __launch_bounds__(RC_THREADS, 1)
       const int s = kc % RC_STAGES;
       if (!mbar_wait_warp(&full_bar[s], (uint32_t)(kc / RC_STAGES) & 1u, kWaitLimit)) { fail(); break; }
       tc_fence_after();
-      if (lane == 0) {
-        const uint32_t a0 = smem_u32(smem + s * RC_STAGE_BYTES), b0 = a0 + RC_A_BYTES;
+      const uint64_t ad = smem_desc(smem_u32(smem + s * RC_STAGE_BYTES), 16, 1024, kSwizzle128B);
+      const uint64_t bd = ad + (uint64_t)(RC_A_BYTES >> 4);
+      const uint32_t first = kc == 0 ? 0u : 1u;
+      if (elect_one()) {
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_ss(tmem, smem_desc(a0 + k * 32, 16, 1024, kSwizzle128B), smem_desc(b0 + k * 32, 16, 1024, kSwizzle128B),
-                 idesc, (kc | k) != 0);
+          mma_ss(tmem, ad + (uint64_t)((k * 32) >> 4), bd + (uint64_t)((k * 32) >> 4), idesc, k == 0 ? first : 1u);
         mma_commit(&empty_bar[s]);
       }
       __syncwarp();
@@ -188,15 +193,20 @@ __global__ void __launch_bounds__(RC_THREADS, 1)
 
 // ------------------------------------------------------------------ prefill attention
 
-constexpr int PF_STAGES = 2;
-constexpr int PF_Q_BYTES = 3 * kChunk;        // nope 0..63 | nope 64..127 | rope
-constexpr int PF_STAGE_BYTES = 5 * kChunk;    // K_nope x2 | rope | V x2
-constexpr int PF_SMEM = 1024 + PF_Q_BYTES + PF_STAGES * PF_STAGE_BYTES;
-constexpr int PF_THREADS = 192;
-constexpr uint32_t PF_TM_O = 256;             // TMEM: S0 at 0, S1 at 128, O at 256
+constexpr int PF_STAGES = 2;                  // per ring
+constexpr int PF_K_BYTES = 3 * kChunk;        // K_nope x2 | rope  (freed when S completes)
+constexpr int PF_V_BYTES = 2 * kChunk;        // V x2              (freed when P.V completes)
+constexpr int PF_SMEM = 1024 + PF_STAGES * (PF_K_BYTES + PF_V_BYTES);
+constexpr int PF_THREADS = 352;               // K producer, MMA, 8 softmax warps, V producer
+constexpr uint32_t PF_TM_O = 256;             // TMEM: S0 at 0, S1 at 128, O at 256, Q at 384
+constexpr uint32_t PF_TM_Q = 384;             // 192 bf16 features = 96 columns
 constexpr float kRescaleLog2 = 8.f;
 
 struct PrefillArgs {
+  const void* q_nope;
+  int64_t qn_row_stride, qn_head_stride;
+  const void* q_rope;
+  int64_t qr_row_stride, qr_head_stride;
   const int32_t* kv_start;
   const int32_t* kv_len;
   int64_t t_max;         // buffer rows of one batch row (the packed buffer's rows when packed)
@@ -211,15 +221,15 @@ struct PrefillArgs {
 };
 
 __global__ void __launch_bounds__(PF_THREADS, 1)
-    tc_prefill_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_constant__ CUtensorMap qr_map,
-                      const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap r_map,
+    tc_prefill_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap r_map,
                       const __grid_constant__ CUtensorMap v_map, const __grid_constant__ PrefillArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;
-  uint8_t* stages = smem + PF_Q_BYTES;
-  __shared__ __align__(8) uint64_t q_full, full_bar[PF_STAGES], empty_bar[PF_STAGES], s_full[2], p_full, pv_done,
-      mma_drain;
+  uint8_t* k_ring = smem;
+  uint8_t* v_ring = k_ring + PF_STAGES * PF_K_BYTES;
+  __shared__ __align__(8) uint64_t q_tmem, k_full[PF_STAGES], k_empty[PF_STAGES], v_full[PF_STAGES],
+      v_empty[PF_STAGES], s_full[2], p_full, pv_done, mma_drain, xbar[2][4], lbar[4];
+  __shared__ float red_max[2][2][128], red_sum[2][128];
   __shared__ uint32_t tmem_s;
   __shared__ volatile int abort_s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -239,22 +249,26 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   const int64_t key_end = min(len, offs + i_hi + 1);
   const int n_kt = key_end > 0 ? (int)((key_end + 127) / 128) : 0;
   const int64_t ybase = (a.packed ? 0 : (int64_t)b * a.t_max) + start;
-  const int q_row0 = b * a.s_q + i0;
 
   if (threadIdx.x == 0) {
-    tma_prefetch_desc(&qn_map);
-    tma_prefetch_desc(&qr_map);
     tma_prefetch_desc(&k_map);
     tma_prefetch_desc(&r_map);
     tma_prefetch_desc(&v_map);
-    mbar_init(&q_full, 1);
+    mbar_init(&q_tmem, 256);
     for (int s = 0; s < PF_STAGES; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
-    mbar_init(&p_full, 128);
+    mbar_init(&p_full, 256);
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(&xbar[0][q], 64);
+      mbar_init(&xbar[1][q], 64);
+      mbar_init(&lbar[q], 64);
+    }
     mbar_init(&pv_done, 1);
     mbar_init(&mma_drain, 1);
     abort_s = 0;
@@ -274,46 +288,79 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   };
   auto aborted = [&]() -> bool { return __any_sync(0xffffffffu, abort_s != 0); };
 
-  if (warp == 0) {
-    // ------------------------------------------------ TMA producer
-    bool issued[PF_STAGES] = {false, false};
-    uint32_t issued_phase[PF_STAGES] = {0, 0};
-    bool q_issued = false;
+  if (warp == 0 || warp == 10) {
+    // ------------------------------------------------ TMA producers: warp 0 Q and the
+    // K ring (K_nope, rope), warp 10 the V ring; each stage is refilled as soon as
+    // its consumer MMA completes.
+    const bool kside = warp == 0;
+    uint64_t* fullb = kside ? k_full : v_full;
+    uint64_t* emptyb = kside ? k_empty : v_empty;
+    bool issued[PF_STAGES] = {};
+    uint32_t issued_phase[PF_STAGES] = {};
     if (lane == 0 && n_kt > 0) {
-      mbar_arrive_expect_tx(&q_full, PF_Q_BYTES);
-      tma_load_3d(sQ, &qn_map, &q_full, 0, h, q_row0);
-      tma_load_3d(sQ + kChunk, &qn_map, &q_full, 64, h, q_row0);
-      tma_load_3d(sQ + 2 * kChunk, &qr_map, &q_full, 0, h, q_row0);
-      q_issued = true;
       for (int kt = 0; kt < n_kt && !abort_s; ++kt) {
         const int s = kt % PF_STAGES;
         const uint32_t ph = (uint32_t)(kt / PF_STAGES) & 1u;
-        if (kt >= PF_STAGES && !mbar_wait(&empty_bar[s], ph ^ 1u, kWaitLimit)) { fail(); break; }
-        uint8_t* st = stages + s * PF_STAGE_BYTES;
+        if (kt >= PF_STAGES && !mbar_wait(&emptyb[s], ph ^ 1u, kWaitLimit)) { fail(); break; }
         const int y = (int)(ybase + (int64_t)kt * 128);
-        mbar_arrive_expect_tx(&full_bar[s], PF_STAGE_BYTES);
-        tma_load_3d(st, &k_map, &full_bar[s], 0, h, y);
-        tma_load_3d(st + kChunk, &k_map, &full_bar[s], 64, h, y);
-        tma_load_2d(st + 2 * kChunk, &r_map, &full_bar[s], 0, y);
-        tma_load_3d(st + 3 * kChunk, &v_map, &full_bar[s], 0, h, y);
-        tma_load_3d(st + 4 * kChunk, &v_map, &full_bar[s], 64, h, y);
+        if (kside) {
+          uint8_t* st = k_ring + s * PF_K_BYTES;
+          mbar_arrive_expect_tx(&fullb[s], PF_K_BYTES);
+          tma_load_3d(st, &k_map, &fullb[s], 0, h, y);
+          tma_load_3d(st + kChunk, &k_map, &fullb[s], 64, h, y);
+          tma_load_2d(st + 2 * kChunk, &r_map, &fullb[s], 0, y);
+        } else {
+          uint8_t* st = v_ring + s * PF_V_BYTES;
+          mbar_arrive_expect_tx(&fullb[s], PF_V_BYTES);
+          tma_load_3d(st, &v_map, &fullb[s], 0, h, y);
+          tma_load_3d(st + kChunk, &v_map, &fullb[s], 64, h, y);
+        }
         issued[s] = true;
         issued_phase[s] = ph;
       }
       // Every issued copy lands before the CTA may exit.
-      if (q_issued) mbar_wait(&q_full, 0, kWaitLimit);
       for (int s = 0; s < PF_STAGES; ++s)
-        if (issued[s]) mbar_wait(&full_bar[s], issued_phase[s], kWaitLimit);
+        if (issued[s]) mbar_wait(&fullb[s], issued_phase[s], kWaitLimit);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
     const uint32_t idesc_pv = idesc_bf16_f32(128, 128, 0, 1);
+    // Stage s's descriptors are the base's plus s stage sizes (16-byte units).
+    const uint64_t kdesc0 = smem_desc(smem_u32(k_ring), 16, 1024, kSwizzle128B);
+    const uint64_t vdesc0 = smem_desc(smem_u32(v_ring), kChunk, 1024, kSwizzle128B);
     auto issue_s = [&](int j) -> bool {
       const int s = j % PF_STAGES;
-      if (!mbar_wait_warp(&full_bar[s], (uint32_t)(j / PF_STAGES) & 1u, kWaitLimit)) return false;
-      uint8_t* st = stages + s * PF_STAGE_BYTES;
+      if (!mbar_wait_warp(&k_full[s], (uint32_t)(j / PF_STAGES) & 1u, kWaitLimit)) return false;
+      tc_fence_after();
+      // A = Q from TMEM (features packed two per column), B = the K tile.
+      // Issued by one elected lane of the converged warp with descriptors
+      // that differ from a base by constants: the tensor core then accepts an
+      // M=128 N=128 MMA about every 68 cycles (a lane-0 branch with per-MMA
+      // descriptor arithmetic issues at roughly half that rate).
+      const uint64_t kd = kdesc0 + (uint64_t)(s * (PF_K_BYTES >> 4));
+      const uint32_t d_s = tmem + (uint32_t)((j & 1) * 128);
+      if (elect_one()) {
+#pragma unroll
+        for (int c = 0; c < 3; ++c)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ts(d_s, tmem + PF_TM_Q + (uint32_t)(c * 32 + k * 8),
+                   kd + (uint64_t)((c * kChunk + k * 32) >> 4), idesc_s, (c | k) != 0);
+        mma_commit(&s_full[j & 1]);
+        mma_commit(&k_empty[s]);
+      }
+      __syncwarp();
+      return true;
+    };
+    bool ok = n_kt == 0 || mbar_wait_warp(&q_tmem, 0, kWaitLimit);
+    if (ok && n_kt > 0) ok = issue_s(0);
+    for (int j = 0; ok && j < n_kt; ++j) {
+      if (j + 1 < n_kt && !issue_s(j + 1)) { ok = false; break; }
+      const int s = j % PF_STAGES;
+      if (!mbar_wait_warp(&v_full[s], (uint32_t)(j / PF_STAGES) & 1u, kWaitLimit)) { ok = false; break; }
+      uint8_t* st = v_ring + s * PF_V_BYTES;
       const int64_t valid = len - (int64_t)j * 128;
       if (valid < 128) {
         // Tail tile: clear the V rows past the window, so that P = 0 never
@@ -321,40 +368,23 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         const int v0 = valid < 0 ? 0 : (int)valid;
         for (int q = lane; q < (128 - v0) * 16; q += 32) {
           const int c = q / ((128 - v0) * 8), rem = q % ((128 - v0) * 8);
-          *reinterpret_cast<uint4*>(st + (3 + c) * kChunk + (v0 + rem / 8) * 128 + (rem % 8) * 16) =
+          *reinterpret_cast<uint4*>(st + c * kChunk + (v0 + rem / 8) * 128 + (rem % 8) * 16) =
               make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
         __syncwarp();
       }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(st);
-#pragma unroll
-        for (int c = 0; c < 3; ++c)
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + (uint32_t)((j & 1) * 128),
-                   smem_desc(q0 + c * kChunk + k * 32, 16, 1024, kSwizzle128B),
-                   smem_desc(k0 + c * kChunk + k * 32, 16, 1024, kSwizzle128B), idesc_s, (c | k) != 0);
-        mma_commit(&s_full[j & 1]);
-      }
-      __syncwarp();
-      return true;
-    };
-    bool ok = n_kt == 0 || mbar_wait_warp(&q_full, 0, kWaitLimit);
-    if (ok && n_kt > 0) ok = issue_s(0);
-    for (int j = 0; ok && j < n_kt; ++j) {
-      if (j + 1 < n_kt && !issue_s(j + 1)) { ok = false; break; }
       if (!mbar_wait_warp(&p_full, (uint32_t)j & 1u, kWaitLimit)) { ok = false; break; }
       tc_fence_after();
-      if (lane == 0) {
-        const uint32_t v0 = smem_u32(stages + (j % PF_STAGES) * PF_STAGE_BYTES + 3 * kChunk);
+      const uint64_t vd = vdesc0 + (uint64_t)(s * (PF_V_BYTES >> 4));
+      const uint32_t p_src = tmem + (uint32_t)((j & 1) * 128);
+      const uint32_t first = j == 0 ? 0u : 1u;
+      if (elect_one()) {
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ts(tmem + PF_TM_O, tmem + (uint32_t)((j & 1) * 128 + k * 8),
-                 smem_desc(v0 + k * 2048, kChunk, 1024, kSwizzle128B), idesc_pv, (j | k) != 0);
-        mma_commit(&empty_bar[j % PF_STAGES]);
+          mma_ts(tmem + PF_TM_O, p_src + (uint32_t)(k * 8), vd + (uint64_t)((k * 2048) >> 4), idesc_pv,
+                 k == 0 ? first : 1u);
+        mma_commit(&v_empty[s]);
         mma_commit(&pv_done);
       }
       __syncwarp();
@@ -366,39 +396,86 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     __syncwarp();
     mbar_wait_warp(&mma_drain, 0, kWaitLimit);
   } else {
-    // ------------------------------------------------ softmax + epilogue (warps 2..5)
+    // ------------------------------------------------ softmax + epilogue (warps 2..9)
+    // Warp w owns TMEM lanes 32*(w%4).. (its query rows) and score columns
+    // 64*half.. of them, half = (w-2)/4: two warps per SM sub-partition share
+    // the exponentials of a tile.  The two warps of a row quarter combine their
+    // row maxima through shared memory (double-buffered, an mbarrier per tile
+    // parity), so both take the same running-maximum decisions; each keeps its
+    // own partial sum, added once at the end.
     const int quarter = warp & 3;
+    const int hf = (warp - 2) >> 2;
     const int r = 32 * quarter + lane;
     const int i = i0 + r;
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
+    const uint32_t col0 = 64u * (uint32_t)hf;
     const int64_t limit = i < a.s_q ? offs + i : -1;       // last visible window position
     const int64_t min_limit = offs + i0;                   // the tile's first row
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
+    if (n_kt > 0) {
+      // Q row into TMEM (the S MMAs' A operand): half 0 writes features
+      // 0..95 (q_nope), half 1 features 96..191 (q_nope tail, rotated q_rope),
+      // 16 bytes = 4 columns per load.  Rows past the block are zero.
+      uint4 qv[12];
+      const bool real = i < a.s_q;
+      const int64_t n = (int64_t)b * a.s_q + i;
+      const uint4* qn = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q_nope) +
+                                                       n * a.qn_row_stride + (int64_t)h * a.qn_head_stride);
+      const uint4* qr = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q_rope) +
+                                                       n * a.qr_row_stride + (int64_t)h * a.qr_head_stride);
+#pragma unroll
+      for (int u = 0; u < 12; ++u) {
+        const int unit = hf * 12 + u;                       // 0..15 q_nope, 16..23 q_rope
+        qv[u] = make_uint4(0, 0, 0, 0);
+        if (real) qv[u] = unit < 16 ? __ldg(qn + unit) : __ldg(qr + (unit - 16));
+      }
+#pragma unroll
+      for (int c = 0; c < 3; ++c) {
+        uint32_t rr[16];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          rr[4 * u] = qv[4 * c + u].x, rr[4 * u + 1] = qv[4 * c + u].y, rr[4 * u + 2] = qv[4 * c + u].z,
+          rr[4 * u + 3] = qv[4 * c + u].w;
+        tmem_st16(tmem + lane_off + PF_TM_Q + 48u * (uint32_t)hf + 16u * (uint32_t)c, rr);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&q_tmem);
+    }
     for (int j = 0; j < n_kt; ++j) {
       if (!mbar_wait_warp(&s_full[j & 1], (uint32_t)(j >> 1) & 1u, kWaitLimit)) { ok = false; break; }
       tc_fence_after();
-      float x[128];
-      {
-        uint32_t v[32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(tmem + lane_off + (uint32_t)((j & 1) * 128 + c * 32), v);
-          tmem_wait_ld_regs(v);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[e]) * a.scale_log2;
-        }
-      }
-      const int64_t kbase = (int64_t)j * 128;
-      const bool full = (kbase + 127 <= min_limit) && (kbase + 127 < len);
+      // This thread's 64 raw scores in two 32-column loads behind one wait.
+      uint32_t v[2][32];
+      tmem_ld32(tmem + lane_off + (uint32_t)((j & 1) * 128) + col0, v[0]);
+      tmem_ld32(tmem + lane_off + (uint32_t)((j & 1) * 128) + col0 + 32, v[1]);
+      tmem_wait_ld_regs(v[0]);
+      reg_fence32(v[1]);
+      const int64_t kbase = (int64_t)j * 128 + col0;
+      const bool full = ((int64_t)j * 128 + 127 <= min_limit) && ((int64_t)j * 128 + 127 < len);
       if (!full) {
 #pragma unroll
-        for (int e = 0; e < 128; ++e)
-          if (kbase + e > limit) x[e] = -INFINITY;
-      }
-      float mx = x[0];
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
-      for (int e = 1; e < 128; ++e) mx = fmaxf(mx, x[e]);
+          for (int e = 0; e < 32; ++e)
+            if (kbase + c * 32 + e > limit) v[c][e] = __float_as_uint(-INFINITY);
+      }
+      // Partial row maximum with eight independent chains.
+      float m8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(v[c][e]));
+      const float mpart = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      red_max[j & 1][hf][r] = mpart;
+      mbar_arrive(&xbar[j & 1][quarter]);
+      if (!mbar_wait_warp(&xbar[j & 1][quarter], (uint32_t)(j >> 1) & 1u, kWaitLimit)) { ok = false; break; }
+      const float mraw = fmaxf(mpart, red_max[j & 1][hf ^ 1][r]);
+      const float mx = mraw * a.scale_log2;          // log2 units (the scale is positive)
       // Move the running maximum only when it grows by more than 2^8.
       const bool move = mx > m_used + kRescaleLog2;
       float alpha = 1.f;
@@ -407,44 +484,45 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         m_used = mx;
         l *= alpha;
       }
-      uint32_t pk[64];
-      float sum = 0.f;
+      uint32_t pk[32];
+      float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       if (m_used == -INFINITY) {
 #pragma unroll
-        for (int e = 0; e < 64; ++e) pk[e] = 0u;
+        for (int e = 0; e < 32; ++e) pk[e] = 0u;
       } else {
+        const float neg_m = -m_used;
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          const float p0 = ex2_approx(x[2 * e] - m_used), p1 = ex2_approx(x[2 * e + 1] - m_used);
-          sum += p0 + p1;
-          pk[e] = pack_bf16x2(p0, p1);
-        }
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(v[c][2 * e]), a.scale_log2, neg_m));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(v[c][2 * e + 1]), a.scale_log2, neg_m));
+            s8[e & 7] += p0 + p1;
+            pk[c * 16 + e] = pack_bf16x2(p0, p1);
+          }
       }
-      l += sum;
-      // O holds P(0..j-1).V once the previous P.V is done; correct it in place
-      // (warp-uniform: tcgen05.ld/st are collective).
+      l += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+      // O holds P(0..j-1).V once the previous P.V is done; correct this
+      // thread's 64 columns in place (warp-uniform: tcgen05.ld/st are collective).
       if (j > 0) {
         if (!mbar_wait_warp(&pv_done, (uint32_t)(j - 1) & 1u, kWaitLimit)) { ok = false; break; }
         if (__any_sync(0xffffffffu, move)) {
           tc_fence_after();
           const float f = move ? alpha : 1.f;
-          uint32_t v[32];
+          uint32_t o[32];
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            tmem_ld32(tmem + lane_off + PF_TM_O + c * 32, v);
-            tmem_wait_ld_regs(v);
+          for (int c = 0; c < 2; ++c) {
+            tmem_ld32(tmem + lane_off + PF_TM_O + col0 + c * 32, o);
+            tmem_wait_ld_regs(o);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * f);
-            tmem_st32(tmem + lane_off + PF_TM_O + c * 32, v);
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+            tmem_st32(tmem + lane_off + PF_TM_O + col0 + c * 32, o);
           }
         }
       }
-      {
-        uint32_t (&p0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
-        uint32_t (&p1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
-        tmem_st32(tmem + lane_off + (uint32_t)((j & 1) * 128), p0);
-        tmem_st32(tmem + lane_off + (uint32_t)((j & 1) * 128 + 32), p1);
-      }
+      // P (bf16 pairs) over the scores: both warps of the quarter have read
+      // their scores (the maximum exchange above), so the columns are free.
+      tmem_st32(tmem + lane_off + (uint32_t)((j & 1) * 128) + 32u * (uint32_t)hf, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&p_full);
@@ -456,49 +534,57 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     } else if (!ok) {
       fail();
     }
+    // The row's sum: this half's plus the partner's.
+    if (ok) {
+      red_sum[hf][r] = l;
+      mbar_arrive(&lbar[quarter]);
+      ok = mbar_wait_warp(&lbar[quarter], 0, kWaitLimit);
+      if (ok) l += red_sum[hf ^ 1][r];
+      else fail();
+    }
     // Epilogue: O / l, heads concatenated; lse in natural log.
     const bool visible = l > 0.f;
     const float inv = visible ? 1.f / l : 0.f;
     const bool write = i < a.s_q;
     const int64_t n = (int64_t)b * a.s_q + i;
+    const int64_t ocol = (int64_t)h * a.v_dim + col0;
     if (ok && n_kt > 0) {
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + PF_TM_O + c * 32, v);
-        tmem_wait_ld_regs(v);
+      for (int c = 0; c < 2; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_off + PF_TM_O + col0 + c * 32, o);
+        tmem_wait_ld_regs(o);
         if (write) {
           if (a.out_f32) {
-            float* o = static_cast<float*>(a.out) + n * a.out_row_stride + (int64_t)h * a.v_dim + c * 32;
+            float* dst = static_cast<float*>(a.out) + n * a.out_row_stride + ocol + c * 32;
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<float4*>(o + e) =
-                  make_float4(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv,
-                              __uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
+              *reinterpret_cast<float4*>(dst + e) =
+                  make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
+                              __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
           } else {
-            __nv_bfloat16* o =
-                static_cast<__nv_bfloat16*>(a.out) + n * a.out_row_stride + (int64_t)h * a.v_dim + c * 32;
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + n * a.out_row_stride + ocol + c * 32;
 #pragma unroll
             for (int e = 0; e < 32; e += 8) {
               uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
-              w.y = pack_bf16x2(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
-              w.z = pack_bf16x2(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv);
-              w.w = pack_bf16x2(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv);
-              *reinterpret_cast<uint4*>(o + e) = w;
+              w.x = pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+              *reinterpret_cast<uint4*>(dst + e) = w;
             }
           }
         }
       }
     } else if (ok && write) {
       // No visible key (a row shorter than its block): zeros.
-      for (int d = 0; d < a.v_dim; ++d) {
-        if (a.out_f32) static_cast<float*>(a.out)[n * a.out_row_stride + (int64_t)h * a.v_dim + d] = 0.f;
-        else static_cast<__nv_bfloat16*>(a.out)[n * a.out_row_stride + (int64_t)h * a.v_dim + d] = __float2bfloat16_rn(0.f);
+      for (int d = 0; d < 64; ++d) {
+        if (a.out_f32) static_cast<float*>(a.out)[n * a.out_row_stride + ocol + d] = 0.f;
+        else static_cast<__nv_bfloat16*>(a.out)[n * a.out_row_stride + ocol + d] = __float2bfloat16_rn(0.f);
       }
     }
-    if (ok && write && a.lse)
+    if (ok && write && hf == 0 && a.lse)
       a.lse[n * gridDim.y + h] = visible ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
   }
   tc_fence_before();
@@ -549,21 +635,8 @@ cudaError_t launch_tc_reconstruct(const ReconstructParams& p, cudaStream_t strea
 }
 
 cudaError_t launch_tc_prefill(const PrefillParams& p, cudaStream_t stream) {
-  CUtensorMap qn_map, qr_map, k_map, r_map, v_map;
-  const uint64_t n_q = (uint64_t)p.batch * p.s_q;
+  CUtensorMap k_map, r_map, v_map;
   const uint64_t buf_rows = p.packed ? (uint64_t)p.t_max : (uint64_t)p.batch * p.t_max;
-  {
-    const uint64_t dims[3] = {(uint64_t)p.nope, (uint64_t)p.heads, n_q};
-    const uint64_t strides[2] = {(uint64_t)p.qn_head_stride * 2, (uint64_t)p.qn_row_stride * 2};
-    const uint32_t box[3] = {64, 1, 128};
-    if (!encode_tmap_bf16(&qn_map, p.q_nope, 3, dims, strides, box)) return cudaErrorInvalidValue;
-  }
-  {
-    const uint64_t dims[3] = {(uint64_t)p.rope_dim, (uint64_t)p.heads, n_q};
-    const uint64_t strides[2] = {(uint64_t)p.qr_head_stride * 2, (uint64_t)p.qr_row_stride * 2};
-    const uint32_t box[3] = {64, 1, 128};
-    if (!encode_tmap_bf16(&qr_map, p.q_rope, 3, dims, strides, box)) return cudaErrorInvalidValue;
-  }
   {
     const uint64_t dims[3] = {(uint64_t)p.nope, (uint64_t)p.heads, buf_rows};
     const uint64_t strides[2] = {(uint64_t)p.k_head_stride * 2, (uint64_t)p.k_row_stride * 2};
@@ -589,6 +662,12 @@ cudaError_t launch_tc_prefill(const PrefillParams& p, cudaStream_t stream) {
   }
   PrefillArgs a;
   memset(&a, 0, sizeof(a));
+  a.q_nope = p.q_nope;
+  a.qn_row_stride = p.qn_row_stride;
+  a.qn_head_stride = p.qn_head_stride;
+  a.q_rope = p.q_rope;
+  a.qr_row_stride = p.qr_row_stride;
+  a.qr_head_stride = p.qr_head_stride;
   a.kv_start = p.kv_start;
   a.kv_len = p.kv_len;
   a.t_max = p.t_max;
@@ -604,7 +683,7 @@ cudaError_t launch_tc_prefill(const PrefillParams& p, cudaStream_t stream) {
   a.lse = p.lse;
   a.status = p.status;
   const dim3 grid((unsigned)a.n_qtiles, (unsigned)p.heads, (unsigned)p.batch);
-  tc_prefill_kernel<<<grid, PF_THREADS, PF_SMEM, stream>>>(qn_map, qr_map, k_map, r_map, v_map, a);
+  tc_prefill_kernel<<<grid, PF_THREADS, PF_SMEM, stream>>>(k_map, r_map, v_map, a);
   return cudaGetLastError();
 }
 
