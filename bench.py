@@ -398,6 +398,41 @@ def ours(args):
     rb_bytes = 2 * rb_B * rb_w * (w.rank + w.rope) * rb_lat.element_size()
     del rb_lat, rb_rope, rb_dst
 
+    # the reconstructed prefill of a 4096-token prompt (RoPE of the query rope
+    # part, per-head K/V materialisation, causal attention), three launches per
+    # step, each part also timed alone; CUDA graphs of 3 steps, replayed
+    from mla_latent_kv_12_gb300.pipeline import PrefillStep
+    pf = PrefillStep(W.make_inputs(W.PREFILL_BF16), dev)
+
+    def graph_us(fn, per_graph=3, reps=3):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                for _ in range(per_graph):
+                    fn()
+        g.replay()
+        torch.cuda.synchronize()
+        a0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        return a0.elapsed_time(a1) / (per_graph * reps) * 1e3
+
+    pf_step_us = graph_us(pf.run)
+    pf_att_us = graph_us(pf.attend)
+    pf_rec_us = graph_us(pf.reconstruct)
+    pf_rope_us = graph_us(pf.rope_q)
+    pfw = pf.w
+    pf_pairs = sum(max(int(pf.inp.kv_len[b]) - pfw.s_q + i + 1, 0) for b in range(pfw.batch) for i in range(pfw.s_q))
+    pf_att_flops = pf_pairs * 2 * pfw.heads * (pfw.nope + pfw.rope + pfw.v)
+    pf_rec_flops = 2 * pf.latent.shape[0] * pf.latent.shape[1] * pfw.rank * pfw.heads * (pfw.nope + pfw.v)
+    pf_status = int(pf.status.item())
+    del pf
+
     hbm, tf_burst, tf_sus, src = load_peaks()
     byts, flops = algorithmic(inp)
     ach_gbs = byts / (dec_ms / 1e3) / 1e9
@@ -442,6 +477,16 @@ def ours(args):
         "select_topk": {"us_per_call": select_us, "rows": w.n_q, "top_k": sel_k, "score_bytes": sel_bytes,
                         "note": "mla_select_topk over f32 scores of each query row's window, "
                                 "10 calls per CUDA graph, replayed"},
+        "prefill": {"workload": W.PREFILL_BF16.name, "us_per_step": pf_step_us,
+                    "tokens_per_s": pfw.n_q / (pf_step_us * 1e-6),
+                    "attention_us": pf_att_us, "attention_tflops": pf_att_flops / (pf_att_us * 1e-6) / 1e12,
+                    "attention_frac_of_measured_bf16_burst": pf_att_flops / (pf_att_us * 1e-6) / 1e12 / tf_burst,
+                    "reconstruct_us": pf_rec_us,
+                    "reconstruct_tflops": pf_rec_flops / (pf_rec_us * 1e-6) / 1e12,
+                    "rope_us": pf_rope_us, "device_status": pf_status,
+                    "note": "mla_rope_partial_interleaved + mla_reconstruct_kv + mla_prefill_attend; attention "
+                            "flops = causal (query, key) pairs x 2 x H x (nope + rope + v); 3 steps per CUDA "
+                            "graph, replayed"},
         "rollback": {"us_per_call": rollback_us, "bytes_per_call": rb_bytes,
                      "gbs": rb_bytes / (rollback_us * 1e-6) / 1e9,
                      "frac_of_measured_hbm": rb_bytes / (rollback_us * 1e-6) / 1e9 / hbm,
