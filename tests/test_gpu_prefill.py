@@ -108,3 +108,33 @@ def test_prefill_flags_a_window_outside_the_buffer():
     torch.cuda.synchronize()
     assert int(step.status.item()) == 0
     _check(step, inp, list(range(0, w.n_q, 7)), [3])
+
+
+def test_chunked_prefill_after_a_long_cache_sampled():
+    # a 512-token chunk appended after ~3000 cached tokens per row (packed rows):
+    # the chunk's queries see the whole earlier cache plus their causal prefix
+    w = dataclasses.replace(W.PREFILL_BF16, name="prefill_chunk", batch=3, s_q=512, t=0, seed=9,
+                            ragged=(2900, 3100))
+    inp = W.make_inputs(w, layout="flat")
+    step = PrefillStep(inp, DEV)
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    rows = [0, 127, 128, 511, 512, 700, 1023, 1024, 1300, 1535]
+    _check(step, inp, rows, [2, 100])
+
+
+def test_single_token_prefill_equals_the_decode_path():
+    # S_q = 1 through the prefill path matches the absorbed decode step on the same inputs
+    w = dataclasses.replace(W.DENSE_BF16, name="prefill_one", t=1000, seed=10)
+    inp = W.make_inputs(w)
+    step = PrefillStep(inp, DEV)
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    _check(step, inp, [0], list(range(0, 128, 9)))
+    from mla_latent_kv_12_gb300.pipeline import DecodeStep
+    dstep = DecodeStep(inp, DEV)
+    dstep.run()
+    torch.cuda.synchronize()
+    H.assert_close(step.out.cpu(), dstep.out.cpu().to(torch.float64).numpy(), "bf16", "prefill vs decode")
