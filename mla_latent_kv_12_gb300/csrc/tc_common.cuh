@@ -176,6 +176,19 @@ __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Named barrier over `count` threads that also ORs a predicate across them:
+// every participant gets the same answer.
+__device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
 // 2^x on the special-function unit (PTX ex2.approx; relative error ~2^-22,
 // +0 for -inf).
 __device__ __forceinline__ float ex2_approx(float x) {

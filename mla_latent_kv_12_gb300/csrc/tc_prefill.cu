@@ -7,10 +7,11 @@
 //
 //   tc_reconstruct_kernel  K_nope[t,h,:] = latent[t,:] . W_UK_h^T,
 //                          V[t,h,:]      = latent[t,:] . W_UV_h^T
-//     grid (row tiles of 128, heads), one tcgen05 MMA chain M=128 tokens x
-//     N=256 (head h's 256 rows of kv_b_proj) x K=rank, fed by a 2-stage TMA
-//     ring (two CTAs per SM); the f32 accumulator is rounded to bf16 into swizzled shared memory
-//     and written with TMA tensor stores.
+//     persistent (one CTA per SM over (128-row tile, head) tiles): per tile
+//     one tcgen05 MMA chain M=128 tokens x N=256 (head h's 256 rows of
+//     kv_b_proj) x K=rank, fed by a 3-stage TMA ring, into one of two TMEM
+//     accumulators; the epilogue warps round the other accumulator to bf16
+//     into swizzled shared memory and write it with TMA tensor stores.
 //
 //   tc_prefill_kernel      causal flash attention, one CTA per (128 query
 //     rows, head, batch row).  Q (nope || rotated rope, 192 features) is
@@ -53,30 +54,35 @@ __device__ __forceinline__ uint32_t sw128(int r, int u) { return (uint32_t)(r * 
 
 // ------------------------------------------------------------------ reconstruct
 
-constexpr int RC_STAGES = 2;       // two CTAs per SM: one's epilogue overlaps the other's MMAs
+constexpr int RC_STAGES = 3;
 constexpr int RC_A_BYTES = kChunk;          // 128 tokens x 64 latent features
 constexpr int RC_B_BYTES = 2 * kChunk;      // 256 weight rows x 64 latent features
 constexpr int RC_STAGE_BYTES = RC_A_BYTES + RC_B_BYTES;
-constexpr int RC_SMEM = 1024 + RC_STAGES * RC_STAGE_BYTES;
-constexpr int RC_THREADS = 192;
+constexpr int RC_OUT_BYTES = 4 * kChunk;    // one tile's bf16 output: K_nope x2 | V x2 chunks
+constexpr int RC_SMEM = 1024 + RC_STAGES * RC_STAGE_BYTES + RC_OUT_BYTES;
+constexpr int RC_THREADS = 192;             // producer, MMA issuer, 4 epilogue warps
 
 struct ReconArgs {
   int32_t k_chunks;     // rank / 64
   int32_t head_rows;    // nope + v rows of kv_b_proj per head
+  int32_t row_tiles;    // 128-row tiles
+  int32_t n_tiles;      // row_tiles * heads (tile = row tile fastest, then head)
   int32_t* status;
 };
 
-__global__ void __launch_bounds__(RC_THREADS, 2)
+// Persistent: CTA c takes tiles c, c + grid, ...  Two TMEM accumulators of
+// 256 columns: the epilogue of one tile runs under the MMAs of the next.
+__global__ void __launch_bounds__(RC_THREADS, 1)
     tc_reconstruct_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__ CUtensorMap w_map,
                           const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                           const __grid_constant__ ReconArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full_bar[RC_STAGES], empty_bar[RC_STAGES], mma_done;
+  uint8_t* out_s = smem + RC_STAGES * RC_STAGE_BYTES;
+  __shared__ __align__(8) uint64_t full_bar[RC_STAGES], empty_bar[RC_STAGES], acc_full[2], acc_empty[2], mma_drain;
   __shared__ uint32_t tmem_s;
   __shared__ volatile int abort_s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row0 = blockIdx.x * 128, h = blockIdx.y;
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&lat_map);
@@ -87,12 +93,16 @@ __global__ void __launch_bounds__(RC_THREADS, 2)
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    mbar_init(&mma_done, 1);
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&acc_full[q], 1);
+      mbar_init(&acc_empty[q], 128);
+    }
+    mbar_init(&mma_drain, 1);
     abort_s = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_s, 256);
+    tmem_alloc(&tmem_s, 512);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -103,22 +113,28 @@ __global__ void __launch_bounds__(RC_THREADS, 2)
     abort_s = 1;
     if (a.status) atomicOr(a.status, MLA_DEVICE_TIMEOUT);
   };
+  const int n_mine = a.n_tiles > (int)blockIdx.x ? (a.n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
 
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer
+    // ------------------------------------------------ TMA producer: every k-chunk of every tile
     bool issued[RC_STAGES] = {};
     uint32_t issued_phase[RC_STAGES] = {};
     if (lane == 0) {
-      for (int kc = 0; kc < a.k_chunks && !abort_s; ++kc) {
-        const int s = kc % RC_STAGES;
-        const uint32_t ph = (uint32_t)(kc / RC_STAGES) & 1u;
-        if (kc >= RC_STAGES && !mbar_wait(&empty_bar[s], ph ^ 1u, kWaitLimit)) { fail(); break; }
-        uint8_t* st = smem + s * RC_STAGE_BYTES;
-        mbar_arrive_expect_tx(&full_bar[s], RC_STAGE_BYTES);
-        tma_load_2d(st, &lat_map, &full_bar[s], kc * 64, row0);
-        tma_load_2d(st + RC_A_BYTES, &w_map, &full_bar[s], kc * 64, h * a.head_rows);
-        issued[s] = true;
-        issued_phase[s] = ph;
+      int q = 0;
+      for (int it = 0; it < n_mine && !abort_s; ++it) {
+        const int tile = (int)blockIdx.x + it * (int)gridDim.x;
+        const int row0 = (tile % a.row_tiles) * 128, h = tile / a.row_tiles;
+        for (int kc = 0; kc < a.k_chunks && !abort_s; ++kc, ++q) {
+          const int s = q % RC_STAGES;
+          const uint32_t ph = (uint32_t)(q / RC_STAGES) & 1u;
+          if (q >= RC_STAGES && !mbar_wait(&empty_bar[s], ph ^ 1u, kWaitLimit)) { fail(); break; }
+          uint8_t* st = smem + s * RC_STAGE_BYTES;
+          mbar_arrive_expect_tx(&full_bar[s], RC_STAGE_BYTES);
+          tma_load_2d(st, &lat_map, &full_bar[s], kc * 64, row0);
+          tma_load_2d(st + RC_A_BYTES, &w_map, &full_bar[s], kc * 64, h * a.head_rows);
+          issued[s] = true;
+          issued_phase[s] = ph;
+        }
       }
       for (int s = 0; s < RC_STAGES; ++s)
         if (issued[s]) mbar_wait(&full_bar[s], issued_phase[s], kWaitLimit);
@@ -127,39 +143,64 @@ __global__ void __launch_bounds__(RC_THREADS, 2)
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     const uint32_t idesc = idesc_bf16_f32(128, 256, 0, 0);
-    for (int kc = 0; kc < a.k_chunks; ++kc) {
-      const int s = kc % RC_STAGES;
-      if (!mbar_wait_warp(&full_bar[s], (uint32_t)(kc / RC_STAGES) & 1u, kWaitLimit)) { fail(); break; }
+    const uint64_t desc0 = smem_desc(smem_u32(smem), 16, 1024, kSwizzle128B);
+    bool ok = true;
+    int q = 0;
+    for (int it = 0; ok && it < n_mine; ++it) {
+      const int acc = it & 1;
+      // The epilogue has read this accumulator's previous tile.
+      if (it >= 2 && !mbar_wait_warp(&acc_empty[acc], (uint32_t)((it >> 1) - 1) & 1u, kWaitLimit)) { ok = false; break; }
       tc_fence_after();
-      const uint64_t ad = smem_desc(smem_u32(smem + s * RC_STAGE_BYTES), 16, 1024, kSwizzle128B);
-      const uint64_t bd = ad + (uint64_t)(RC_A_BYTES >> 4);
-      const uint32_t first = kc == 0 ? 0u : 1u;
-      if (elect_one()) {
+      for (int kc = 0; kc < a.k_chunks; ++kc, ++q) {
+        const int s = q % RC_STAGES;
+        if (!mbar_wait_warp(&full_bar[s], (uint32_t)(q / RC_STAGES) & 1u, kWaitLimit)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t ad = desc0 + (uint64_t)(s * (RC_STAGE_BYTES >> 4));
+        const uint64_t bd = ad + (uint64_t)(RC_A_BYTES >> 4);
+        const uint32_t first = kc == 0 ? 0u : 1u;
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ss(tmem, ad + (uint64_t)((k * 32) >> 4), bd + (uint64_t)((k * 32) >> 4), idesc, k == 0 ? first : 1u);
-        mma_commit(&empty_bar[s]);
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tmem + (uint32_t)(acc * 256), ad + (uint64_t)((k * 32) >> 4), bd + (uint64_t)((k * 32) >> 4),
+                   idesc, k == 0 ? first : 1u);
+          mma_commit(&empty_bar[s]);
+        }
+        __syncwarp();
       }
+      if (!ok) break;
+      if (elect_one()) mma_commit(&acc_full[acc]);
       __syncwarp();
+      if (abort_s) ok = false;
     }
-    if (lane == 0) mma_commit(&mma_done);
+    if (!ok) fail();
+    if (elect_one()) mma_commit(&mma_drain);
     __syncwarp();
+    mbar_wait_warp(&mma_drain, 0, kWaitLimit);
   } else {
     // ------------------------------------------------ epilogue (warps 2..5)
     const int quarter = warp & 3;
     const int r = 32 * quarter + lane;                     // token row of the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
-    const bool ok = mbar_wait_warp(&mma_done, 0, kWaitLimit);
-    if (!ok) fail();
-    if (ok && !abort_s) {
+    const bool issuer = warp == 2 && lane == 0;
+    for (int it = 0; it < n_mine; ++it) {
+      const int acc = it & 1;
+      const int tile = (int)blockIdx.x + it * (int)gridDim.x;
+      const int row0 = (tile % a.row_tiles) * 128, h = tile / a.row_tiles;
+      const bool ok = mbar_wait_warp(&acc_full[acc], (uint32_t)(it >> 1) & 1u, kWaitLimit);
+      if (!ok) fail();
+      // The previous tile's stores have read the staging buffer.
+      if (issuer) bulk_wait_read();
+      // One decision for all four warps, so that none waits at a barrier the
+      // others have left.
+      if (named_sync_or(1, 128, !ok || abort_s)) break;
       tc_fence_after();
       // Chunks 0,1 = K_nope features 0..63, 64..127; chunks 2,3 = V.
 #pragma unroll 1
       for (int p = 0; p < 8; ++p) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_off + p * 32, v);
-        tmem_wait_ld();
-        uint8_t* chunk = smem + (p >> 1) * kChunk;
+        tmem_ld32(tmem + (uint32_t)(acc * 256) + lane_off + p * 32, v);
+        tmem_wait_ld_regs(v);
+        uint8_t* chunk = out_s + (p >> 1) * kChunk;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           uint4 w;
@@ -170,24 +211,27 @@ __global__ void __launch_bounds__(RC_THREADS, 2)
           *reinterpret_cast<uint4*>(chunk + sw128(r, (p & 1) * 4 + u)) = w;
         }
       }
+      // The accumulator may take the next tile once every lane's loads are done.
+      tc_fence_before();
+      mbar_arrive(&acc_empty[acc]);
       fence_proxy_async_smem();
+      named_sync(1, 128);
+      if (issuer) {
+        tma_store_3d(&k_map, out_s, 0, h, row0);
+        tma_store_3d(&k_map, out_s + kChunk, 64, h, row0);
+        tma_store_3d(&v_map, out_s + 2 * kChunk, 0, h, row0);
+        tma_store_3d(&v_map, out_s + 3 * kChunk, 64, h, row0);
+        bulk_commit();
+      }
     }
-    named_sync(1, 128);
-    if (ok && !abort_s && warp == 2 && lane == 0) {
-      tma_store_3d(&k_map, smem, 0, h, row0);
-      tma_store_3d(&k_map, smem + kChunk, 64, h, row0);
-      tma_store_3d(&v_map, smem + 2 * kChunk, 0, h, row0);
-      tma_store_3d(&v_map, smem + 3 * kChunk, 64, h, row0);
-      bulk_commit();
-      bulk_wait_all();
-    }
+    if (issuer) bulk_wait_all();
     __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -628,8 +672,12 @@ cudaError_t launch_tc_reconstruct(const ReconstructParams& p, cudaStream_t strea
     cudaFuncSetAttribute(tc_reconstruct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RC_SMEM);
     attr = true;
   }
-  ReconArgs a{p.rank / 64, p.nope + p.v_dim, p.status};
-  const dim3 grid((unsigned)((p.n_rows + 127) / 128), (unsigned)p.heads);
+  const int row_tiles = (int)((p.n_rows + 127) / 128);
+  const int64_t n_tiles = (int64_t)row_tiles * p.heads;
+  if (n_tiles >= (1LL << 31)) return cudaErrorInvalidValue;
+  ReconArgs a{p.rank / 64, p.nope + p.v_dim, row_tiles, (int32_t)n_tiles, p.status};
+  const int sms = device_sm_count();
+  const unsigned grid = (unsigned)(n_tiles < sms ? n_tiles : sms);
   tc_reconstruct_kernel<<<grid, RC_THREADS, RC_SMEM, stream>>>(lat_map, w_map, k_map, v_map, a);
   return cudaGetLastError();
 }
