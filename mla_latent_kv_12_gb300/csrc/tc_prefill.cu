@@ -14,16 +14,14 @@
 //     into swizzled shared memory and write it with TMA tensor stores.
 //
 //   tc_prefill_kernel      causal flash attention, one CTA per (128 query
-//     rows, head, batch row).  Q (nope || rotated rope, 192 features) is
-//     loaded once into TMEM (the score MMAs read A from there, which issues
-//     faster than from shared memory); each 128-key tile brings K_nope and the
-//     cache's shared rope key (one ring, freed when the tile's scores are
-//     done) and V
+//     rows, head, batch row).  Q (nope || rotated rope, 192 features) stays
+//     in shared memory; each 128-key tile brings K_nope and the cache's
+//     shared rope key (one ring, freed when the tile's scores are done) and V
 //     (a second ring, freed when its P.V is done) by TMA.  Warp 1 issues
 //     S(j+1) = Q.K^T into one of two TMEM score buffers while eight softmax
 //     warps (two per quarter of the query rows, 64 score columns each) turn
-//     S(j) into bf16 P in place; then it issues O += P.V with P read from
-//     TMEM.  The running maximum is only moved when
+//     S(j) into bf16 P (two TMEM buffers of their own); then it issues
+//     O += P.V with P read from TMEM.  The running maximum is only moved when
 //     it grows by more than 2^8 (the accumulated O and sum are then rescaled
 //     in TMEM), so most tiles skip the correction.
 #include <cuda_bf16.h>
@@ -238,19 +236,16 @@ __global__ void __launch_bounds__(RC_THREADS, 1)
 // ------------------------------------------------------------------ prefill attention
 
 constexpr int PF_STAGES = 2;                  // per ring
+constexpr int PF_Q_BYTES = 3 * kChunk;        // Q tile: nope 0..63 | nope 64..127 | rope
 constexpr int PF_K_BYTES = 3 * kChunk;        // K_nope x2 | rope  (freed when S completes)
 constexpr int PF_V_BYTES = 2 * kChunk;        // V x2              (freed when P.V completes)
-constexpr int PF_SMEM = 1024 + PF_STAGES * (PF_K_BYTES + PF_V_BYTES);
+constexpr int PF_SMEM = 1024 + PF_Q_BYTES + PF_STAGES * (PF_K_BYTES + PF_V_BYTES);
 constexpr int PF_THREADS = 352;               // K producer, MMA, 8 softmax warps, V producer
-constexpr uint32_t PF_TM_O = 256;             // TMEM: S0 at 0, S1 at 128, O at 256, Q at 384
-constexpr uint32_t PF_TM_Q = 384;             // 192 bf16 features = 96 columns
+constexpr uint32_t PF_TM_O = 256;             // TMEM: S0 at 0, S1 at 128, O at 256, P0 at 384, P1 at 448
+constexpr uint32_t PF_TM_P = 384;             // 128 keys of bf16 P = 64 columns per buffer
 constexpr float kRescaleLog2 = 8.f;
 
 struct PrefillArgs {
-  const void* q_nope;
-  int64_t qn_row_stride, qn_head_stride;
-  const void* q_rope;
-  int64_t qr_row_stride, qr_head_stride;
   const int32_t* kv_start;
   const int32_t* kv_len;
   int64_t t_max;         // buffer rows of one batch row (the packed buffer's rows when packed)
@@ -265,13 +260,15 @@ struct PrefillArgs {
 };
 
 __global__ void __launch_bounds__(PF_THREADS, 1)
-    tc_prefill_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap r_map,
+    tc_prefill_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_constant__ CUtensorMap qr_map,
+                      const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap r_map,
                       const __grid_constant__ CUtensorMap v_map, const __grid_constant__ PrefillArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* k_ring = smem;
+  uint8_t* q_s = smem;
+  uint8_t* k_ring = smem + PF_Q_BYTES;
   uint8_t* v_ring = k_ring + PF_STAGES * PF_K_BYTES;
-  __shared__ __align__(8) uint64_t q_tmem, k_full[PF_STAGES], k_empty[PF_STAGES], v_full[PF_STAGES],
+  __shared__ __align__(8) uint64_t q_full, k_full[PF_STAGES], k_empty[PF_STAGES], v_full[PF_STAGES],
       v_empty[PF_STAGES], s_full[2], p_full, pv_done, mma_drain, xbar[2][4], lbar[4];
   __shared__ float red_max[2][2][128], red_sum[2][128];
   __shared__ uint32_t tmem_s;
@@ -293,12 +290,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
   const int64_t key_end = min(len, offs + i_hi + 1);
   const int n_kt = key_end > 0 ? (int)((key_end + 127) / 128) : 0;
   const int64_t ybase = (a.packed ? 0 : (int64_t)b * a.t_max) + start;
+  const int q_row0 = b * a.s_q + i0;
 
   if (threadIdx.x == 0) {
+    tma_prefetch_desc(&qn_map);
+    tma_prefetch_desc(&qr_map);
     tma_prefetch_desc(&k_map);
     tma_prefetch_desc(&r_map);
     tma_prefetch_desc(&v_map);
-    mbar_init(&q_tmem, 256);
+    mbar_init(&q_full, 1);
     for (int s = 0; s < PF_STAGES; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -341,7 +341,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     uint64_t* emptyb = kside ? k_empty : v_empty;
     bool issued[PF_STAGES] = {};
     uint32_t issued_phase[PF_STAGES] = {};
+    bool q_issued = false;
     if (lane == 0 && n_kt > 0) {
+      if (kside) {
+        mbar_arrive_expect_tx(&q_full, PF_Q_BYTES);
+        tma_load_3d(q_s, &qn_map, &q_full, 0, h, q_row0);
+        tma_load_3d(q_s + kChunk, &qn_map, &q_full, 64, h, q_row0);
+        tma_load_3d(q_s + 2 * kChunk, &qr_map, &q_full, 0, h, q_row0);
+        q_issued = true;
+      }
       for (int kt = 0; kt < n_kt && !abort_s; ++kt) {
         const int s = kt % PF_STAGES;
         const uint32_t ph = (uint32_t)(kt / PF_STAGES) & 1u;
@@ -363,6 +371,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         issued_phase[s] = ph;
       }
       // Every issued copy lands before the CTA may exit.
+      if (q_issued) mbar_wait(&q_full, 0, kWaitLimit);
       for (int s = 0; s < PF_STAGES; ++s)
         if (issued[s]) mbar_wait(&fullb[s], issued_phase[s], kWaitLimit);
     }
@@ -373,16 +382,17 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const uint32_t idesc_pv = idesc_bf16_f32(128, 128, 0, 1);
     // Stage s's descriptors are the base's plus s stage sizes (16-byte units).
     const uint64_t kdesc0 = smem_desc(smem_u32(k_ring), 16, 1024, kSwizzle128B);
+    const uint64_t qdesc = smem_desc(smem_u32(q_s), 16, 1024, kSwizzle128B);
     const uint64_t vdesc0 = smem_desc(smem_u32(v_ring), kChunk, 1024, kSwizzle128B);
     auto issue_s = [&](int j) -> bool {
       const int s = j % PF_STAGES;
       if (!mbar_wait_warp(&k_full[s], (uint32_t)(j / PF_STAGES) & 1u, kWaitLimit)) return false;
       tc_fence_after();
-      // A = Q from TMEM (features packed two per column), B = the K tile.
-      // Issued by one elected lane of the converged warp with descriptors
-      // that differ from a base by constants: the tensor core then accepts an
-      // M=128 N=128 MMA about every 68 cycles (a lane-0 branch with per-MMA
-      // descriptor arithmetic issues at roughly half that rate).
+      // A = the Q tile, B = the K tile, both in shared memory.  Issued by one
+      // elected lane of the converged warp with descriptors that differ from
+      // a base by constants: the tensor core then accepts an M=128 N=128 MMA
+      // about every 68 cycles (a lane-0 branch with per-MMA descriptor
+      // arithmetic issues at roughly half that rate).
       const uint64_t kd = kdesc0 + (uint64_t)(s * (PF_K_BYTES >> 4));
       const uint32_t d_s = tmem + (uint32_t)((j & 1) * 128);
       if (elect_one()) {
@@ -390,7 +400,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         for (int c = 0; c < 3; ++c)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ts(d_s, tmem + PF_TM_Q + (uint32_t)(c * 32 + k * 8),
+            mma_ss(d_s, qdesc + (uint64_t)((c * kChunk + k * 32) >> 4),
                    kd + (uint64_t)((c * kChunk + k * 32) >> 4), idesc_s, (c | k) != 0);
         mma_commit(&s_full[j & 1]);
         mma_commit(&k_empty[s]);
@@ -398,7 +408,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       __syncwarp();
       return true;
     };
-    bool ok = n_kt == 0 || mbar_wait_warp(&q_tmem, 0, kWaitLimit);
+    bool ok = n_kt == 0 || mbar_wait_warp(&q_full, 0, kWaitLimit);
     if (ok && n_kt > 0) ok = issue_s(0);
     for (int j = 0; ok && j < n_kt; ++j) {
       if (j + 1 < n_kt && !issue_s(j + 1)) { ok = false; break; }
@@ -421,7 +431,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
       if (!mbar_wait_warp(&p_full, (uint32_t)j & 1u, kWaitLimit)) { ok = false; break; }
       tc_fence_after();
       const uint64_t vd = vdesc0 + (uint64_t)(s * (PF_V_BYTES >> 4));
-      const uint32_t p_src = tmem + (uint32_t)((j & 1) * 128);
+      const uint32_t p_src = tmem + PF_TM_P + (uint32_t)((j & 1) * 64);
       const uint32_t first = j == 0 ? 0u : 1u;
       if (elect_one()) {
 #pragma unroll
@@ -457,36 +467,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const int64_t min_limit = offs + i0;                   // the tile's first row
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    if (n_kt > 0) {
-      // Q row into TMEM (the S MMAs' A operand): half 0 writes features
-      // 0..95 (q_nope), half 1 features 96..191 (q_nope tail, rotated q_rope),
-      // 16 bytes = 4 columns per load.  Rows past the block are zero.
-      uint4 qv[12];
-      const bool real = i < a.s_q;
-      const int64_t n = (int64_t)b * a.s_q + i;
-      const uint4* qn = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q_nope) +
-                                                       n * a.qn_row_stride + (int64_t)h * a.qn_head_stride);
-      const uint4* qr = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q_rope) +
-                                                       n * a.qr_row_stride + (int64_t)h * a.qr_head_stride);
-#pragma unroll
-      for (int u = 0; u < 12; ++u) {
-        const int unit = hf * 12 + u;                       // 0..15 q_nope, 16..23 q_rope
-        qv[u] = make_uint4(0, 0, 0, 0);
-        if (real) qv[u] = unit < 16 ? __ldg(qn + unit) : __ldg(qr + (unit - 16));
-      }
-#pragma unroll
-      for (int c = 0; c < 3; ++c) {
-        uint32_t rr[16];
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          rr[4 * u] = qv[4 * c + u].x, rr[4 * u + 1] = qv[4 * c + u].y, rr[4 * u + 2] = qv[4 * c + u].z,
-          rr[4 * u + 3] = qv[4 * c + u].w;
-        tmem_st16(tmem + lane_off + PF_TM_Q + 48u * (uint32_t)hf + 16u * (uint32_t)c, rr);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&q_tmem);
-    }
     for (int j = 0; j < n_kt; ++j) {
       if (!mbar_wait_warp(&s_full[j & 1], (uint32_t)(j >> 1) & 1u, kWaitLimit)) { ok = false; break; }
       tc_fence_after();
@@ -564,9 +544,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
           }
         }
       }
-      // P (bf16 pairs) over the scores: both warps of the quarter have read
-      // their scores (the maximum exchange above), so the columns are free.
-      tmem_st32(tmem + lane_off + (uint32_t)((j & 1) * 128) + 32u * (uint32_t)hf, pk);
+      // P (bf16 pairs) into its own buffer: the buffer last held P(j-2),
+      // whose P.V is complete (P.V(j-1), waited for above, accumulates into
+      // the same O after it).  The score buffer is left to the next scores:
+      // MMAs into different accumulators are not ordered, so P must not
+      // share columns with a later score MMA.
+      tmem_st32(tmem + lane_off + PF_TM_P + (uint32_t)((j & 1) * 64) + 32u * (uint32_t)hf, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&p_full);
@@ -683,8 +666,21 @@ cudaError_t launch_tc_reconstruct(const ReconstructParams& p, cudaStream_t strea
 }
 
 cudaError_t launch_tc_prefill(const PrefillParams& p, cudaStream_t stream) {
-  CUtensorMap k_map, r_map, v_map;
+  CUtensorMap qn_map, qr_map, k_map, r_map, v_map;
+  const uint64_t n_q = (uint64_t)p.batch * p.s_q;
   const uint64_t buf_rows = p.packed ? (uint64_t)p.t_max : (uint64_t)p.batch * p.t_max;
+  {
+    const uint64_t dims[3] = {(uint64_t)p.nope, (uint64_t)p.heads, n_q};
+    const uint64_t strides[2] = {(uint64_t)p.qn_head_stride * 2, (uint64_t)p.qn_row_stride * 2};
+    const uint32_t box[3] = {64, 1, 128};
+    if (!encode_tmap_bf16(&qn_map, p.q_nope, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)p.rope_dim, (uint64_t)p.heads, n_q};
+    const uint64_t strides[2] = {(uint64_t)p.qr_head_stride * 2, (uint64_t)p.qr_row_stride * 2};
+    const uint32_t box[3] = {64, 1, 128};
+    if (!encode_tmap_bf16(&qr_map, p.q_rope, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
   {
     const uint64_t dims[3] = {(uint64_t)p.nope, (uint64_t)p.heads, buf_rows};
     const uint64_t strides[2] = {(uint64_t)p.k_head_stride * 2, (uint64_t)p.k_row_stride * 2};
@@ -710,12 +706,6 @@ cudaError_t launch_tc_prefill(const PrefillParams& p, cudaStream_t stream) {
   }
   PrefillArgs a;
   memset(&a, 0, sizeof(a));
-  a.q_nope = p.q_nope;
-  a.qn_row_stride = p.qn_row_stride;
-  a.qn_head_stride = p.qn_head_stride;
-  a.q_rope = p.q_rope;
-  a.qr_row_stride = p.qr_row_stride;
-  a.qr_head_stride = p.qr_head_stride;
   a.kv_start = p.kv_start;
   a.kv_len = p.kv_len;
   a.t_max = p.t_max;
@@ -731,7 +721,7 @@ cudaError_t launch_tc_prefill(const PrefillParams& p, cudaStream_t stream) {
   a.lse = p.lse;
   a.status = p.status;
   const dim3 grid((unsigned)a.n_qtiles, (unsigned)p.heads, (unsigned)p.batch);
-  tc_prefill_kernel<<<grid, PF_THREADS, PF_SMEM, stream>>>(k_map, r_map, v_map, a);
+  tc_prefill_kernel<<<grid, PF_THREADS, PF_SMEM, stream>>>(qn_map, qr_map, k_map, r_map, v_map, a);
   return cudaGetLastError();
 }
 
