@@ -27,6 +27,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MLA decode tokens/s and latent-cache HBM GB/s (% of GB300 roofline)"
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode +
+# combine launch pair of the current kernels, from an ncu capture of this
+# bench (cold caches between launches, so the split partials' round trip,
+# 4.2 MB at B=1, is counted as a DRAM re-read that a warm L2 serves).
+MEASURED_TRAFFIC = {"dense_bf16_b1_t4096_h128": 4953088 + 4226176}
 L2_BYTES = 129 * 2 ** 20
 
 
@@ -442,7 +447,7 @@ def ours(args):
             if mem_bound else
             {"bound": "tensor", "achieved": ach_tf, "peak": tf_burst, "unit": "TFLOP/s",
              "frac": ach_tf / tf_burst})
-    roof.update({"traffic": None, "kernel": "mla_decode_attend (decode + combine)",
+    roof.update({"traffic": MEASURED_TRAFFIC.get(w.name), "kernel": "mla_decode_attend (decode + combine)",
                  "peak_source": src, "algorithmic_bytes": byts, "algorithmic_flops": flops,
                  "kernel_ms": dec_ms, "tensor_tflops": ach_tf, "cache_gbs": ach_gbs})
 
