@@ -10,9 +10,9 @@
 //    context accumulator [128 x 512] would fill a whole SM's TMEM, so the pair
 //    splits the feature axis evenly: CTA r scores latent dims [256r, 256r+256)
 //    and rope dims [32r, 32r+32) (18 MMA K-steps each).  Each CTA rounds its
-//    partial scores to fp16 and sends them to the peer with one bulk copy per
-//    tile into the peer's shared memory (counted as transactions on the
-//    receiving barrier); both CTAs then add the same two fp16 partials in f32
+//    partial scores to fp16 and stores them straight into the peer's shared
+//    memory with asynchronous remote stores (st.async, counted as
+//    transactions on the receiving barrier); both CTAs then add the same two fp16 partials in f32
 //    (commutative, so bit-identical), run the same online softmax, and each
 //    accumulates O[:, own 256 latent dims] += P . latent[:, own dims].  No MMA
 //    work is repeated and every latent byte is read by one CTA (the 128-byte
@@ -291,7 +291,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   uint8_t* smem = smem_raw;
   uint8_t* stages = smem;
   // Exchange buffers, each [8][128 heads][16 B] of fp16 scores: xin[b] is written
-  // by the peer's bulk copy, xout[b] is staged here and copied to the peer.
+  // by the peer's remote stores, xout[b] holds this CTA's own half for its
+  // softmax warps.
   uint8_t* xin = smem + STAGES * STAGE_BYTES;        // 2 x XH_BYTES
   uint8_t* xout = xin + 2 * XH_BYTES;                // 2 x XH_BYTES
 
@@ -332,7 +333,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     mbar_init(&q_full, 8);      // softmax warps (latent dims 0..127, rope) + exchange warps (128..255)
     mbar_init(&o_free, 4);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&x_full[b], 1);   // local expect_tx arrival + the peer's bulk-copy bytes
+      mbar_init(&x_full[b], 1);   // local expect_tx arrival + the peer's remote-store bytes
       mbar_init(&x_free[b], 4);   // the peer's softmax warps have read xin[b] (so our copy is done)
       mbar_init(&xo_full[b], 4);  // our exchange warps have staged xout[b]
       mbar_init(&xo_free[b], 4);  // our softmax warps have read xout[b]
@@ -594,8 +595,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else if (warp >= 6 && warp < 10) {
     // ============================================================ exchange warps
     // Read this CTA's partial scores from TMEM, round them to fp16 (saturating)
-    // and send them to the peer with one bulk copy per tile, one tile ahead of
-    // the softmax warps (two send and two receive buffers).
+    // and send them to the peer with remote stores, one tile ahead of the
+    // softmax warps (two send and two receive buffers).
     const int quarter = warp & 3;
     const int h = 32 * quarter + lane;
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
@@ -652,7 +653,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_free);
+        // Each 16-byte piece goes to our own softmax warps (xout) and, as an
+        // asynchronous remote store that completes on the peer's x_full, into
+        // the peer's receive buffer: no staging round trip, no bulk copy.
         uint8_t* xo = xout + b * XH_BYTES;
+        const uint32_t xi = xin_peer + b * XH_BYTES;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           uint32_t w[4];
@@ -665,17 +670,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             w[q] = *reinterpret_cast<const uint32_t*>(&hv);
           }
           *reinterpret_cast<uint4*>(xo + (c * 128 + h) * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+          st_async_v4(xi + (uint32_t)((c * 128 + h) * 16), w[0], w[1], w[2], w[3], x_full_peer[b]);
         }
-        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&xo_full[b]);
-        if (issuer) {
-          if (!mbar_wait(&xo_full[b], use & 1u, kWaitLimit))
-            fail();
-          else
-            bulk_copy_to_peer(xin_peer + b * XH_BYTES, smem_u32(xo), XH_BYTES, x_full_peer[b]);
-          mbar_arrive_expect_tx_u32(smem_u32(&x_full[b]), XH_BYTES);
-        }
+        // Our receive buffer b expects the peer's XH_BYTES for this tile.
+        if (issuer) mbar_arrive_expect_tx_u32(smem_u32(&x_full[b]), XH_BYTES);
         ++tile;
       }
     }
@@ -930,7 +930,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
 
   // ---------------------------------------------------------------- teardown
-  if (warp == 8 && lane == 0) bulk_wait_all();   // the exchange issuer's copies are done
   pdl_trigger();
   tc_fence_before();
   __syncthreads();
