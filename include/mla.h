@@ -430,7 +430,9 @@ int mla_rollback_lengths(const int32_t* kv_len_before, const int32_t* keep, cons
  *                                                h*(nope+v_dim) .. +nope)
  *   v[t, h, :]      = latent[t, :] . W_UV_h^T   (the next v_dim rows)
  * kv_b_proj is [heads*(nope+v_dim), rank] contiguous.  k_nope / v element
- * (t, h, d) sits at t*row_stride + h*head_stride + d.  bf16 in and out, f32
+ * (t, h, d) sits at t*row_stride + h*head_stride + d, rows and heads not
+ * overlapping (row-major or head-major; else MLA_ERR_INVALID_ARGUMENT).
+ * bf16 in and out, f32
  * accumulation.  Served: bf16, nope = v_dim = 128, rank a multiple of 64 up
  * to 1024, 16-byte aligned pointers and strides; other requests return
  * MLA_ERR_UNSUPPORTED.  The rope part of the keys is not materialised: it is

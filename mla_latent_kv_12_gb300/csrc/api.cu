@@ -645,6 +645,14 @@ int mla_reconstruct_kv(const void* latent, int64_t latent_row_stride, int64_t n_
   MLA_CHECK(latent_row_stride >= rank && k_head_stride >= nope && v_head_stride >= v_dim && k_row_stride >= 0 &&
                 v_row_stride >= 0,
             "reconstruct: strides too small");
+  // The outputs are written: their (row, head) vectors must not overlap, in a
+  // row-major ([rows, heads, d]) or head-major ([heads, rows, d]) layout.
+  auto disjoint = [&](int64_t row_stride, int64_t head_stride, int64_t d) {
+    return (row_stride >= (int64_t)heads * head_stride && head_stride >= d) ||
+           (head_stride >= n_rows * row_stride && row_stride >= d);
+  };
+  MLA_CHECK(disjoint(k_row_stride, k_head_stride, nope) && disjoint(v_row_stride, v_head_stride, v_dim),
+            "reconstruct: output rows or heads overlap");
   if (!(dtype == MLA_DTYPE_BF16 && nope == 128 && v_dim == 128 && rank % 64 == 0 && rank <= 1024 &&
         heads <= 65535))
     return fail(MLA_ERR_UNSUPPORTED, "reconstruct: served for bf16, nope = v = 128, rank a multiple of 64 "

@@ -229,3 +229,23 @@ def test_row_plans_reject_bad_bookkeeping(lib):
         lib.plan_filter([0, 1], [4, 3], [2], 4)
     with pytest.raises(lib.MLAError, match="right-aligned"):
         lib.plan_merge([4, 5], [0, 1], [4, 3])
+
+
+def test_reconstruct_and_prefill_validation(lib):
+    L = lib.lib
+    MB = 1 << 20
+    # latent, row stride, rows, kv_b_proj, H, nope, v, rank, k, k strides, v, v strides, dtype, status, stream
+    rec = [16 * MB, 512, 300, 64 * MB, 128, 128, 128, 512, 128 * MB, 128 * 256, 256, 128 * MB + 256, 128 * 256,
+           256, 1, None, None]
+    for i, v, want in [(0, None, 1), (2, 0, 1), (14, 5, 1), (1, 256, 1), (9, 64, 1), (5, 64, 2), (14, 0, 2),
+                       (0, 16 * MB + 2, 1)]:
+        bad = list(rec); bad[i] = v
+        assert L.mla_reconstruct_kv(*bad) == want, (i, v)
+    # q_nope + strides, q_rope + strides, k + strides, v + strides, rope + stride, packed, dtype, kv_start,
+    # kv_len, B, S, H, nope, rope, v, t_max, scale, out, out stride, out dtype, lse, status, stream
+    pf = [16 * MB, 128 * 128, 128, 20 * MB, 128 * 64, 64, 32 * MB, 128 * 256, 256, 32 * MB + 256, 128 * 256, 256,
+          48 * MB, 64, 0, 1, 16, 32, 2, 300, 128, 128, 64, 128, 700, 0.07, 64 * MB, 128 * 128, 1, None, None, None]
+    for i, v, want in [(0, None, 1), (16, None, 1), (19, 0, 1), (25, 0.0, 1), (25, float("inf"), 1),
+                       (27, 1000, 1), (21, 96, 2), (22, 96, 1), (15, 0, 2), (26, 64 * MB + 8, 1), (1, 100, 1)]:
+        bad = list(pf); bad[i] = v
+        assert L.mla_prefill_attend(*bad) == want, (i, v)
