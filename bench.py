@@ -31,7 +31,7 @@ METRIC = "MLA decode tokens/s and latent-cache HBM GB/s (% of GB300 roofline)"
 # combine launch pair of the current kernels, from an ncu capture of this
 # bench (cold caches between launches, so the split partials' round trip,
 # 4.2 MB at B=1, is counted as a DRAM re-read that a warm L2 serves).
-MEASURED_TRAFFIC = {"dense_bf16_b1_t4096_h128": 4953088 + 4226176}
+MEASURED_TRAFFIC = {"dense_bf16_b1_t4096_h128": 4952320 + 4226304}
 L2_BYTES = 129 * 2 ** 20
 
 
