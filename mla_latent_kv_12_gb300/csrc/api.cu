@@ -146,6 +146,10 @@ int mla_absorb_q(const void* q_nope, int64_t q_nope_row_stride, int64_t q_nope_h
   const bool tc = dtype == MLA_DTYPE_BF16 && nope == 128 && rank % 128 == 0 && rank <= 4096 &&
                   n_q <= 256 && aligned16(q_nope) && aligned16(kv_b_proj) &&
                   q_nope_head_stride % 8 == 0 && q_nope_row_stride % 8 == 0;
+  // Up to four rows the product is a matrix-vector product bound by the
+  // weight read: CUDA cores stream it (no MMA tile to fill).
+  if (dtype == MLA_DTYPE_BF16 && gemv_absorb_serves(p))
+    return cuda_status(launch_gemv_absorb(p, (cudaStream_t)stream), "absorb (matrix-vector) launch");
   if (tc) return cuda_status(launch_tc_absorb(p, (cudaStream_t)stream), "absorb (tensor core) launch");
   return cuda_status(launch_simt_absorb(p, dtype, (cudaStream_t)stream), "absorb launch");
 }
@@ -369,7 +373,9 @@ int mla_decode_step(const void* q_nope, int64_t q_nope_row_stride, int64_t q_nop
   rp.position_offset = q_position_offset;
   rp.out_col = rank;
   rope_inverse_frequencies(theta, rope_dim, rp.inv_freq);
-  st = cuda_status(launch_tc_absorb(ap, (cudaStream_t)stream, &rp), "decode_step: absorb + rope launch");
+  st = cuda_status(gemv_absorb_serves(ap) ? launch_gemv_absorb(ap, (cudaStream_t)stream, &rp)
+                                           : launch_tc_absorb(ap, (cudaStream_t)stream, &rp),
+                   "decode_step: absorb + rope launch");
   if (st != MLA_OK) return st;
   DecodeTail tail{kv_b_proj, out, out_row_stride, out_dtype, heads, nope, v_dim, rank};
   return cuda_status(launch_tc_decode(g, MLA_DTYPE_BF16, dws, dws_bytes, (cudaStream_t)stream, &tail),

@@ -94,6 +94,9 @@ void rope_inverse_frequencies(float theta, int rotary_dims, float* inv_freq);
 
 cudaError_t launch_simt_absorb(const AbsorbParams& p, int dtype, cudaStream_t stream);
 cudaError_t launch_tc_absorb(const AbsorbParams& p, cudaStream_t stream, const AbsorbRope* rope = nullptr);
+// CUDA-core matrix-vector absorb for 1..4 query rows (bf16, rank 512, nope 128).
+bool gemv_absorb_serves(const AbsorbParams& p);
+cudaError_t launch_gemv_absorb(const AbsorbParams& p, cudaStream_t stream, const AbsorbRope* rope = nullptr);
 
 struct ProjectParams {
   const void* ctx;
