@@ -1208,26 +1208,30 @@ __global__ void __launch_bounds__(PROJ_THREADS) tc_combine_project_kernel(const 
   tc_fence_after();
 
   bool ok = true;
-  if (threadIdx.x == 0) {
+  if (warp == 0) {
+    // One elected lane of the converged warp issues, descriptors = base + constants.
     const uint32_t idesc = idesc_bf16_f32(128, npad, 0, 0);
     const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
     for (int i = 0; i < 8 && ok; ++i) {
-      ok = mbar_wait(&bar_full[i], 0, kWaitLimit);
+      ok = mbar_wait_warp(&bar_full[i], 0, kWaitLimit);
       if (!ok) break;
       tc_fence_after();
+      const uint64_t ad = smem_desc(a0 + i * PROJ_BOX_BYTES, 16, 1024, kSwizzle128B);
+      const uint64_t bd = smem_desc(b0 + i * npad * 128, 16, 1024, kSwizzle128B);
+      if (elect_one()) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint64_t ad = smem_desc(a0 + i * PROJ_BOX_BYTES + k * 32, 16, 1024, kSwizzle128B);
-        const uint64_t bd = smem_desc(b0 + i * npad * 128 + k * 32, 16, 1024, kSwizzle128B);
-        mma_ss(tmem, ad, bd, idesc, (i | k) != 0);
+        for (int k = 0; k < 4; ++k)
+          mma_ss(tmem, ad + (uint64_t)((k * 32) >> 4), bd + (uint64_t)((k * 32) >> 4), idesc, (i | k) != 0);
       }
+      __syncwarp();
     }
-    if (!ok) {
+    if (!ok && lane == 0) {
       if (a.status) atomicOr(a.status, MLA_DEVICE_TIMEOUT);
       for (int i = 0; i < 8; ++i) mbar_wait(&bar_full[i], 0, kWaitLimit);  // drain in-flight copies
     }
-    mma_ok_s = ok ? 1 : 0;
-    mma_commit(&bar_mma);
+    if (lane == 0) mma_ok_s = ok ? 1 : 0;
+    if (elect_one()) mma_commit(&bar_mma);
+    __syncwarp();
   }
   __syncthreads();
   ok = mbar_wait_warp(&bar_mma, 0, kWaitLimit) && mma_ok_s != 0;
