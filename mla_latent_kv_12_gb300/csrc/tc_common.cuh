@@ -55,12 +55,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// Arrive on the barrier at shared::cluster address `remote` (another CTA's),
-// releasing this thread's prior shared::cluster stores at cluster scope.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
-}
-
 // Relaxed arrives for freeing a buffer that this thread's warp has just read:
 // `dep` must be a value computed from every datum read (so the warp has
 // received all of them before the arrive issues); no release fence is paid.
@@ -77,27 +71,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 }
 
 // try_wait without a suspend-time hint (measured faster on the decode's
-// per-tile hand-offs: the waiter resumes as soon as the phase completes); the
-// cluster-scope form below keeps a hint for the rarer cross-CTA waits.
-constexpr uint32_t kSuspendHintNs = 1000000;
-
+// per-tile hand-offs: the waiter resumes as soon as the phase completes).
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -114,16 +94,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
   return true;
 }
 
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, long long limit) {
-  const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait_cluster(a, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait_cluster(a, parity)) {
-    if (clock64() - t0 > limit) return false;
-  }
-  return true;
-}
-
 // Warp-uniform forms: every lane of the calling warp gets the same answer, so a
 // warp never splits on a timeout.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, long long limit) {
@@ -131,10 +101,6 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, l
   return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ bool mbar_wait_cluster_warp(uint64_t* bar, uint32_t parity, long long limit) {
-  const bool ok = mbar_wait_cluster(bar, parity, limit);
-  return __all_sync(0xffffffffu, ok);
-}
 
 // Arrive on the local barrier and raise its expected transaction bytes.
 __device__ __forceinline__ void mbar_arrive_expect_tx_u32(uint32_t bar, uint32_t bytes) {
@@ -148,17 +114,6 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t x, ui
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
                ::"r"(remote_addr), "r"(x), "r"(y), "r"(z), "r"(w), "r"(remote_bar)
                : "memory");
-}
-
-// Bulk copy of `bytes` from this CTA's shared memory into another CTA's
-// (shared::cluster address), completing as transactions on that CTA's barrier.
-__device__ __forceinline__ void bulk_copy_to_peer(uint32_t remote_dst, uint32_t local_src, uint32_t bytes,
-                                                  uint32_t remote_bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t"
-      "cp.async.bulk.commit_group;"
-      ::"r"(remote_dst), "r"(local_src), "r"(bytes), "r"(remote_bar)
-      : "memory");
 }
 
 // Wait until this thread's bulk copies have finished reading their source.
