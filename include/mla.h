@@ -116,9 +116,10 @@ int mla_rope_partial_interleaved(const void* in, void* out, int dtype, int64_t r
  * Only columns [0, rank) of each q_out head row are written, so q_out may be
  * the packed [n_q, H, rank+rope] query that mla_decode_attend reads.
  * fp32 accumulation; all three tensors have `dtype`.
- * bf16 with nope = 128, rank = 512, n_q <= 256 and 16-byte aligned pointers
- * and strides runs on the tensor cores (tcgen05); everything else on the CUDA
- * cores.
+ * bf16 with nope = 128, rank = 512 and 1..4 query rows is a matrix-vector
+ * product bound by the weight read and runs on the CUDA cores (one CTA per
+ * head); bf16 with 5..256 rows and 16-byte aligned pointers and strides runs
+ * on the tensor cores (tcgen05); everything else on the CUDA cores.
  */
 int mla_absorb_q(const void* q_nope, int64_t q_nope_row_stride, int64_t q_nope_head_stride,
                  const void* kv_b_proj, void* q_out, int64_t q_out_row_stride,
