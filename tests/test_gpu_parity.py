@@ -148,6 +148,14 @@ def test_verify_f32_tiny_causal():
     run_and_compare(inp)
 
 
+@pytest.mark.parametrize("batch", [2, 3, 4])
+def test_matrix_vector_absorb_row_counts(batch):
+    # 2..4 query rows take the CUDA-core absorb (with the query RoPE folded in
+    # the fused step); the granular run checks q_lat and the rotated q_rope.
+    w = dataclasses.replace(W.DENSE_BF16, batch=batch, t=700)
+    run_and_compare(W.make_inputs(w), heads=[0, 9, 64, 127])
+
+
 @pytest.mark.parametrize("batch", [1, 17, 64])
 def test_fused_step_row_counts(batch):
     # 1, 17 and 64 query rows: N = 16, 32 and 64 in the fused projection MMA,
