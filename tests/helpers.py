@@ -1,6 +1,6 @@
 """Shared helpers of the parity tests: tolerances, oracle adapters, comparisons.
 
-Tolerances (spec bounds): bf16 caches -- max-abs <= 2e-2 and relative L2
+Tolerances of the path's contract: bf16 caches -- max-abs <= 2e-2 and relative L2
 <= 5e-3; f32 caches -- relative L2 <= 1e-4; gathers and indices -- bit-exact.
 """
 from __future__ import annotations
