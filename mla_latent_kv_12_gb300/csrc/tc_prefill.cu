@@ -9,9 +9,10 @@
 //                          V[t,h,:]      = latent[t,:] . W_UV_h^T
 //     persistent (one CTA per SM over (128-row tile, head) tiles): per tile
 //     one tcgen05 MMA chain M=128 tokens x N=256 (head h's 256 rows of
-//     kv_b_proj) x K=rank, fed by a 3-stage TMA ring, into one of two TMEM
+//     kv_b_proj) x K=rank, fed by a 4-stage TMA ring, into one of two TMEM
 //     accumulators; the epilogue warps round the other accumulator to bf16
-//     into swizzled shared memory and write it with TMA tensor stores.
+//     into swizzled shared memory (half a tile at a time) and write it with
+//     TMA tensor stores.
 //
 //   tc_prefill_kernel      causal flash attention, one CTA per (128 query
 //     rows, head, batch row).  Q (nope || rotated rope, 192 features) stays
@@ -52,11 +53,11 @@ __device__ __forceinline__ uint32_t sw128(int r, int u) { return (uint32_t)(r * 
 
 // ------------------------------------------------------------------ reconstruct
 
-constexpr int RC_STAGES = 3;
+constexpr int RC_STAGES = 4;
 constexpr int RC_A_BYTES = kChunk;          // 128 tokens x 64 latent features
 constexpr int RC_B_BYTES = 2 * kChunk;      // 256 weight rows x 64 latent features
 constexpr int RC_STAGE_BYTES = RC_A_BYTES + RC_B_BYTES;
-constexpr int RC_OUT_BYTES = 4 * kChunk;    // one tile's bf16 output: K_nope x2 | V x2 chunks
+constexpr int RC_OUT_BYTES = 2 * kChunk;    // half a tile's bf16 output (K_nope, then V): 2 chunks
 constexpr int RC_SMEM = 1024 + RC_STAGES * RC_STAGE_BYTES + RC_OUT_BYTES;
 constexpr int RC_THREADS = 192;             // producer, MMA issuer, 4 epilogue warps
 
@@ -192,34 +193,43 @@ __global__ void __launch_bounds__(RC_THREADS, 1)
       // others have left.
       if (named_sync_or(1, 128, !ok || abort_s)) break;
       tc_fence_after();
-      // Chunks 0,1 = K_nope features 0..63, 64..127; chunks 2,3 = V.
+      // Two halves through one 32 KB staging buffer: K_nope (accumulator
+      // columns 0..127), then V (128..255), each as two 64-feature chunks.
 #pragma unroll 1
-      for (int p = 0; p < 8; ++p) {
-        uint32_t v[32];
-        tmem_ld32(tmem + (uint32_t)(acc * 256) + lane_off + p * 32, v);
-        tmem_wait_ld_regs(v);
-        uint8_t* chunk = out_s + (p >> 1) * kChunk;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1]));
-          w.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3]));
-          w.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5]));
-          w.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7]));
-          *reinterpret_cast<uint4*>(chunk + sw128(r, (p & 1) * 4 + u)) = w;
+      for (int half = 0; half < 2; ++half) {
+        if (half == 1) {
+          if (issuer) bulk_wait_read();       // the K_nope stores have read the buffer
+          named_sync(1, 128);
         }
-      }
-      // The accumulator may take the next tile once every lane's loads are done.
-      tc_fence_before();
-      mbar_arrive(&acc_empty[acc]);
-      fence_proxy_async_smem();
-      named_sync(1, 128);
-      if (issuer) {
-        tma_store_3d(&k_map, out_s, 0, h, row0);
-        tma_store_3d(&k_map, out_s + kChunk, 64, h, row0);
-        tma_store_3d(&v_map, out_s + 2 * kChunk, 0, h, row0);
-        tma_store_3d(&v_map, out_s + 3 * kChunk, 64, h, row0);
-        bulk_commit();
+#pragma unroll 1
+        for (int p = 0; p < 4; ++p) {
+          uint32_t v[32];
+          tmem_ld32(tmem + (uint32_t)(acc * 256 + half * 128 + p * 32) + lane_off, v);
+          tmem_wait_ld_regs(v);
+          uint8_t* chunk = out_s + (p >> 1) * kChunk;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1]));
+            w.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3]));
+            w.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5]));
+            w.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7]));
+            *reinterpret_cast<uint4*>(chunk + sw128(r, (p & 1) * 4 + u)) = w;
+          }
+        }
+        if (half == 1) {
+          // The accumulator may take the next tile once every lane's loads are done.
+          tc_fence_before();
+          mbar_arrive(&acc_empty[acc]);
+        }
+        fence_proxy_async_smem();
+        named_sync(1, 128);
+        if (issuer) {
+          const CUtensorMap* map = half == 0 ? &k_map : &v_map;
+          tma_store_3d(map, out_s, 0, h, row0);
+          tma_store_3d(map, out_s + kChunk, 64, h, row0);
+          bulk_commit();
+        }
       }
     }
     if (issuer) bulk_wait_all();
