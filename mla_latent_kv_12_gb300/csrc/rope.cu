@@ -42,10 +42,21 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) rope_kernel(const __grid_
   const int lane = threadIdx.x & 31;
   const int64_t n_ic = (p.inner + kVecPerWarp - 1) / kVecPerWarp;
   const int64_t wv = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-  if (wv >= p.rows * p.tokens * n_ic) return;
-  const int64_t ic = wv % n_ic;
-  const int64_t t = (wv / n_ic) % p.tokens;
-  const int64_t r = wv / (n_ic * p.tokens);
+  const int64_t n_wv = p.rows * p.tokens * n_ic;
+  if (wv >= n_wv) return;
+  int64_t ic, t, r;
+  if (n_wv < (1LL << 31)) {
+    // 32-bit division (a 64-bit one costs about a hundred instructions)
+    const uint32_t w = (uint32_t)wv, nic = (uint32_t)n_ic, tok = (uint32_t)p.tokens;
+    const uint32_t rt = w / nic;
+    ic = w - rt * nic;
+    r = rt / tok;
+    t = rt - (uint32_t)r * tok;
+  } else {
+    ic = wv % n_ic;
+    t = (wv / n_ic) % p.tokens;
+    r = wv / (n_ic * p.tokens);
+  }
   const int half = p.rotary_dims >> 1;
   const int64_t i0 = ic * kVecPerWarp;
   const int nv = (int)min((int64_t)kVecPerWarp, p.inner - i0);
