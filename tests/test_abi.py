@@ -249,3 +249,28 @@ def test_reconstruct_and_prefill_validation(lib):
                        (27, 1000, 1), (21, 96, 2), (22, 96, 1), (15, 0, 2), (26, 64 * MB + 8, 1), (1, 100, 1)]:
         bad = list(pf); bad[i] = v
         assert L.mla_prefill_attend(*bad) == want, (i, v)
+
+
+def test_row_plans_random_cases_match_the_oracle(lib):
+    # many random right-aligned caches: bookkeeping and the planned gather
+    # reproduce the oracle's rollback, filter and merge exactly
+    from oracle import mla_oracle as O
+    r = np.random.default_rng(82)
+    for trial in range(200):
+        B, width = int(r.integers(1, 5)), int(r.integers(0, 12))
+        appended = int(r.integers(0, width + 1))
+        offs = r.integers(appended, width + 1, B)
+        pad = width - offs
+        a = r.integers(-50, 50, (B, max(width, 1), 1)).astype(np.float64)[:, :width]
+        before = offs - appended
+        keep = r.integers(0, appended + 1, B)
+        shift, new_pad, new_off, new_width = lib.plan_rollback(pad, offs, before, keep, width)
+        (want,), w, off_o, pad_o = O.rollback_right_aligned([a], pad, offs, before, keep)
+        assert (new_width, list(new_off), list(new_pad)) == (w, list(off_o), list(pad_o))
+        if width:
+            assert np.array_equal(_apply_plan(a, new_width, shift.numpy()), want)
+            keep_rows = r.integers(0, B, int(r.integers(1, 4)))
+            shift, new_pad, new_off, new_width = lib.plan_filter(pad, offs, keep_rows, width)
+            (want,), w, off_o, pad_o = O.filter_right_aligned([a], pad, offs, keep_rows)
+            assert (new_width, list(new_off), list(new_pad)) == (w, list(off_o), list(pad_o))
+            assert np.array_equal(_apply_plan(a, new_width, shift.numpy(), src_row=keep_rows), want)
