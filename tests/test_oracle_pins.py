@@ -337,6 +337,33 @@ def test_gather_selected_is_indexing():
     assert np.array_equal(g[1, 2], np.r_[lat[1, 5], rp[1, 5]])
 
 
+def test_gather_selected_dense_rows_list_the_window_in_order():
+    # Count -1 (the page's null selection): the row's visible window, first key
+    # first, cut after k_max entries; slots past the window stay zero.  Written
+    # out by hand from the buffer indices (kv_start + t), not through the oracle.
+    r = rng(19)
+    lat = r.integers(-30000, 30000, size=(3, 12, 4)).astype(np.int16)
+    rp = r.integers(-30000, 30000, size=(3, 12, 2)).astype(np.int16)
+    row = lambda bb, t: np.r_[lat[bb, t], rp[bb, t]]
+    sel = np.zeros((3, 5), dtype=np.int64)
+    # row 0: window of 9 keys at buffer rows 2..10, k_max 5 -> rows 2, 3, 4, 5, 6
+    # row 1: window of 3 keys at buffer rows 7..9 -> rows 7, 8, 9, then zeros
+    # row 2: mixed with a listed row -- count 2 takes the listed positions
+    sel[2, :2] = [4, 0]
+    g = O.gather_selected(lat, rp, [2, 7, 1], [9, 3, 6], 1, sel, [-1, -1, 2], 5)
+    assert [np.array_equal(g[0, j], row(0, 2 + j)) for j in range(5)] == [True] * 5
+    assert [np.array_equal(g[1, j], row(1, 7 + j)) for j in range(3)] == [True] * 3
+    assert np.all(g[1, 3:] == 0)
+    assert np.array_equal(g[2, 0], row(2, 5)) and np.array_equal(g[2, 1], row(2, 1))
+    assert np.all(g[2, 2:] == 0)
+    # verify rows (s_q = 2): token 0 sees one key fewer than token 1, in order
+    g = O.gather_selected(lat, rp, [0], [4], 2, np.zeros((2, 6), np.int64), [-1, -1], 6)
+    assert [np.array_equal(g[0, j], row(0, j)) for j in range(3)] == [True] * 3
+    assert np.all(g[0, 3:] == 0)
+    assert [np.array_equal(g[1, j], row(0, j)) for j in range(4)] == [True] * 4
+    assert np.all(g[1, 4:] == 0)
+
+
 # ---------------------------------------------------------------- RMSNorm / append pins
 
 def test_rms_norm_closed_forms():
