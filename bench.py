@@ -5,16 +5,19 @@ One *step* is one pass of the whole hot path for one attention layer: RoPE of
 the new query's rope part, absorption of q_nope through W_UK, latent attention
 over the cache (split-K flash decode + combine) and the W_UV projection.
 Consecutive steps use the buffers (cache, weights, queries) of R distinct
-layers whose total size exceeds the 129 MB L2, so no step finds its inputs in
-L2 from the step before.
+layers, R chosen so that the bytes one step touches, times R, exceed twice the
+129 MB L2: no step finds its inputs in L2 from the step before.
 
-Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU
-oracle on the same workload instead (the reference arm).  ``--workload`` picks
-another of the five workloads (default: dense bf16, B=1, T=4096).
+The headline line is the batched ragged decode (B = 32 rows of U[1024, 32768]
+cached keys, 128 heads), the largest one-token decode workload; ``per_config``
+adds the other decode workloads (dense B = 1, sparse top-2048, multi-row
+verify dense and sparse), each timed the same way.  ``--impl reference`` times
+the float64 CPU oracle on the headline workload instead (the reference arm).
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -29,24 +32,26 @@ sys.path.insert(0, ROOT)
 METRIC = "MLA decode tokens/s and latent-cache HBM GB/s (% of GB300 roofline)"
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode +
 # combine launch pair of the current kernels, from an ncu capture of this
-# bench (cold caches between launches, so the split partials' round trip,
-# 4.2 MB at B=1, is counted as a DRAM re-read that a warm L2 serves).
-MEASURED_TRAFFIC = {"dense_bf16_b1_t4096_h128": 4952320 + 4226304}
+# bench's workload; absent when the kernels changed after the capture.
+MEASURED_TRAFFIC: dict = {}
 L2_BYTES = 129 * 2 ** 20
+WORKLOADS = ("tiny_f32", "dense_bf16", "ragged_bf16", "sparse_bf16", "verify_bf16", "verify_sparse_bf16")
+HEADLINE = "ragged_bf16"
+PER_CONFIG = ("dense_bf16", "ragged_bf16", "sparse_bf16", "verify_bf16", "verify_sparse_bf16")
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="dense_bf16",
-                    choices=["tiny_f32", "dense_bf16", "ragged_bf16", "sparse_bf16", "verify_bf16",
-                             "verify_sparse_bf16"])
+    ap.add_argument("--workload", default=HEADLINE, choices=WORKLOADS)
+    ap.add_argument("--no-per-config", action="store_true", help="time the headline workload only")
+    ap.add_argument("--no-side", action="store_true", help="skip the append / top-k / rollback / prefill objects")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def workload(name):
@@ -78,7 +83,7 @@ def algorithmic(inp, with_sel=True):
     if inp.sel is not None and with_sel:
         cnt = inp.sel_count.clamp(min=0)
         keys_rows = int(cnt.sum())                      # each (row, token) gathers its own rows
-        byts = keys_rows * row_bytes + int(cnt.numel()) * 0 + keys_rows * 4
+        byts = keys_rows * row_bytes + keys_rows * 4    # rows + their indices
         visits = keys_rows
     else:
         byts = int(inp.kv_len.sum()) * row_bytes       # one pass over each batch row's window
@@ -90,8 +95,36 @@ def algorithmic(inp, with_sel=True):
     return byts, flops
 
 
+def step_algorithmic(inp):
+    """(bytes, flops) of the whole step: the decode's cache bytes and flops, plus
+    W_UK and W_UV (read once each), the query in and the output out, and the
+    absorb and projection flops."""
+    w = inp.w
+    esize = 4 if w.dtype == "f32" else 2
+    byts, flops = algorithmic(inp)
+    weights = w.heads * (w.nope + w.v) * w.rank * esize   # all of kv_b_proj: W_UK and W_UV once each
+    q_in = w.n_q * w.heads * (w.nope + w.rope) * esize
+    out = w.n_q * w.heads * w.v * esize
+    flops += 2 * w.n_q * w.heads * w.rank * (w.nope + w.v)
+    return byts + weights + q_in + out, flops
+
+
+def roofline(byts, flops, seconds, hbm, tf_peak, src):
+    """The benchmark spec's roofline: the slower of bytes at the HBM rate and flops at the bf16 rate."""
+    ach_gbs = byts / seconds / 1e9
+    ach_tf = flops / seconds / 1e12
+    mem_bound = (byts / (hbm * 1e9)) >= (flops / (tf_peak * 1e12))
+    if mem_bound:
+        r = {"bound": "hbm", "achieved": ach_gbs, "peak": hbm, "unit": "GB/s", "frac": ach_gbs / hbm}
+    else:
+        r = {"bound": "tensor", "achieved": ach_tf, "peak": tf_peak, "unit": "TFLOP/s", "frac": ach_tf / tf_peak}
+    r.update({"peak_source": src, "algorithmic_bytes": byts, "algorithmic_flops": flops,
+              "seconds": seconds, "gbs": ach_gbs, "tflops": ach_tf})
+    return r
+
+
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 100 ms while running."""
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms while running."""
 
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -101,22 +134,35 @@ class ClockSampler:
         self.index = index
         self.samples = []
         self.proc = None
+        self.error = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
-        except OSError:
+        except OSError as e:
             self.proc = None
+            self.error = str(e)
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.samples.append([x.strip() for x in line.split(",")])
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 4 and parts[0].replace(".", "").isdigit():
+                self.samples.append((time.perf_counter(), parts))
+
+    def wait_samples(self, n, timeout=3.0, keep_busy=None):
+        """Blocks until ``n`` samples have arrived (running ``keep_busy`` meanwhile)."""
+        t0 = time.perf_counter()
+        while self.proc is not None and len(self.samples) < n and time.perf_counter() - t0 < timeout:
+            if keep_busy is not None:
+                keep_busy()
+            else:
+                time.sleep(0.01)
 
     def __exit__(self, *a):
         if self.proc:
@@ -126,17 +172,18 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
-        if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
-        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
-        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+    def summary(self, since=None):
+        rows = [p for t, p in self.samples if since is None or t >= since]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0,
+                    "error": self.error}
+        sm = [float(s[0]) for s in rows]
+        mx = [float(s[1]) for s in rows if s[1].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[k] for s in self.samples for k in range(4)
+        reasons = sorted({names[k] for s in rows for k in range(4)
                           if len(s) > 4 + k and s[4 + k].lower() == "active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(self.samples)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
 
 
 def max_over_ranks(x: float, device) -> float:
@@ -155,25 +202,95 @@ def dist_env():
         int(os.environ.get("LOCAL_RANK", 0))
 
 
-def time_oracle(inp, seconds, heads_per_row=None):
-    """Times the float64 oracle (rotations + reconstructed attention) on whole
-    query rows, or on ``heads_per_row`` heads of each row, until ~``seconds``
-    of CPU work.  Returns (tokens/s scaled to whole rows, units done, elapsed,
-    threads)."""
-    from tests import helpers as H
+# ---------------------------------------------------------------- the oracle on the host cores
+
+def one_row_inputs(inp, b):
+    """The inputs of batch row ``b`` alone (its window copied out, kv_start 0)."""
+    import torch
+    from mla_latent_kv_12_gb300.workloads import DecodeInputs
     w = inp.w
-    hs = None if heads_per_row is None else list(range(min(heads_per_row, w.heads)))
-    frac = 1.0 if hs is None else len(hs) / w.heads
+    bb = 0 if inp.packed_flat else b
+    s, n = int(inp.kv_start[b]), int(inp.kv_len[b])
+    w1 = dataclasses.replace(w, batch=1)
+    rows = slice(b * w.s_q, (b + 1) * w.s_q)
+    sel = inp.sel[rows].clone() if inp.sel is not None else None
+    cnt = inp.sel_count[rows].clone() if inp.sel is not None else None
+    return DecodeInputs(w1, inp.q_nope[b:b + 1].clone(), inp.q_rope_raw[b:b + 1].clone(),
+                        inp.latent[bb:bb + 1, s:s + n].clone(), inp.rope_raw[bb:bb + 1, s:s + n].clone(),
+                        inp.kv_b_proj, torch.zeros(1, dtype=torch.int32), torch.tensor([n], dtype=torch.int32),
+                        inp.q_offset[b:b + 1].clone(), False, sel, cnt)
+
+
+def _oracle_task(args):
+    """One task of the host-core oracle pool: the reconstructed-path oracle for
+    all query tokens of one batch row, on a subset of heads.  Returns seconds."""
+    inp1, heads = args
+    from tests import helpers as H
     t0 = time.perf_counter()
-    done = 0
-    while True:
-        H.oracle_reference_out_only(inp, rows=[done % w.n_q], heads=hs)
-        done += 1
+    H.oracle_reference_out_only(inp1, rows=list(range(inp1.w.s_q)), heads=heads)
+    return time.perf_counter() - t0
+
+
+class OraclePool:
+    """The float64 oracle as it stands, run on the host cores by a pool of
+    single-threaded processes (spawned, BLAS limited to one thread each), one
+    task per (batch row, group of heads)."""
+
+    def __init__(self, workers=None):
+        import multiprocessing as mp
+        self.workers = workers or (len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
+                                   else os.cpu_count())
+        saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+        for k in saved:
+            os.environ[k] = "1"
+        try:
+            self.pool = mp.get_context("spawn").Pool(self.workers)
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        self.pool.map(_oracle_task, [])            # workers up before any timing
+
+    def run(self, inp, rows, heads_per_task):
+        """Tokens/s equivalent of the oracle over ``rows`` batch rows, each cut
+        into tasks of ``heads_per_task`` heads.  Returns (tokens, seconds)."""
+        w = inp.w
+        groups = [list(range(h, min(h + heads_per_task, w.heads))) for h in range(0, w.heads, heads_per_task)]
+        tasks = [(one_row_inputs(inp, b), g) for b in rows for g in groups]
+        t0 = time.perf_counter()
+        self.pool.map(_oracle_task, tasks, chunksize=1)
         el = time.perf_counter() - t0
-        if el >= seconds or done >= 64:
-            break
-    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    return done * frac / el, done, el, threads
+        return len(rows) * w.s_q, el
+
+    def run_heads(self, inp, b, heads):
+        """One batch row on the listed heads, one head per task."""
+        inp1 = one_row_inputs(inp, b)
+        t0 = time.perf_counter()
+        self.pool.map(_oracle_task, [(inp1, [h]) for h in heads], chunksize=1)
+        return time.perf_counter() - t0
+
+    def close(self):
+        self.pool.terminate()
+        self.pool.join()
+
+
+def cpu_baseline(inp, seconds, pool):
+    """The oracle on whole batch rows (all heads) until about ``seconds`` have passed."""
+    w = inp.w
+    heads_per_task = max(1, w.heads // pool.workers)
+    done_tokens, el = 0, 0.0
+    b = 0
+    while el < seconds and b < w.batch:
+        t, e = pool.run(inp, [b], heads_per_task)
+        done_tokens += t
+        el += e
+        b += 1
+    return {"value": done_tokens / el, "unit": "tokens/s", "cores": pool.workers, "kind": "oracle",
+            "sample": f"{b} batch row(s) of {w.name} ({done_tokens} query tokens, all {w.heads} heads), "
+                      f"float64 reconstructed-path oracle, {pool.workers} single-threaded processes "
+                      f"(one per core, tasks of {heads_per_task} heads), {el:.1f} s"}
 
 
 def reference_arm(args):
@@ -183,69 +300,71 @@ def reference_arm(args):
     from mla_latent_kv_12_gb300 import workloads as W
     w = workload(args.workload)
     inp = W.make_inputs(w, layout=layout_of(w))
-    # Each step: one query row of the workload on a fixed subset of heads (the
-    # oracle's cost is linear in heads), so that K + W steps take minutes.
-    heads = 8 if w.heads >= 64 else None
-    rates = []
-    threads = 1
+    pool = OraclePool()
+    # Each step: all query tokens of one batch row on one head per worker
+    # (the oracle's cost is linear in heads), rows in turn.
+    heads = list(range(min(pool.workers, w.heads)))
+    times = []
     for k in range(args.warmup + args.steps):
-        v, done, el, threads = time_oracle(inp, 0.0, heads_per_row=heads)
+        el = pool.run_heads(inp, k % w.batch, heads)
         if k >= args.warmup:
-            rates.append(el / done)
-    sec_per_unit = statistics.mean(rates)
-    frac = 1.0 if heads is None else heads / w.heads
-    value = frac / sec_per_unit
-    sec_per_row = sec_per_unit / frac
+            times.append(el)
+    pool.close()
+    sec = statistics.mean(times)
+    tokens = w.s_q * len(heads) / w.heads          # query tokens' worth of work per step
+    value = tokens / sec
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": sec_per_row * 1e3, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "layers": 1, "l2": "cpu"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": f"per step one query row of {w.name} on {heads or w.heads} of "
-                                   f"{w.heads} heads (scaled to whole rows), float64 "
-                                   "reconstructed-path oracle (numpy BLAS)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": pool.workers, "kind": "oracle",
+                         "sample": f"per step all {w.s_q} query token(s) of one batch row of {w.name} on "
+                                   f"{len(heads)} of {w.heads} heads (one head per process, rows in turn); "
+                                   f"value counts the work done ({tokens:.4g} tokens per step), float64 "
+                                   "reconstructed-path oracle"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def ours(args):
-    import numpy as np
+# ---------------------------------------------------------------- the GPU arm
+
+def layers_for(inp, step_bytes):
+    """Distinct layers to rotate so that consecutive uses of one layer are
+    separated by more than twice the L2 of other layers' bytes (one layer when
+    a step alone touches that much)."""
+    if step_bytes >= 2 * L2_BYTES:
+        return 1
+    return min(16, -(-2 * L2_BYTES // max(step_bytes, 1)) + 1)
+
+
+def measure(w, steps, warmup, dev, world, peaks, e2e=False, clocks=None):
+    """Times the whole step and the decode launches of workload ``w`` on R
+    rotating layers with CUDA-graph replays.  Returns a dict."""
     import torch
-    import torch.distributed as dist
-
-    rank, world, local = dist_env()
-    if world > 1:
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-
     from mla_latent_kv_12_gb300 import mla
     from mla_latent_kv_12_gb300 import workloads as W
     from mla_latent_kv_12_gb300.pipeline import DecodeStep
 
-    w = workload(args.workload)
+    hbm, tf_burst, _, src = peaks
     inp = W.make_inputs(w, layout=layout_of(w))
-    one = DecodeStep(inp, dev)
-    layer_bytes = (one.latent.numel() + one.rope.numel() + one.kv_b_proj.numel()) * one.latent.element_size()
-    R = max(1, min(16, -(-2 * L2_BYTES // layer_bytes)))
-    steps = [one] + [DecodeStep(inp, dev) for _ in range(R - 1)]
-    stream = torch.cuda.current_stream()
-
-    # One CUDA graph per layer for the whole step, and one for its decode launches
-    # (planner + decode + combine) to time the dominant kernel without host gaps.
-    for s in steps:
+    byts, flops = algorithmic(inp)
+    sbytes, sflops = step_algorithmic(inp)
+    R = layers_for(inp, sbytes)
+    steps_l = [DecodeStep(inp, dev) for _ in range(R)]
+    one = steps_l[0]
+    for s in steps_l:
         s.run()
         if s.fused:      # the decode-only graphs read the absorbed query of the separate entry points
             s.rope_q()
             s.absorb()
     torch.cuda.synchronize()
-    g_step, g_att = [], []
     cap = torch.cuda.Stream()
+    g_step, g_att = [], []
     with torch.cuda.stream(cap):
-        for s in steps:
+        for s in steps_l:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=cap):
                 s.run()
@@ -256,56 +375,88 @@ def ours(args):
             g_att.append(g)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
-
-    for k in range(args.warmup):
+    for k in range(warmup):
         g_step[k % R].replay()
+    kk = [warmup]
+
+    def busy():
+        g_step[kk[0] % R].replay()
+        kk[0] += 1
+        torch.cuda.synchronize()
+    if clocks is not None:          # clocks sampled under this load, right before and during the timed region
+        clocks.wait_samples(len(clocks.samples) + 3, keep_busy=busy)
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    t_clk = time.perf_counter()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(steps):
+        g_step[k % R].replay()
+    stop.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    with ClockSampler(local) as clk:
-        torch.cuda.synchronize()
-        start.record(stream)
-        for k in range(args.steps):
-            g_step[k % R].replay()
-        stop.record(stream)
-        torch.cuda.synchronize()
-        # the decode launches alone, same layer rotation, bracketed one by one
-        for k in range(args.steps):
-            ev_dec[k][0].record(stream)
-            g_att[k % R].replay()
-            ev_dec[k][1].record(stream)
-        torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
     ms_total = max_over_ranks(start.elapsed_time(stop), dev)
-    ms_step = ms_total / args.steps
-    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_dec)
-    tokens = w.n_q * args.steps * world
-    value = tokens / (ms_total / 1e3)
+    clk = clocks.summary(since=t_clk - 0.2) if clocks is not None else None
+    # the decode launches alone (decode + combine, + planner), same layer rotation, one by one
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for k in range(steps):
+        ev[k][0].record(stream)
+        g_att[k % R].replay()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    ms_step = ms_total / steps
+    status = max(int(s.status.item()) for s in steps_l)
+    res = {
+        "workload": w.name, "batch": w.batch, "s_q": w.s_q, "heads": w.heads, "layers": R,
+        "tokens_per_s": w.n_q * world / (ms_step / 1e3), "ms_per_step": ms_step, "kernel_ms": dec_ms,
+        "cache_gbs": byts / (dec_ms / 1e3) / 1e9, "device_status": status,
+        "step_launches": one.launches_per_step(), "decode_launches": one.attend_launches(),
+        "roofline": roofline(byts, flops, dec_ms / 1e3, hbm, tf_burst, src),
+        "step_roofline": roofline(sbytes, sflops, ms_step / 1e3, hbm, tf_burst, src),
+        "kind": "tcgen05" if mla.decode_kernel_kind(w.heads, w.rank, w.rope, one.dtype, one.dtype) == 1
+        else "cuda-core",
+    }
+    res["roofline"]["traffic"] = MEASURED_TRAFFIC.get(w.name)
+    res["roofline"]["kernel"] = "mla_decode_attend (decode + combine)"
+    res["step_roofline"]["note"] = ("whole step: cache bytes + W_UK + W_UV + query in + output out, "
+                                    "absorb + attention + projection flops")
+    if clk is not None:
+        res["clocks"] = clk
+    if e2e:
+        res["e2e"] = measure_e2e(steps_l, inp, steps, cap, stream, world)
+    res["_inp"] = inp
+    res["_steps"] = steps_l
+    res["_cap"] = cap
+    return res
 
-    # end to end: pinned host query in, host result out, every step
-    e2e_steps = max(10, args.steps // 4)
+
+def measure_e2e(steps_l, inp, steps, cap, stream, world):
+    """The same step through the public API with the query copied in from pinned
+    host memory and the output copied back, every step (one CUDA graph per layer)."""
+    import torch
+    w = inp.w
+    R = len(steps_l)
+    one = steps_l[0]
     hq = [inp.q_nope.reshape(w.n_q, w.heads, w.nope).pin_memory(), inp.q_rope_raw.pin_memory()]
     hout = torch.empty(one.out.shape, dtype=one.out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in hq)
     d2h = hout.numel() * hout.element_size()
+
     def e2e_step(s):
         s.q_nope.copy_(hq[0], non_blocking=True)
         s.q_rope_raw.copy_(hq[1], non_blocking=True)
         s.run()
         hout.copy_(s.out, non_blocking=True)
     for k in range(3):
-        e2e_step(steps[k % R])
+        e2e_step(steps_l[k % R])
     torch.cuda.synchronize()
-    # one CUDA graph per layer holding the host->device copies, the step's
-    # launches and the device->host copy, as a serving loop would replay it
     g_e2e = []
     with torch.cuda.stream(cap):
-        for s in steps:
+        for s in steps_l:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=cap):
                 e2e_step(s)
@@ -314,109 +465,29 @@ def ours(args):
         g_e2e[k % R].replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(10, steps)
     e0.record(stream)
-    for k in range(e2e_steps):
+    for k in range(n):
         g_e2e[k % R].replay()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    e2e_value = w.n_q * world / (e2e_ms / 1e3)
+    ms = e0.elapsed_time(e1) / n
+    return {"value": w.n_q * world / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "timing": "CUDA graph per layer: host->device copies of the query, the step's launches, "
+                      "device->host copy of the output; replayed"}
 
-    # the cache append of the page's forward (RMSNorm + RoPE of one new token per
-    # batch row), timed alone over a scratch cache: one launch per call
-    ap_lat = torch.zeros(w.batch, 4, w.rank, dtype=one.dtype, device=dev)
-    ap_rope = torch.zeros(w.batch, 4, w.rope, dtype=one.dtype, device=dev)
-    ap_len = torch.zeros(w.batch, dtype=torch.int32, device=dev)
-    ap_in = inp.latent[:, :1].reshape(w.batch if inp.latent.shape[0] == w.batch else 1, 1, w.rank)
-    ap_in = ap_in.expand(w.batch, 1, w.rank).contiguous().to(dev)
-    ap_rin = torch.randn(w.batch, 1, w.rope, device=dev).to(one.dtype)
-    ap_w = torch.ones(w.rank, dtype=one.dtype, device=dev)
-    ap_per_graph, ap_reps = 20, 10
-    for _ in range(3):
-        mla.append_compressed(ap_in, ap_rin, ap_w, 1e-6, w.theta, ap_lat, ap_rope, None, ap_len)
-    torch.cuda.synchronize()
-    g_ap = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(cap):
-        with torch.cuda.graph(g_ap, stream=cap):
-            for _ in range(ap_per_graph):
-                mla.append_compressed(ap_in, ap_rin, ap_w, 1e-6, w.theta, ap_lat, ap_rope, None, ap_len)
-    g_ap.replay()
-    torch.cuda.synchronize()
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a0.record(stream)
-    for _ in range(ap_reps):
-        g_ap.replay()
-    a1.record(stream)
-    torch.cuda.synchronize()
-    append_us = a0.elapsed_time(a1) / (ap_per_graph * ap_reps) * 1e3
-    ap_bytes = w.batch * (w.rank + w.rope) * one.latent.element_size() * 2
 
-    # the DSA top-k selection (2048 positions per query row from f32 scores over
-    # the row's window), timed alone: 10 calls per CUDA graph, replayed
-    sel_k = 2048
-    sel_len = inp.kv_len.repeat_interleave(w.s_q).to(torch.int32).to(dev)
-    sel_scores = torch.randn(w.n_q, int(inp.kv_len.max()), device=dev)
-    sel_out = torch.empty(w.n_q, sel_k, dtype=torch.int32, device=dev)
-    sel_cnt = torch.empty(w.n_q, dtype=torch.int32, device=dev)
-    for _ in range(3):
-        mla.select_topk(sel_scores, sel_len, sel_k, sel_out, sel_cnt)
-    torch.cuda.synchronize()
-    g_sel = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(cap):
-        with torch.cuda.graph(g_sel, stream=cap):
-            for _ in range(10):
-                mla.select_topk(sel_scores, sel_len, sel_k, sel_out, sel_cnt)
-    g_sel.replay()
-    torch.cuda.synchronize()
-    a0.record(stream)
-    for _ in range(5):
-        g_sel.replay()
-    a1.record(stream)
-    torch.cuda.synchronize()
-    select_us = a0.elapsed_time(a1) / 50 * 1e3
-    sel_bytes = int(inp.kv_len.repeat_interleave(w.s_q).sum()) * 4
-
-    # the speculative-round rollback of a right-aligned cache (8 rows x 65536
-    # tokens of latent || rope, the verify batch's cache): one row-gather launch
-    # per state array, 2 x 0.6 GB moved per call, larger than L2
-    rb_B, rb_W = 8, 65536
-    rb_lat = torch.randn(rb_B, rb_W, w.rank, device=dev).to(one.dtype)
-    rb_rope = torch.randn(rb_B, rb_W, w.rope, device=dev).to(one.dtype)
-    rb_off = np.full(rb_B, rb_W - 7)
-    rb_off[::2] = rb_W                                     # half the rows fill the width
-    rb_keep = np.arange(rb_B) % 5                          # 0..4 of 4 appended tokens kept (4 = all)
-    rb_keep = np.minimum(rb_keep, 4)
-    rb_shift, _, _, rb_w = mla.plan_rollback(rb_W - rb_off, rb_off, rb_off - 4, rb_keep, rb_W)
-    rb_shift = rb_shift.to(dev)
-    rb_dst = [torch.empty(rb_B, rb_w, a.shape[2], dtype=a.dtype, device=dev) for a in (rb_lat, rb_rope)]
-
-    def rollback_call():
-        for a, d in zip((rb_lat, rb_rope), rb_dst):
-            mla.cache_shift_rows(a, d, shift=rb_shift)
-    for _ in range(3):
-        rollback_call()
-    torch.cuda.synchronize()
-    g_rb = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(cap):
-        with torch.cuda.graph(g_rb, stream=cap):
-            for _ in range(5):
-                rollback_call()
-    g_rb.replay()
-    torch.cuda.synchronize()
-    a0.record(stream)
-    for _ in range(4):
-        g_rb.replay()
-    a1.record(stream)
-    torch.cuda.synchronize()
-    rollback_us = a0.elapsed_time(a1) / 20 * 1e3
-    rb_bytes = 2 * rb_B * rb_w * (w.rank + w.rope) * rb_lat.element_size()
-    del rb_lat, rb_rope, rb_dst
-
-    # the reconstructed prefill of a 4096-token prompt (RoPE of the query rope
-    # part, per-head K/V materialisation, causal attention), three launches per
-    # step, each part also timed alone; CUDA graphs of 3 steps, replayed
+def side_objects(w, one, inp, dev, cap, peaks):
+    """The other kernels of the library, each timed alone with CUDA-graph replays."""
+    import numpy as np
+    import torch
+    from mla_latent_kv_12_gb300 import mla
+    from mla_latent_kv_12_gb300 import workloads as W
     from mla_latent_kv_12_gb300.pipeline import PrefillStep
-    pf = PrefillStep(W.make_inputs(W.PREFILL_BF16), dev)
+    hbm, tf_burst, _, _ = peaks
+    stream = torch.cuda.current_stream()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     def graph_us(fn, per_graph=3, reps=3):
         for _ in range(2):
@@ -436,6 +507,48 @@ def ours(args):
         torch.cuda.synchronize()
         return a0.elapsed_time(a1) / (per_graph * reps) * 1e3
 
+    # the cache append of the page's forward (RMSNorm + RoPE of one new token per batch row)
+    ap_lat = torch.zeros(w.batch, 4, w.rank, dtype=one.dtype, device=dev)
+    ap_rope = torch.zeros(w.batch, 4, w.rope, dtype=one.dtype, device=dev)
+    ap_len = torch.zeros(w.batch, dtype=torch.int32, device=dev)
+    ap_in = torch.randn(w.batch, 1, w.rank, device=dev).to(one.dtype)
+    ap_rin = torch.randn(w.batch, 1, w.rope, device=dev).to(one.dtype)
+    ap_w = torch.ones(w.rank, dtype=one.dtype, device=dev)
+    append_us = graph_us(lambda: mla.append_compressed(ap_in, ap_rin, ap_w, 1e-6, w.theta, ap_lat, ap_rope,
+                                                       None, ap_len), per_graph=20, reps=10)
+    ap_bytes = w.batch * (w.rank + w.rope) * one.latent.element_size() * 2
+
+    # the DSA top-k selection (2048 positions per query row from f32 scores over the row's window)
+    sel_k = 2048
+    sel_len = inp.kv_len.repeat_interleave(w.s_q).to(torch.int32).to(dev)
+    sel_scores = torch.randn(w.n_q, int(inp.kv_len.max()), device=dev)
+    sel_out = torch.empty(w.n_q, sel_k, dtype=torch.int32, device=dev)
+    sel_cnt = torch.empty(w.n_q, dtype=torch.int32, device=dev)
+    select_us = graph_us(lambda: mla.select_topk(sel_scores, sel_len, sel_k, sel_out, sel_cnt), per_graph=10,
+                         reps=5)
+    sel_bytes = int(inp.kv_len.repeat_interleave(w.s_q).sum()) * 4
+    del sel_scores
+
+    # the speculative-round rollback of a right-aligned cache (8 rows x 65536 tokens of latent || rope)
+    rb_B, rb_W = 8, 65536
+    rb_lat = torch.randn(rb_B, rb_W, w.rank, device=dev).to(one.dtype)
+    rb_rope = torch.randn(rb_B, rb_W, w.rope, device=dev).to(one.dtype)
+    rb_off = np.full(rb_B, rb_W - 7)
+    rb_off[::2] = rb_W                                     # half the rows fill the width
+    rb_keep = np.minimum(np.arange(rb_B) % 5, 4)           # 0..4 of 4 appended tokens kept
+    rb_shift, _, _, rb_w = mla.plan_rollback(rb_W - rb_off, rb_off, rb_off - 4, rb_keep, rb_W)
+    rb_shift = rb_shift.to(dev)
+    rb_dst = [torch.empty(rb_B, rb_w, a.shape[2], dtype=a.dtype, device=dev) for a in (rb_lat, rb_rope)]
+
+    def rollback_call():
+        for a, d in zip((rb_lat, rb_rope), rb_dst):
+            mla.cache_shift_rows(a, d, shift=rb_shift)
+    rollback_us = graph_us(rollback_call, per_graph=5, reps=4)
+    rb_bytes = 2 * rb_B * rb_w * (w.rank + w.rope) * rb_lat.element_size()
+    del rb_lat, rb_rope, rb_dst
+
+    # the reconstructed prefill of a 4096-token prompt (query RoPE, K/V materialisation, causal attention)
+    pf = PrefillStep(W.make_inputs(W.PREFILL_BF16), dev)
     pf_step_us = graph_us(pf.run)
     pf_att_us = graph_us(pf.attend)
     pf_rec_us = graph_us(pf.reconstruct)
@@ -446,51 +559,12 @@ def ours(args):
     pf_rec_flops = 2 * pf.latent.shape[0] * pf.latent.shape[1] * pfw.rank * pfw.heads * (pfw.nope + pfw.v)
     pf_status = int(pf.status.item())
     del pf
-
-    hbm, tf_burst, tf_sus, src = load_peaks()
-    byts, flops = algorithmic(inp)
-    ach_gbs = byts / (dec_ms / 1e3) / 1e9
-    ach_tf = flops / (dec_ms / 1e3) / 1e12
-    mem_bound = (byts / hbm) >= (flops / 1e3 / tf_burst)
-    roof = ({"bound": "hbm", "achieved": ach_gbs, "peak": hbm, "unit": "GB/s", "frac": ach_gbs / hbm}
-            if mem_bound else
-            {"bound": "tensor", "achieved": ach_tf, "peak": tf_burst, "unit": "TFLOP/s",
-             "frac": ach_tf / tf_burst})
-    roof.update({"traffic": MEASURED_TRAFFIC.get(w.name), "kernel": "mla_decode_attend (decode + combine)",
-                 "peak_source": src, "algorithmic_bytes": byts, "algorithmic_flops": flops,
-                 "kernel_ms": dec_ms, "tensor_tflops": ach_tf, "cache_gbs": ach_gbs})
-
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        v, done, el, threads = time_oracle(inp, args.cpu_seconds)
-        cpu = {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": f"{done} query rows (all heads) of {w.name}, float64 reconstructed-path "
-                         f"oracle, {el:.1f} s"}
-    kind = mla.decode_kernel_kind(w.heads, w.rank, w.rope, one.dtype, one.dtype)
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "s_q": w.s_q, "heads": w.heads,
-                   "rank": w.rank, "rope": w.rope, "layers": 1,
-                   "l2": f"rotating {R} layers' buffers ({R * layer_bytes / 2**20:.0f} MiB > L2)",
-                   "decode_kernel": "tcgen05" if kind == 1 else "cuda-core",
-                   "parallelism": f"replicas{world}"},
-        "clocks": clk.summary(),
-        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "timing": "CUDA graph per layer: host->device copies of the query, the step's launches, "
-                          "device->host copy of the output; replayed"},
-        "gpu_launches": one.launches_per_step() * args.steps,
-        "timing": "CUDA graph per layer step, replayed; decode kernel timed on its own graph replays",
-        "roofline": roof,
-        "cpu_baseline": cpu,
-        "cache_gbs": ach_gbs,
+    return {
         "append": {"us_per_call": append_us, "tokens_per_call": w.batch, "bytes_per_call": ap_bytes,
                    "note": "mla_append_compressed (RMSNorm + RoPE of one new token per batch row), "
                            "20 calls per CUDA graph, replayed"},
         "select_topk": {"us_per_call": select_us, "rows": w.n_q, "top_k": sel_k, "score_bytes": sel_bytes,
+                        "gbs": sel_bytes / (select_us * 1e-6) / 1e9,
                         "note": "mla_select_topk over f32 scores of each query row's window, "
                                 "10 calls per CUDA graph, replayed"},
         "prefill": {"workload": W.PREFILL_BF16.name, "us_per_step": pf_step_us,
@@ -510,6 +584,66 @@ def ours(args):
                              "8 x 65536 tokens of latent || rope, read + write bytes, 5 calls per CUDA "
                              "graph, replayed"},
     }
+
+
+def public(res):
+    return {k: v for k, v in res.items() if not k.startswith("_")}
+
+
+def ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    # the host-core oracle pool is spawned before the first CUDA call
+    pool = OraclePool() if (rank == 0 and not args.no_cpu_baseline) else None
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+
+    w = workload(args.workload)
+    with ClockSampler(local) as clk:
+        head = measure(w, args.steps, args.warmup, dev, world, peaks, e2e=True, clocks=clk)
+    inp, one, cap = head["_inp"], head["_steps"][0], head["_cap"]
+    side = {} if args.no_side else side_objects(w, one, inp, dev, cap, peaks)
+    del head["_steps"]
+    per_config = {}
+    if not args.no_per_config:
+        for name in PER_CONFIG:
+            if name == args.workload:
+                per_config[workload(name).name] = {k: v for k, v in public(head).items() if k not in ("e2e", "clocks")}
+                continue
+            r = measure(workload(name), max(args.steps, 20), max(args.warmup, 3), dev, world, peaks)
+            per_config[r["workload"]] = public(r)
+            del r
+            torch.cuda.empty_cache()
+    cpu = None
+    if pool is not None:
+        cpu = cpu_baseline(inp, args.cpu_seconds, pool)
+        pool.close()
+    roof = dict(head["roofline"])
+    line = {
+        "metric": METRIC, "value": head["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "s_q": w.s_q, "heads": w.heads,
+                   "rank": w.rank, "rope": w.rope, "cached_keys": int(inp.kv_len.sum()), "layers": 1,
+                   "l2": f"rotating {head['layers']} layers' buffers (inputs of one step x layers > 2 x L2)",
+                   "decode_kernel": head["kind"], "parallelism": f"replicas{world}"},
+        "clocks": head.get("clocks"),
+        "e2e": head["e2e"],
+        "gpu_launches": head["step_launches"] * args.steps,
+        "timing": "CUDA graph per layer step, replayed; decode kernel timed on its own graph replays",
+        "roofline": roof,
+        "step_roofline": head["step_roofline"],
+        "cpu_baseline": cpu,
+        "cache_gbs": head["cache_gbs"],
+        "per_config": per_config,
+    }
+    line.update(side)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -72,6 +72,12 @@ typedef enum mla_dtype { MLA_DTYPE_F32 = 0, MLA_DTYPE_BF16 = 1 } mla_dtype;
 #define MLA_DEVICE_TIMEOUT (1 << 5)             /* a bounded device wait gave up    */
 #define MLA_DEVICE_LAYOUT (1 << 6)              /* shared memory not laid out as the
                                                    kernel expects; nothing computed */
+#define MLA_DEVICE_SCORE_RANGE (1 << 7)         /* a bf16 decode score half exceeded
+                                                   MLA_FP16_SCORE_LIMIT (see
+                                                   mla_decode_attend)               */
+/* Largest |half score| (unscaled q . k over one CTA's 288 features) that the
+ * bf16 decode's fp16 score exchange carries within the bf16 tolerance. */
+#define MLA_FP16_SCORE_LIMIT 256.0f
 
 /* Static, never NULL. */
 const char* mla_status_string(int status);
@@ -79,6 +85,12 @@ const char* mla_status_string(int status);
 const char* mla_last_error_detail(void);
 /* ABI version, (major << 16) | minor. */
 int mla_version(void);
+
+/* The page's softmax scale, 1/sqrt(qk_nope + qk_rope) (MLA page,
+ * attendReconstructed and attendAbsorbed: scores divided by the square root of
+ * qkHeadDim = qk_nope_head_dim + qk_rope_head_dim), rounded once to f32; pass
+ * it as `softmax_scale`.  0 for negative dims or a zero sum. */
+float mla_default_softmax_scale(int32_t nope, int32_t rope_dim);
 
 /*
  * Partial interleaved RoPE (MLA page, partialInterleavedRopeMlx).
@@ -116,10 +128,13 @@ int mla_rope_partial_interleaved(const void* in, void* out, int dtype, int64_t r
  * Only columns [0, rank) of each q_out head row are written, so q_out may be
  * the packed [n_q, H, rank+rope] query that mla_decode_attend reads.
  * fp32 accumulation; all three tensors have `dtype`.
- * bf16 with nope = 128, rank = 512 and 1..4 query rows is a matrix-vector
- * product bound by the weight read and runs on the CUDA cores (one CTA per
- * head); bf16 with 5..256 rows and 16-byte aligned pointers and strides runs
- * on the tensor cores (tcgen05); everything else on the CUDA cores.
+ * bf16 is served for heads 64 or 128, nope = 128 and rank = 512 (other bf16
+ * shapes: MLA_ERR_UNSUPPORTED), with q_nope and kv_b_proj 16-byte aligned
+ * and q_nope strides multiples of 16 bytes (else MLA_ERR_INVALID_ARGUMENT),
+ * at most 2^20 rows: 1..4 query rows are a matrix-vector product bound by the
+ * weight read and run on the CUDA cores (one CTA per head), 5 rows and more
+ * on the tensor cores (tcgen05, blocks of 256 rows).  f32 (any shape) runs
+ * on the CUDA cores.
  */
 int mla_absorb_q(const void* q_nope, int64_t q_nope_row_stride, int64_t q_nope_head_stride,
                  const void* kv_b_proj, void* q_out, int64_t q_out_row_stride,
@@ -154,9 +169,18 @@ int mla_absorb_q(const void* q_nope, int64_t q_nope_row_stride, int64_t q_nope_h
  * q, latent and rope have `dtype`.  workspace must hold
  * mla_decode_workspace_size(...) bytes (256-byte aligned) and may be NULL
  * when that size is 0.
- * bf16 with heads = 128, rank = 512, rope_dim = 64 runs the tensor-core
- * flash-decode kernel (tcgen05 + TMA, split-K over SM pairs); other shapes
- * and f32 run a CUDA-core kernel.  mla_decode_kernel_kind tells which.
+ * bf16 with heads 64 or 128, rank = 512, rope_dim = 64 runs the tensor-core
+ * flash-decode kernel (tcgen05 + TMA, split-K over SM pairs; 64 heads are
+ * padded to the MMA's 128 rows inside the kernel); it needs q, latent, rope
+ * and ctx_out 16-byte aligned, strides that are multiples of 16 bytes, equal
+ * zero-ness of the two batch strides and at most 2^20 query rows (else
+ * MLA_ERR_INVALID_ARGUMENT).  Other bf16 shapes return MLA_ERR_UNSUPPORTED
+ * and launch nothing.  f32 (any shape) runs a CUDA-core kernel.
+ * Score range: each SM pair exchanges its two halves of a score (the
+ * unscaled q . k over 288 of the 576 features) as fp16, so each half is
+ * clamped to +-65504 and carries a rounding error of 2^-11 of its size; a
+ * half whose magnitude exceeds MLA_FP16_SCORE_LIMIT sets
+ * MLA_DEVICE_SCORE_RANGE (the result is still written, with that error).
  */
 int mla_decode_attend(const void* q, int64_t q_row_stride, int64_t q_head_stride,
                       const void* latent, int64_t latent_row_stride, int64_t latent_batch_stride,
@@ -214,7 +238,7 @@ size_t mla_decode_workspace_size(int32_t batch, int32_t s_q, int32_t heads, int3
                                  int dtype);
 
 /* 1 if mla_decode_attend runs the tensor-core kernel for these sizes, 0 if the
- * CUDA-core kernel, -1 if the request is invalid. */
+ * CUDA-core kernel (f32), -1 if the request is invalid or not served. */
 int mla_decode_kernel_kind(int32_t heads, int32_t rank, int32_t rope_dim, int dtype, int out_dtype);
 
 /*
@@ -225,8 +249,11 @@ int mla_decode_kernel_kind(int32_t heads, int32_t rank, int32_t rope_dim, int dt
  * W_UV_h = rows [h*(nope+v_dim)+nope, (h+1)*(nope+v_dim)) of kv_b_proj.
  * ctx[n, h, c] sits at ctx + n*ctx_row_stride + h*ctx_head_stride + c.  The
  * output stops before o_proj.  fp32 accumulation.  ctx and kv_b_proj have
- * `dtype`; out has out_dtype.  bf16 inputs with rank = 512, v_dim = 128,
- * n_q <= 64 and 16-byte aligned pointers/strides run on the tensor cores.
+ * `dtype`; out has out_dtype.  bf16 is served for heads 64 or 128, rank =
+ * 512 and v_dim = 128 (other bf16 shapes: MLA_ERR_UNSUPPORTED) on the tensor
+ * cores (tcgen05, blocks of 64 query rows, at most 2^20 rows), with ctx and
+ * kv_b_proj 16-byte aligned and ctx strides multiples of 16 bytes (else
+ * MLA_ERR_INVALID_ARGUMENT).  f32 (any shape) runs on the CUDA cores.
  */
 int mla_project_v(const void* ctx, int64_t ctx_row_stride, int64_t ctx_head_stride,
                   const void* kv_b_proj, int dtype, void* out, int64_t out_row_stride,

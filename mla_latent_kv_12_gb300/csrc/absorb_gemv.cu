@@ -98,10 +98,9 @@ __global__ void __launch_bounds__(kGemvThreads) absorb_gemv_kernel(const __grid_
 template <int NQ>
 cudaError_t launch_nq(const GemvArgs& g, cudaStream_t stream) {
   const size_t smem = (size_t)8 * NQ * kGemvRank * sizeof(float);
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(absorb_gemv_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    attr = true;
+  {
+    const cudaError_t ea = set_max_dynamic_smem(absorb_gemv_kernel<NQ>, (int)smem);
+    if (ea != cudaSuccess) return ea;
   }
   return launch_pdl(absorb_gemv_kernel<NQ>, dim3(g.p.heads), dim3(kGemvThreads), smem, stream, g);
 }

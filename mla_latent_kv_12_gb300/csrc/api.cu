@@ -65,9 +65,11 @@ int device_sm_count() {
   return n;
 }
 
-// Tensor-core path availability for the decode step.
+// The bf16 shapes the tensor-core kernels serve (the GLM / DeepSeek MLA
+// shape with 64 or 128 heads).  Other bf16 shapes are refused.
+static bool served_heads(int32_t heads) { return heads == 64 || heads == 128; }
 static bool tc_decode_shape(int32_t heads, int32_t rank, int32_t rope_dim, int dtype) {
-  return dtype == MLA_DTYPE_BF16 && heads == 128 && rank == 512 && rope_dim == 64;
+  return dtype == MLA_DTYPE_BF16 && served_heads(heads) && rank == 512 && rope_dim == 64;
 }
 
 }  // namespace mla
@@ -89,6 +91,11 @@ const char* mla_status_string(int status) {
 }
 
 const char* mla_last_error_detail(void) { return g_detail; }
+
+float mla_default_softmax_scale(int32_t nope, int32_t rope_dim) {
+  if (nope < 0 || rope_dim < 0 || nope + rope_dim <= 0) return 0.f;
+  return (float)(1.0 / sqrt((double)nope + (double)rope_dim));
+}
 
 int mla_version(void) { return (1 << 16) | 0; }
 
@@ -143,20 +150,26 @@ int mla_absorb_q(const void* q_nope, int64_t q_nope_row_stride, int64_t q_nope_h
             "absorb: strides too small for the head widths");
   AbsorbParams p{q_nope, q_nope_row_stride, q_nope_head_stride, kv_b_proj, q_out,
                  q_out_row_stride, q_out_head_stride, n_q, heads, nope, v_dim, rank};
-  const bool tc = dtype == MLA_DTYPE_BF16 && nope == 128 && rank % 128 == 0 && rank <= 4096 &&
-                  n_q <= 256 && aligned16(q_nope) && aligned16(kv_b_proj) &&
-                  q_nope_head_stride % 8 == 0 && q_nope_row_stride % 8 == 0;
+  if (dtype == MLA_DTYPE_F32)
+    return cuda_status(launch_simt_absorb(p, dtype, (cudaStream_t)stream), "absorb launch");
+  if (!(served_heads(heads) && nope == 128 && rank == 512))
+    return fail(MLA_ERR_UNSUPPORTED, "absorb: bf16 is served for heads 64 or 128, nope 128, rank 512 "
+                                     "(got heads %d, nope %d, rank %d)", heads, nope, rank);
+  MLA_CHECK(n_q <= (1 << 20), "absorb: at most 2^20 query rows");
+  MLA_CHECK(aligned16(q_nope) && aligned16(kv_b_proj) && q_nope_head_stride % 8 == 0 &&
+                q_nope_row_stride % 8 == 0,
+            "absorb: q_nope and kv_b_proj must be 16-byte aligned, q_nope strides multiples of 16 bytes");
   // Up to four rows the product is a matrix-vector product bound by the
   // weight read: CUDA cores stream it (no MMA tile to fill).
-  if (dtype == MLA_DTYPE_BF16 && gemv_absorb_serves(p))
+  if (gemv_absorb_serves(p))
     return cuda_status(launch_gemv_absorb(p, (cudaStream_t)stream), "absorb (matrix-vector) launch");
-  if (tc) return cuda_status(launch_tc_absorb(p, (cudaStream_t)stream), "absorb (tensor core) launch");
-  return cuda_status(launch_simt_absorb(p, dtype, (cudaStream_t)stream), "absorb launch");
+  return cuda_status(launch_tc_absorb(p, (cudaStream_t)stream), "absorb (tensor core) launch");
 }
 
 int mla_decode_kernel_kind(int32_t heads, int32_t rank, int32_t rope_dim, int dtype, int out_dtype) {
   if (heads <= 0 || rank <= 0 || rope_dim < 0 || !valid_dtype(dtype) || !valid_dtype(out_dtype)) return -1;
-  return tc_decode_shape(heads, rank, rope_dim, dtype) ? 1 : 0;
+  if (dtype == MLA_DTYPE_F32) return 0;
+  return tc_decode_shape(heads, rank, rope_dim, dtype) ? 1 : -1;
 }
 
 static int decode_geometry(DecodeGeometry& g, const void* q, int64_t q_row_stride,
@@ -225,6 +238,12 @@ size_t mla_decode_workspace_size(int32_t batch, int32_t s_q, int32_t heads, int3
   if (batch <= 0 || s_q <= 0 || heads <= 0 || rank <= 0 || rope_dim < 0 || t_max <= 0 ||
       !valid_dtype(dtype) || (selected && k_max <= 0))
     return 0;
+  const int64_t n_q = (int64_t)batch * s_q;   // 64-bit: no overflow before the limits below
+  if (dtype == MLA_DTYPE_BF16) {
+    if (!tc_decode_shape(heads, rank, rope_dim, dtype) || n_q > (1 << 20)) return 0;
+    return (tc_decode_workspace((int32_t)n_q) + 255) & ~(size_t)255;
+  }
+  if (n_q > (1 << 24)) return 0;
   DecodeGeometry g;
   memset(&g, 0, sizeof(g));
   g.batch = batch;
@@ -235,9 +254,7 @@ size_t mla_decode_workspace_size(int32_t batch, int32_t s_q, int32_t heads, int3
   g.t_max = t_max;
   g.k_max = selected ? k_max : 0;
   g.sel = selected ? reinterpret_cast<const int32_t*>(16) : nullptr;
-  size_t need = tc_decode_shape(heads, rank, rope_dim, dtype)
-                    ? tc_decode_workspace(batch * s_q, heads, rank)
-                    : simt_decode_workspace(g, nullptr);
+  const size_t need = simt_decode_workspace(g, nullptr);
   return (need + 255) & ~(size_t)255;
 }
 
@@ -259,6 +276,9 @@ int mla_decode_attend(const void* q, int64_t q_row_stride, int64_t q_head_stride
                            ctx_row_stride, ctx_head_stride, lse_out, device_status, true);
   if (st != MLA_OK) return st;
   MLA_CHECK(valid_dtype(out_dtype), "decode: bad out_dtype %d", out_dtype);
+  if (dtype == MLA_DTYPE_BF16 && !tc_decode_shape(heads, rank, rope_dim, dtype))
+    return fail(MLA_ERR_UNSUPPORTED, "decode: bf16 is served for heads 64 or 128, rank 512, rope_dim 64 "
+                                     "(got heads %d, rank %d, rope_dim %d)", heads, rank, rope_dim);
   const size_t need = mla_decode_workspace_size(batch, s_q, heads, rank, rope_dim, t_max, k_max,
                                                 selected_positions != nullptr, dtype);
   MLA_CHECK(workspace_bytes >= need && (need == 0 || workspace),
@@ -286,11 +306,15 @@ int mla_decode_attend(const void* q, int64_t q_row_stride, int64_t q_head_stride
                      "decode launch");
 }
 
-static size_t step_q_bytes(int32_t n_q) { return ((size_t)n_q * 128 * 576 * 2 + 255) & ~(size_t)255; }
-static size_t step_ctx_bytes(int32_t n_q) { return ((size_t)n_q * 128 * 512 * 2 + 255) & ~(size_t)255; }
+static size_t step_q_bytes(int32_t n_q, int32_t heads) {
+  return ((size_t)n_q * heads * 576 * 2 + 255) & ~(size_t)255;
+}
+static size_t step_ctx_bytes(int32_t n_q, int32_t heads) {
+  return ((size_t)n_q * heads * 512 * 2 + 255) & ~(size_t)255;
+}
 static bool step_shape(int dtype, int32_t heads, int32_t nope, int32_t v_dim, int32_t rank, int32_t rope_dim,
                        int64_t n_q) {
-  return dtype == MLA_DTYPE_BF16 && heads == 128 && nope == 128 && v_dim == 128 && rank == 512 &&
+  return dtype == MLA_DTYPE_BF16 && served_heads(heads) && nope == 128 && v_dim == 128 && rank == 512 &&
          rope_dim == 64 && n_q > 0 && n_q <= 64;
 }
 
@@ -301,8 +325,7 @@ size_t mla_decode_step_workspace_size(int32_t batch, int32_t s_q, int32_t heads,
       !step_shape(dtype, heads, nope, v_dim, rank, rope_dim, (int64_t)batch * s_q))
     return 0;
   const int32_t n_q = batch * s_q;
-  return step_q_bytes(n_q) + step_ctx_bytes(n_q) +
-         ((tc_decode_workspace(n_q, heads, rank) + 255) & ~(size_t)255);
+  return step_q_bytes(n_q, heads) + step_ctx_bytes(n_q, heads) + ((tc_decode_workspace(n_q) + 255) & ~(size_t)255);
 }
 
 int mla_decode_step(const void* q_nope, int64_t q_nope_row_stride, int64_t q_nope_head_stride,
@@ -326,8 +349,8 @@ int mla_decode_step(const void* q_nope, int64_t q_nope_row_stride, int64_t q_nop
   const int64_t n_q = (int64_t)batch * s_q;
   if (!step_shape(dtype, heads, nope, v_dim, rank, rope_dim, n_q))
     return fail(MLA_ERR_UNSUPPORTED,
-                "decode_step: the fused step serves bf16, heads 128, nope 128, v 128, rank 512, rope 64 and at "
-                "most 64 query rows; compose the four entry points for other requests");
+                "decode_step: the fused step serves bf16, heads 64 or 128, nope 128, v 128, rank 512, rope 64 "
+                "and at most 64 query rows; compose the four entry points for other requests");
   MLA_CHECK(aligned16(q_nope) && aligned16(q_rope) && aligned16(kv_b_proj) && aligned16(latent) &&
                 aligned16(rope),
             "decode_step: q_nope, q_rope, kv_b_proj, latent and rope must be 16-byte aligned");
@@ -351,8 +374,8 @@ int mla_decode_step(const void* q_nope, int64_t q_nope_row_stride, int64_t q_nop
             "decode_step: workspace must be 256-byte aligned");
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   void* qbuf = ws;
-  void* ctxbuf = ws + step_q_bytes((int32_t)n_q);
-  uint8_t* dws = ws + step_q_bytes((int32_t)n_q) + step_ctx_bytes((int32_t)n_q);
+  void* ctxbuf = ws + step_q_bytes((int32_t)n_q, heads);
+  uint8_t* dws = ws + step_q_bytes((int32_t)n_q, heads) + step_ctx_bytes((int32_t)n_q, heads);
   const size_t dws_bytes = workspace_bytes - (size_t)(dws - ws);
   const int64_t D = rank + rope_dim;
   DecodeGeometry g;
@@ -472,11 +495,15 @@ int mla_project_v(const void* ctx, int64_t ctx_row_stride, int64_t ctx_head_stri
             "project_v: strides too small");
   ProjectParams p{ctx, ctx_row_stride, ctx_head_stride, kv_b_proj, out, out_row_stride,
                   n_q, heads, nope, v_dim, rank};
-  const bool tc = dtype == MLA_DTYPE_BF16 && rank == 512 && v_dim == 128 && n_q <= 64 &&
-                  aligned16(ctx) && aligned16(kv_b_proj) && ctx_head_stride % 8 == 0 &&
-                  ctx_row_stride % 8 == 0;
-  if (tc) return cuda_status(launch_tc_project(p, out_dtype, (cudaStream_t)stream), "project_v (tensor core) launch");
-  return cuda_status(launch_simt_project(p, dtype, out_dtype, (cudaStream_t)stream), "project_v launch");
+  if (dtype == MLA_DTYPE_F32)
+    return cuda_status(launch_simt_project(p, dtype, out_dtype, (cudaStream_t)stream), "project_v launch");
+  if (!(served_heads(heads) && rank == 512 && v_dim == 128))
+    return fail(MLA_ERR_UNSUPPORTED, "project_v: bf16 is served for heads 64 or 128, rank 512, v_dim 128 "
+                                     "(got heads %d, rank %d, v_dim %d)", heads, rank, v_dim);
+  MLA_CHECK(n_q <= (1 << 20), "project_v: at most 2^20 query rows");
+  MLA_CHECK(aligned16(ctx) && aligned16(kv_b_proj) && ctx_head_stride % 8 == 0 && ctx_row_stride % 8 == 0,
+            "project_v: ctx and kv_b_proj must be 16-byte aligned, ctx strides multiples of 16 bytes");
+  return cuda_status(launch_tc_project(p, out_dtype, (cudaStream_t)stream), "project_v (tensor core) launch");
 }
 
 int mla_gather_selected(const void* latent, int64_t latent_row_stride, int64_t latent_batch_stride,

@@ -48,12 +48,12 @@ struct DecodeGeometry {
   int32_t* device_status;
 };
 
-// CUDA-core decode (any shape, f32 or bf16 inputs).
+// CUDA-core decode of the f32 path (any shape; f32 q and cache).
 size_t simt_decode_workspace(const DecodeGeometry& g, int* splits_out);
 cudaError_t launch_simt_decode(const DecodeGeometry& g, int dtype, int out_dtype, void* workspace,
                                size_t workspace_bytes, cudaStream_t stream);
 
-// Tensor-core decode (bf16, heads 128, rank 512, rope 64).  With a tail, the
+// Tensor-core decode (bf16, heads 64 or 128, rank 512, rope 64).  With a tail, the
 // split combine is fused with the W_UV projection (bf16 context in
 // g.ctx_out, n_q <= 64, v_dim 128) and `tail->out` receives [n_q, H*v].
 struct DecodeTail {
@@ -63,7 +63,7 @@ struct DecodeTail {
   int out_dtype;
   int32_t heads, nope, v_dim, rank;
 };
-size_t tc_decode_workspace(int32_t n_q, int32_t heads, int32_t rank);
+size_t tc_decode_workspace(int32_t n_q);
 cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* workspace,
                              size_t workspace_bytes, cudaStream_t stream, const DecodeTail* tail = nullptr);
 

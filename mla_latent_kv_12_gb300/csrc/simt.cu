@@ -1,8 +1,9 @@
-// CUDA-core kernels: the general-shape decode (any heads / rank / rope, f32 or
-// bf16 storage), its split combine, query absorption, value projection and
-// the selected-position gather.  f32 arithmetic throughout; these serve the
-// f32 path (where TF32 tensor cores would miss a 1e-4 relative bound) and
-// shapes outside the tensor-core kernels.
+// CUDA-core kernels of the f32 path: the general-shape decode (any heads /
+// rank / rope over an f32 cache), its split combine, query absorption and value
+// projection, plus the selected-position gather (f32 or bf16 rows, a bit-exact
+// copy).  f32 arithmetic throughout: TF32 tensor cores would miss the f32
+// path's 1e-4 relative bound.  bf16 caches are served by the tensor-core
+// kernels only (other bf16 shapes are refused by the host API).
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -348,11 +349,8 @@ cudaError_t launch_simt_decode(const DecodeGeometry& g, int dtype, int out_dtype
 #define MLA_SIMT_DECODE(T, TO)                                                       \
   simt_decode_kernel<T, TO><<<grid, kDecodeWarps * 32, 0, stream>>>(g, ws, splits); \
   if (splits > 1) simt_combine_kernel<TO><<<dim3(g.heads, n_q), 128, 0, stream>>>(g, ws, splits);
-  if (dtype == MLA_DTYPE_F32) {
-    if (out_dtype == MLA_DTYPE_F32) { MLA_SIMT_DECODE(float, float) } else { MLA_SIMT_DECODE(float, __nv_bfloat16) }
-  } else {
-    if (out_dtype == MLA_DTYPE_F32) { MLA_SIMT_DECODE(__nv_bfloat16, float) } else { MLA_SIMT_DECODE(__nv_bfloat16, __nv_bfloat16) }
-  }
+  if (dtype != MLA_DTYPE_F32) return cudaErrorInvalidValue;
+  if (out_dtype == MLA_DTYPE_F32) { MLA_SIMT_DECODE(float, float) } else { MLA_SIMT_DECODE(float, __nv_bfloat16) }
 #undef MLA_SIMT_DECODE
   return cudaGetLastError();
 }
@@ -360,27 +358,19 @@ cudaError_t launch_simt_decode(const DecodeGeometry& g, int dtype, int out_dtype
 cudaError_t launch_simt_absorb(const AbsorbParams& p, int dtype, cudaStream_t stream) {
   dim3 grid((p.rank + 127) / 128, p.heads, (p.n_q + 31) / 32);
   const size_t smem = 32 * (size_t)p.nope * sizeof(float);
-  if (dtype == MLA_DTYPE_F32)
-    simt_absorb_kernel<float><<<grid, 128, smem, stream>>>(p);
-  else
-    simt_absorb_kernel<__nv_bfloat16><<<grid, 128, smem, stream>>>(p);
+  if (dtype != MLA_DTYPE_F32) return cudaErrorInvalidValue;
+  simt_absorb_kernel<float><<<grid, 128, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_simt_project(const ProjectParams& p, int dtype, int out_dtype, cudaStream_t stream) {
   dim3 grid(p.heads, (p.n_q + 7) / 8);
   const size_t smem = 8 * (size_t)p.rank * sizeof(float);
-  if (dtype == MLA_DTYPE_F32) {
-    if (out_dtype == MLA_DTYPE_F32)
-      simt_project_kernel<float, float><<<grid, 256, smem, stream>>>(p);
-    else
-      simt_project_kernel<float, __nv_bfloat16><<<grid, 256, smem, stream>>>(p);
-  } else {
-    if (out_dtype == MLA_DTYPE_F32)
-      simt_project_kernel<__nv_bfloat16, float><<<grid, 256, smem, stream>>>(p);
-    else
-      simt_project_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, smem, stream>>>(p);
-  }
+  if (dtype != MLA_DTYPE_F32) return cudaErrorInvalidValue;
+  if (out_dtype == MLA_DTYPE_F32)
+    simt_project_kernel<float, float><<<grid, 256, smem, stream>>>(p);
+  else
+    simt_project_kernel<float, __nv_bfloat16><<<grid, 256, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

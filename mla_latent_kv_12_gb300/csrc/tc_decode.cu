@@ -3,8 +3,11 @@
 // ctx = p @ latent; with the per-row windows / selections of Glm52Mla.forward
 // and the causal verify window of Glm52DecoderLayer.attend).
 //
-// Design (bf16, H = 128 heads, rank 512, rope 64):
-//  * All 128 heads of one query row form the M = 128 side of every tcgen05 MMA;
+// Design (bf16, H = 128 or 64 heads, rank 512, rope 64):
+//  * All 128 heads of one query row form the M = 128 side of every tcgen05 MMA
+//    (64 heads are padded to 128 with zero query rows, whose results are
+//    dropped: at one query row the kernel is bound by the cache read, which
+//    the padding does not change);
 //    keys come in tiles of 64 (the N side of the score MMA, the K side of P.V).
 //  * A cluster of two CTAs (an SM pair) owns one stream of work.  The f32
 //    context accumulator [128 x 512] would fill a whole SM's TMEM, so the pair
@@ -76,6 +79,7 @@ struct TcDecodeArgs {
   const int32_t* kv_start;
   const int32_t* kv_len;
   int32_t s_q, n_q;
+  int32_t heads;       // 64 or 128; rows h >= heads of the MMA's M side are zero padding
   const int32_t* sel;
   const int32_t* sel_count;
   int32_t k_max;
@@ -607,6 +611,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     x_full_peer[1] = mapa(smem_u32(&x_full[1]), peer);
     if (a.early_inputs) pdl_wait();   // the query comes from the launch before this one
     uint32_t tile = 0;
+    float half_max = 0.f;   // largest |half score| sent (checked against the fp16 exchange's range)
     int u, n, t0, t1;
     bool whole;
     while (!aborted() && it.next(u, t0, t1, whole)) {
@@ -615,11 +620,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         // Latent dims [dim_base+128, dim_base+256) of this head's query into
         // TMEM columns 64..127 of Q.  Every score MMA of the previous segment
         // has completed (its last scores were read here), so Q is free.
-        const uint4* qlat = reinterpret_cast<const uint4*>(a.q + (int64_t)n * a.q_row_stride +
-                                                           (int64_t)h * a.q_head_stride + dim_base + 128);
         uint4 qv[16];
+        if (h < a.heads) {
+          const uint4* qlat = reinterpret_cast<const uint4*>(a.q + (int64_t)n * a.q_row_stride +
+                                                             (int64_t)h * a.q_head_stride + dim_base + 128);
 #pragma unroll
-        for (int v = 0; v < 16; ++v) qv[v] = __ldg(qlat + v);
+          for (int v = 0; v < 16; ++v) qv[v] = __ldg(qlat + v);
+        } else {
+#pragma unroll
+          for (int v = 0; v < 16; ++v) qv[v] = make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t r[32];
@@ -664,8 +674,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int k = 8 * c + 2 * q;   // scores k, k+1
-            const float lo = fminf(fmaxf(__uint_as_float(k < 32 ? sa[k] : sb[k - 32]), -65504.f), 65504.f);
-            const float hi = fminf(fmaxf(__uint_as_float(k < 32 ? sa[k + 1] : sb[k - 31]), -65504.f), 65504.f);
+            const float lo_raw = __uint_as_float(k < 32 ? sa[k] : sb[k - 32]);
+            const float hi_raw = __uint_as_float(k < 32 ? sa[k + 1] : sb[k - 31]);
+            half_max = fmaxf(half_max, fmaxf(fabsf(lo_raw), fabsf(hi_raw)));
+            const float lo = fminf(fmaxf(lo_raw, -65504.f), 65504.f);
+            const float hi = fminf(fmaxf(hi_raw, -65504.f), 65504.f);
             const __half2 hv = __floats2half2_rn(lo, hi);
             w[q] = *reinterpret_cast<const uint32_t*>(&hv);
           }
@@ -679,6 +692,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         ++tile;
       }
     }
+    // Padding rows (heads >= a.heads) score 0; a key row past the window
+    // holds zeros.  So any half beyond the limit is a real score.
+    if (__any_sync(0xffffffffu, !(half_max <= MLA_FP16_SCORE_LIMIT)) && lane == 0 && a.status)
+      atomicOr(a.status, MLA_DEVICE_SCORE_RANGE);
   } else {
     // ============================================================ softmax / epilogue
     if (a.early_inputs) pdl_wait();   // the query comes from the launch before this one
@@ -697,7 +714,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const int64_t slot = ((int64_t)u + group) * a.width + member;
       if (!any) {
         // Nothing of this row in the group's range: an empty partial (weight 0).
-        if (!whole && rank == 0) {
+        if (!whole && rank == 0 && h < a.heads) {
           a.ws_ml[(slot * 2) * HEADS + h] = -CUDART_INF_F;
           a.ws_ml[(slot * 2 + 1) * HEADS + h] = 0.f;
         }
@@ -710,14 +727,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       // [dim_base, dim_base+128) and the rope half [32*rank, 32*rank+32) here,
       // the other 128 latent dims by the exchange warps; all loads in flight at once.
       {
-        const __nv_bfloat16* qrow = a.q + (int64_t)n * a.q_row_stride + (int64_t)h * a.q_head_stride;
-        const uint4* qlat = reinterpret_cast<const uint4*>(qrow + dim_base);
-        const uint4* qrope = reinterpret_cast<const uint4*>(qrow + RANK + 32 * (int)rank);
         uint4 qv[20];
+        if (h < a.heads) {
+          const __nv_bfloat16* qrow = a.q + (int64_t)n * a.q_row_stride + (int64_t)h * a.q_head_stride;
+          const uint4* qlat = reinterpret_cast<const uint4*>(qrow + dim_base);
+          const uint4* qrope = reinterpret_cast<const uint4*>(qrow + RANK + 32 * (int)rank);
 #pragma unroll
-        for (int v = 0; v < 16; ++v) qv[v] = __ldg(qlat + v);
+          for (int v = 0; v < 16; ++v) qv[v] = __ldg(qlat + v);
 #pragma unroll
-        for (int v = 0; v < 4; ++v) qv[16 + v] = __ldg(qrope + v);
+          for (int v = 0; v < 4; ++v) qv[16 + v] = __ldg(qrope + v);
+        } else {
+#pragma unroll
+          for (int v = 0; v < 20; ++v) qv[v] = make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t r[32];
@@ -880,7 +902,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           store_chunk(c + 1, ob);
         }
       };
-      if (whole) {
+      if (h >= a.heads) {
+        // a padding row: nothing to store
+      } else if (whole) {
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const int64_t off = (int64_t)n * a.ctx_row_stride + (int64_t)h * a.ctx_head_stride + dim_base;
         if (a.out_f32) {
@@ -903,7 +927,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           });
         }
         if (rank == 0 && a.lse)
-          a.lse[(int64_t)n * HEADS + h] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+          a.lse[(int64_t)n * a.heads + h] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
       } else {
         // Partial O as [slot][RANK/8][H][8] f32: a thread stores 8 dims of its
         // head as one 32-byte sector, a warp 1 KB contiguous.
@@ -951,6 +975,7 @@ __global__ void __launch_bounds__(128) tc_combine_kernel(const __grid_constant__
   const int n = blockIdx.x;
   const int d0 = blockIdx.y * CDIMS;
   const int h = threadIdx.x;
+  if (h >= a.heads) return;
   const int u = n / a.width, member = n % a.width;
   const int64_t orow = (int64_t)n * a.ctx_row_stride + (int64_t)h * a.ctx_head_stride + d0;
   float acc[CDIMS];
@@ -1004,7 +1029,7 @@ __global__ void __launch_bounds__(128) tc_combine_kernel(const __grid_constant__
                      pack_bf16x2(acc[6], acc[7]));
     }
     if (blockIdx.y == 0 && a.lse)
-      a.lse[(int64_t)n * HEADS + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -CUDART_INF_F;
+      a.lse[(int64_t)n * a.heads + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -CUDART_INF_F;
   }
 }
 
@@ -1197,7 +1222,7 @@ __global__ void __launch_bounds__(PROJ_THREADS) tc_combine_project_kernel(const 
                               pack_bf16x2(acc[4] * inv, acc[5] * inv), pack_bf16x2(acc[6] * inv, acc[7] * inv));
         }
         if (g == 0 && a.lse && (kind == 1 || kind == 3))
-          a.lse[(int64_t)n * HEADS + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -CUDART_INF_F;
+          a.lse[(int64_t)n * a.heads + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -CUDART_INF_F;
         *reinterpret_cast<uint4*>(sB + (g >> 3) * (npad * 128) + n * 128 + (((g & 7) ^ (n & 7)) << 4)) = packed;
       }
     }
@@ -1271,17 +1296,19 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 int tc_decode_clusters() { return device_sm_count() / 2; }
 
-size_t tc_decode_workspace(int32_t n_q, int32_t heads, int32_t rank) {
+// The partials are laid out for the MMA's 128 rows whatever the head count.
+size_t tc_decode_workspace(int32_t n_q) {
   const size_t slots = (size_t)n_q + tc_decode_clusters();
   return align256((size_t)(n_q + 1) * 4) + align256((size_t)n_q * 4) +
-         align256(slots * heads * rank * 4) + align256(slots * heads * 2 * 4);
+         align256(slots * HEADS * RANK * 4) + align256(slots * HEADS * 2 * 4);
 }
 
 cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* workspace, size_t workspace_bytes,
                              cudaStream_t stream, const DecodeTail* tail) {
   const int n_q = g.batch * g.s_q;
   const int nclusters = tc_decode_clusters();
-  if (workspace_bytes < tc_decode_workspace(n_q, g.heads, g.rank)) return cudaErrorInvalidValue;
+  if (workspace_bytes < tc_decode_workspace(n_q)) return cudaErrorInvalidValue;
+  if (g.heads != 64 && g.heads != HEADS) return cudaErrorInvalidValue;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   TcDecodeArgs a;
   a.q = static_cast<const __nv_bfloat16*>(g.q);
@@ -1297,6 +1324,7 @@ cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* works
   a.kv_len = g.kv_len;
   a.s_q = g.s_q;
   a.n_q = n_q;
+  a.heads = g.heads;
   a.sel = g.sel;
   a.sel_count = g.sel_count;
   a.k_max = g.k_max;
@@ -1314,7 +1342,7 @@ cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* works
   off += align256((size_t)n_q * 4);
   const size_t slots = (size_t)n_q + nclusters;
   a.ws_o = reinterpret_cast<float*>(ws + off);
-  off += align256(slots * g.heads * g.rank * 4);
+  off += align256(slots * HEADS * RANK * 4);
   a.ws_ml = reinterpret_cast<float*>(ws + off);
   a.num_clusters = nclusters;
   // A dense multi-token verify serves each batch row's tokens with a group of
@@ -1364,10 +1392,9 @@ cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* works
         encode_tmap_bf16(&rope_rows_map, g.rope, 2, rd, rs, box))
       a.gather_tma = 1;
   }
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(tc_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    attr = true;
+  {
+    const cudaError_t ea = set_max_dynamic_smem(tc_decode_kernel, SMEM_BYTES);
+    if (ea != cudaSuccess) return ea;
   }
   cudaError_t e = cudaSuccess;
   if (!a.plan_in_kernel) {
@@ -1378,7 +1405,7 @@ cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* works
                  lat_rows_map, rope_rows_map, a);
   if (e != cudaSuccess) return e;
   if (tail == nullptr) {
-    e = launch_pdl(tc_combine_kernel, dim3(n_q, RANK / CDIMS), dim3(HEADS), 0, stream, a);
+    e = launch_pdl(tc_combine_kernel, dim3(n_q, RANK / CDIMS), dim3(g.heads), 0, stream, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
@@ -1398,10 +1425,9 @@ cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* works
   p.v_dim = tail->v_dim;
   p.w_row0 = tail->nope;
   p.w_head_rows = tail->nope + tail->v_dim;
-  static bool attr_tail = false;
-  if (!attr_tail) {
-    cudaFuncSetAttribute(tc_combine_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PROJ_SMEM_MAX);
-    attr_tail = true;
+  {
+    const cudaError_t ea = set_max_dynamic_smem(tc_combine_project_kernel, PROJ_SMEM_MAX);
+    if (ea != cudaSuccess) return ea;
   }
   const size_t smem = 1024 + 8 * PROJ_BOX_BYTES + 8 * (size_t)p.npad * 128 + PROJ_MERGE_BYTES;
   e = launch_pdl(tc_combine_project_kernel, dim3(tail->heads), dim3(PROJ_THREADS), smem, stream, wmap, a, p);

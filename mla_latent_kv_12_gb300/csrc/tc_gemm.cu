@@ -7,6 +7,9 @@
 // Both are weight-read bound at decode sizes (n_q <= 64): each CTA streams one
 // head's weight slice once with TMA and puts the weight on the MMA's M side
 // (swap-AB), so the few query rows become the N dimension (padded to 16).
+// Larger batches are cut into blocks of query rows (256 for the absorb, 64
+// for the projection), one more grid dimension; each block re-reads the
+// weight slice, from L2 after the first.
 // Accumulation is f32 in TMEM; one warp quarter reads back 32 rows each.
 #include <cuda_bf16.h>
 #include <string.h>
@@ -28,13 +31,13 @@ __device__ __forceinline__ void flag_timeout(int32_t* status) {
 }
 
 // ------------------------------------------------------------------ absorb
-// grid (rank/128, heads); 128 threads.  A = W_UK_h^T tile [128 latent x 128 nope]
+// grid (rank/128, heads, row blocks); 128 threads.  A = W_UK_h^T tile [128 latent x 128 nope]
 // (MN-major: latent contiguous in kv_b_proj rows), B = q_nope rows of head h
 // [npad x 128] (K-major).  D [128 latent x npad] f32 in TMEM.
 struct AbsorbArgs {
   void* out;
   int64_t out_row_stride, out_head_stride;
-  int32_t n_q, npad;
+  int32_t n_q, npad;     // npad: query rows per block (the MMA's N), a multiple of 16
   int32_t w_head_rows;  // W_UK_h starts at row h*w_head_rows
   int32_t* status;
   int32_t with_rope;    // CTAs of blockIdx.x == 0 also rotate q_rope of head h
@@ -53,6 +56,7 @@ __global__ void __launch_bounds__(128) tc_absorb_kernel(const __grid_constant__ 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * 128, h = blockIdx.y;
   const int npad = a.npad;
+  const int row0 = blockIdx.z * npad;   // first query row of this block
   const uint32_t ncols = npad <= 32 ? 32 : (npad <= 64 ? 64 : (npad <= 128 ? 128 : 256));
 
   if (threadIdx.x == 0) {
@@ -82,8 +86,8 @@ __global__ void __launch_bounds__(128) tc_absorb_kernel(const __grid_constant__ 
     mbar_arrive_expect_tx(&bar_full, bytes);
     tma_load_2d(sA, &wmap, &bar_full, m0, h * a.w_head_rows);
     tma_load_2d(sA + 16384, &wmap, &bar_full, m0 + 64, h * a.w_head_rows);
-    tma_load_3d(sB, &qmap, &bar_full, 0, h, 0);
-    tma_load_3d(sB + npad * 128, &qmap, &bar_full, 64, h, 0);
+    tma_load_3d(sB, &qmap, &bar_full, 0, h, row0);               // rows past n_q load as zeros
+    tma_load_3d(sB + npad * 128, &qmap, &bar_full, 64, h, row0);
     ok = mbar_wait(&bar_full, 0, kWaitLimit);
     if (ok) {
       tc_fence_after();
@@ -106,7 +110,8 @@ __global__ void __launch_bounds__(128) tc_absorb_kernel(const __grid_constant__ 
     // While the MMAs run: RoPE of head h's rope part, lane j = rotary pair j,
     // warp w = query rows w, w+4, ...
     const AbsorbRope& r = a.rope;
-    for (int n = warp; n < a.n_q; n += 4) {
+    const int row_end = min(a.n_q, row0 + npad);
+    for (int n = row0 + warp; n < row_end; n += 4) {
       const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(r.q_rope) + (int64_t)n * r.row_stride +
                                  (int64_t)h * r.head_stride;
       const __nv_bfloat162 ab = reinterpret_cast<const __nv_bfloat162*>(src)[lane];
@@ -132,7 +137,7 @@ __global__ void __launch_bounds__(128) tc_absorb_kernel(const __grid_constant__ 
       tmem_wait_ld();
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        const int n = c0 + j;
+        const int n = row0 + c0 + j;
         if (n < a.n_q) out[(int64_t)n * a.out_row_stride] = __float2bfloat16_rn(__uint_as_float(r[j]));
       }
     }
@@ -144,7 +149,7 @@ __global__ void __launch_bounds__(128) tc_absorb_kernel(const __grid_constant__ 
 }
 
 // ------------------------------------------------------------------ project
-// grid (heads); 128 threads.  A = W_UV_h [128 v x 512 latent] (K-major),
+// grid (heads, row blocks); 128 threads.  A = W_UV_h [128 v x 512 latent] (K-major),
 // B = ctx rows of head h [npad x 512] (K-major).  8 K-boxes of 64, one
 // barrier each so the MMAs start as soon as the first box lands.
 struct ProjectArgs {
@@ -169,6 +174,7 @@ __global__ void __launch_bounds__(128) tc_project_kernel(const __grid_constant__
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x;
   const int npad = a.npad;
+  const int qrow0 = blockIdx.y * npad;   // first query row of this block
   const uint32_t ncols = npad <= 32 ? 32 : 64;
 
   if (threadIdx.x == 0) {
@@ -194,7 +200,7 @@ __global__ void __launch_bounds__(128) tc_project_kernel(const __grid_constant__
     for (int i = 0; i < 8; ++i) {
       mbar_arrive_expect_tx(&bar_full[i], 16384 + npad * 128);
       tma_load_2d(sA + i * 16384, &wmap, &bar_full[i], 64 * i, row0);
-      tma_load_3d(sB + i * npad * 128, &cmap, &bar_full[i], 64 * i, h, 0);
+      tma_load_3d(sB + i * npad * 128, &cmap, &bar_full[i], 64 * i, h, qrow0);   // rows past n_q: zeros
     }
     const uint32_t idesc = idesc_bf16_f32(128, npad, 0, 0);
     const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
@@ -229,7 +235,7 @@ __global__ void __launch_bounds__(128) tc_project_kernel(const __grid_constant__
       tmem_wait_ld();
 #pragma unroll
       for (int t = 0; t < 16; ++t) {
-        const int n = c0 + t;
+        const int n = qrow0 + c0 + t;
         if (n >= a.n_q) continue;
         const float v = __uint_as_float(r[t]);
         const int64_t off = (int64_t)n * a.out_row_stride + (int64_t)h * a.v_dim + j;
@@ -250,8 +256,11 @@ int pad16(int n) { return (n + 15) & ~15; }
 
 }  // namespace
 
+constexpr int kAbsorbBlockRows = 256, kProjectBlockRows = 64;
+
 cudaError_t launch_tc_absorb(const AbsorbParams& p, cudaStream_t stream, const AbsorbRope* rope) {
-  const int npad = pad16(p.n_q);
+  const int npad = p.n_q > kAbsorbBlockRows ? kAbsorbBlockRows : pad16(p.n_q);
+  const int nblk = (p.n_q + npad - 1) / npad;
   CUtensorMap wmap, qmap;
   {
     const uint64_t dims[2] = {(uint64_t)p.rank, (uint64_t)p.heads * (p.nope + p.v_dim)};
@@ -278,17 +287,18 @@ cudaError_t launch_tc_absorb(const AbsorbParams& p, cudaStream_t stream, const A
     a.rope = *rope;
   }
   const size_t smem = 1024 + 32768 + 2 * (size_t)npad * 128;
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(tc_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 1024 + 32768 + 2 * 256 * 128);
-    attr = true;
+  {
+    const cudaError_t ea = set_max_dynamic_smem(tc_absorb_kernel, (int)(1024 + 32768 + 2 * 256 * 128));
+    if (ea != cudaSuccess) return ea;
   }
-  const cudaError_t e = launch_pdl(tc_absorb_kernel, dim3(p.rank / 128, p.heads), dim3(128), smem, stream, wmap, qmap, a);
+  const cudaError_t e =
+      launch_pdl(tc_absorb_kernel, dim3(p.rank / 128, p.heads, nblk), dim3(128), smem, stream, wmap, qmap, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_tc_project(const ProjectParams& p, int out_dtype, cudaStream_t stream) {
-  const int npad = pad16(p.n_q);
+  const int npad = p.n_q > kProjectBlockRows ? kProjectBlockRows : pad16(p.n_q);
+  const int nblk = (p.n_q + npad - 1) / npad;
   CUtensorMap wmap, cmap;
   {
     const uint64_t dims[2] = {(uint64_t)p.rank, (uint64_t)p.heads * (p.nope + p.v_dim)};
@@ -306,12 +316,11 @@ cudaError_t launch_tc_project(const ProjectParams& p, int out_dtype, cudaStream_
   ProjectArgs a{p.out, p.out_row_stride, p.n_q, npad, p.v_dim, p.nope, p.nope + p.v_dim,
                 out_dtype == MLA_DTYPE_F32 ? 1 : 0, nullptr};
   const size_t smem = 1024 + 8 * 16384 + 8 * (size_t)npad * 128;
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(tc_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 1024 + 8 * 16384 + 8 * 64 * 128);
-    attr = true;
+  {
+    const cudaError_t ea = set_max_dynamic_smem(tc_project_kernel, (int)(1024 + 8 * 16384 + 8 * 64 * 128));
+    if (ea != cudaSuccess) return ea;
   }
-  const cudaError_t e = launch_pdl(tc_project_kernel, dim3(p.heads), dim3(128), smem, stream, wmap, cmap, a);
+  const cudaError_t e = launch_pdl(tc_project_kernel, dim3(p.heads, nblk), dim3(128), smem, stream, wmap, cmap, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

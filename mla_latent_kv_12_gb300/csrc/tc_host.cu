@@ -1,6 +1,7 @@
 #include <cudaTypedefs.h>
 #include <mutex>
 
+#include "attr_cache.h"
 #include "mla_internal.h"
 #include "tc_host.h"
 
@@ -22,7 +23,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   });
   return fn;
 }
+AttrCache g_smem_attrs;
 }  // namespace
+
+cudaError_t set_max_dynamic_smem(const void* kernel, int bytes) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int r = g_smem_attrs.ensure(kernel, dev, bytes, [](const void* f, int b) {
+    return (int)cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, b);
+  });
+  return (cudaError_t)r;
+}
 
 bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                       const uint64_t* strides_bytes, const uint32_t* box) {

@@ -16,6 +16,15 @@ namespace mla {
 bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                       const uint64_t* strides_bytes, const uint32_t* box);
 
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per (kernel, device); thread-safe.  Returns the CUDA error of
+// the attribute call (cudaSuccess when already set).
+cudaError_t set_max_dynamic_smem(const void* kernel, int bytes);
+template <typename... KArgs>
+cudaError_t set_max_dynamic_smem(void (*kernel)(KArgs...), int bytes) {
+  return set_max_dynamic_smem(reinterpret_cast<const void*>(kernel), bytes);
+}
+
 // Launch with programmatic dependent launch allowed: the kernel may start its
 // prologue while the previous kernel in the stream drains; every kernel
 // launched this way calls griddepcontrol.wait before it touches memory the

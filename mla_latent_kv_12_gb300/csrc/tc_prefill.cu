@@ -660,10 +660,9 @@ cudaError_t launch_tc_reconstruct(const ReconstructParams& p, cudaStream_t strea
     const uint32_t box[3] = {64, 1, 128};
     if (!encode_tmap_bf16(&v_map, p.v, 3, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(tc_reconstruct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RC_SMEM);
-    attr = true;
+  {
+    const cudaError_t ea = set_max_dynamic_smem(tc_reconstruct_kernel, RC_SMEM);
+    if (ea != cudaSuccess) return ea;
   }
   const int row_tiles = (int)((p.n_rows + 127) / 128);
   const int64_t n_tiles = (int64_t)row_tiles * p.heads;
@@ -709,10 +708,9 @@ cudaError_t launch_tc_prefill(const PrefillParams& p, cudaStream_t stream) {
     const uint32_t box[3] = {64, 1, 128};
     if (!encode_tmap_bf16(&v_map, p.v, 3, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(tc_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM);
-    attr = true;
+  {
+    const cudaError_t ea = set_max_dynamic_smem(tc_prefill_kernel, PF_SMEM);
+    if (ea != cudaSuccess) return ea;
   }
   PrefillArgs a;
   memset(&a, 0, sizeof(a));

@@ -7,7 +7,6 @@ fails loudly if the built library is missing; there is no fallback.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 from typing import Optional
 
@@ -21,11 +20,13 @@ DEVICE_BAD_SELECTION_COUNT = 1 << 1
 DEVICE_INDEX_OUT_OF_RANGE = 1 << 4
 DEVICE_TIMEOUT = 1 << 5
 DEVICE_LAYOUT = 1 << 6
+DEVICE_SCORE_RANGE = 1 << 7
+FP16_SCORE_LIMIT = 256.0
 
 _DT = {torch.float32: F32, torch.bfloat16: BF16}
 
 EXPORTS = (
-    "mla_status_string", "mla_last_error_detail", "mla_version",
+    "mla_status_string", "mla_last_error_detail", "mla_version", "mla_default_softmax_scale",
     "mla_rope_partial_interleaved", "mla_absorb_q", "mla_decode_attend",
     "mla_decode_workspace_size", "mla_decode_kernel_kind", "mla_project_v",
     "mla_gather_selected", "mla_decode_attend_no_alloc", "mla_decode_step",
@@ -54,6 +55,8 @@ def _load() -> ctypes.CDLL:
     lib.mla_last_error_detail.restype = ctypes.c_char_p
     lib.mla_last_error_detail.argtypes = []
     lib.mla_version.restype = ctypes.c_int
+    lib.mla_default_softmax_scale.restype = f32
+    lib.mla_default_softmax_scale.argtypes = [i32, i32]
     lib.mla_rope_partial_interleaved.restype = ctypes.c_int
     lib.mla_rope_partial_interleaved.argtypes = [vp, vp, ctypes.c_int, i64, i64, i64, i64, i64p, i64p,
                                                  i32, f32, vp, i64, vp]
@@ -384,5 +387,5 @@ def prefill_attend(q_nope: torch.Tensor, q_rope: torch.Tensor, k_nope: torch.Ten
 
 
 def default_scale(nope: int, rope_dim: int) -> float:
-    """The page's softmax scale ``1/sqrt(qk_nope + qk_rope)``."""
-    return 1.0 / math.sqrt(nope + rope_dim)
+    """The page's softmax scale ``1/sqrt(qk_nope + qk_rope)``, as the library computes it."""
+    return float(lib.mla_default_softmax_scale(nope, rope_dim))

@@ -78,6 +78,46 @@ def test_decode_validation(lib):
     assert L.mla_decode_kernel_kind(128, 512, 64, 7, 1) == -1
 
 
+def test_bf16_shapes_outside_the_fast_path_are_refused(lib):
+    # bf16 is served for heads 64 / 128, rank 512, rope 64 (nope 128, v 128 for
+    # the projections); anything else returns MLA_ERR_UNSUPPORTED before any
+    # launch (the pointers here are not device memory: a launch would fault).
+    L = lib.lib
+    args = [16, 576, 576, 16, 576, 0, 16, 576, 0, 1, None, 16, 1, 1, 128, 512, 64, 4096,
+            None, None, 0, 0.07, 16, 65536, 512, 1, None, None, 0, None, None]
+    for i, v in [(14, 16), (14, 96), (15, 256), (16, 32)]:   # heads 16 / 96, rank 256, rope 32
+        bad = list(args); bad[i] = v
+        assert L.mla_decode_attend(*bad) == 2, (i, v)
+        assert "bf16 is served" in L.mla_last_error_detail().decode()
+    assert L.mla_decode_kernel_kind(128, 512, 64, 1, 1) == 1
+    assert L.mla_decode_kernel_kind(64, 512, 64, 1, 1) == 1
+    assert L.mla_decode_kernel_kind(16, 512, 64, 1, 1) == -1
+    assert L.mla_decode_kernel_kind(16, 32, 8, 0, 0) == 0          # f32: CUDA cores, any shape
+    assert L.mla_decode_workspace_size(1, 1, 16, 512, 64, 4096, 0, 0, 1) == 0
+    assert L.mla_decode_workspace_size(1, 1, 64, 512, 64, 4096, 0, 0, 1) > 0
+    # absorb: q_nope, strides, kv_b_proj, q_out, strides, dtype, n_q, heads, nope, v, rank
+    assert L.mla_absorb_q(16, 0, 128, 16, 16, 0, 576, 1, 1, 16, 128, 128, 512, None) == 2
+    assert L.mla_absorb_q(16, 0, 64, 16, 16, 0, 576, 1, 1, 128, 64, 128, 512, None) == 2
+    assert "bf16 is served" in L.mla_last_error_detail().decode()
+    # project: ctx, strides, kv_b_proj, dtype, out, stride, out dtype, n_q, heads, nope, v, rank
+    assert L.mla_project_v(16, 0, 512, 16, 1, 16, 16 * 128, 1, 1, 16, 128, 128, 512, None) == 2
+    assert L.mla_project_v(16, 0, 512, 16, 1, 16, 128 * 64, 1, 1, 128, 128, 64, 512, None) == 2
+
+
+def test_default_scale_and_workspace_limits(lib):
+    L = lib.lib
+    import numpy as np
+    assert L.mla_default_softmax_scale(128, 64) == np.float32(1.0 / np.sqrt(192.0))
+    assert L.mla_default_softmax_scale(16, 8) == np.float32(1.0 / np.sqrt(24.0))
+    assert L.mla_default_softmax_scale(0, 0) == 0.0
+    assert lib.default_scale(128, 64) == float(np.float32(1.0 / np.sqrt(192.0)))
+    # batch * s_q past the limits (and past int32) gives 0, not a wrapped size
+    assert L.mla_decode_workspace_size(1 << 16, 1 << 16, 128, 512, 64, 4096, 0, 0, 1) == 0
+    assert L.mla_decode_workspace_size(1 << 20, 2, 128, 512, 64, 4096, 0, 0, 1) == 0
+    assert L.mla_decode_workspace_size(1 << 20, 1, 128, 512, 64, 4096, 0, 0, 1) > 0
+    assert L.mla_decode_workspace_size(1 << 16, 1 << 16, 4, 32, 8, 64, 0, 0, 0) == 0
+
+
 def test_absorb_and_project_validation(lib):
     L = lib.lib
     assert L.mla_absorb_q(None, 0, 128, 16, 16, 0, 576, 1, 1, 128, 128, 128, 512, None) == 1
@@ -107,7 +147,8 @@ def test_decode_step_validation(lib):
     bad = list(args); bad[36] = 1024                     # workspace too small
     assert L.mla_decode_step(*bad) == 1
     assert L.mla_decode_step_workspace_size(1, 1, 128, 128, 128, 512, 64, 4096, 0, 0, 1) > 0
-    assert L.mla_decode_step_workspace_size(1, 1, 64, 128, 128, 512, 64, 4096, 0, 0, 1) == 0
+    assert L.mla_decode_step_workspace_size(1, 1, 64, 128, 128, 512, 64, 4096, 0, 0, 1) > 0
+    assert L.mla_decode_step_workspace_size(1, 1, 32, 128, 128, 512, 64, 4096, 0, 0, 1) == 0
     assert L.mla_decode_step_workspace_size(1, 1, 128, 128, 128, 512, 64, 4096, 0, 0, 0) == 0
 
 

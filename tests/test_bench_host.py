@@ -64,8 +64,44 @@ def test_reference_arm_rank_rule():
     assert r0.returncode == 0, r0.stderr
     line = json.loads(r0.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0
-    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+    # the reported step time is the time measured per step (not scaled up)
+    assert line["ms_per_step"] < 60_000
+
+
+def test_one_row_inputs_give_the_same_oracle_rows():
+    # the host-core oracle pool works on one batch row at a time: the row cut
+    # out of a ragged packed batch gives the oracle's rows of the whole batch
+    import dataclasses
+    import numpy as np
+    from mla_latent_kv_12_gb300 import workloads as W
+    from tests import helpers as H
+    w = dataclasses.replace(W.RAGGED_BF16, heads=4)
+    inp = W.make_inputs(w, layout="flat", rows=3, t_override=200)
+    for b in range(3):
+        one = bench.one_row_inputs(inp, b)
+        a = H.oracle_reference_out_only(one, rows=[0], heads=[0, 3])
+        full = H.oracle_reference_out_only(inp, rows=[b], heads=[0, 3])
+        assert np.allclose(a[0], full[b], rtol=1e-12, atol=1e-12)
+    w = dataclasses.replace(W.VERIFY_SPARSE_BF16, heads=2, top_k=20)
+    inp = W.make_inputs(w, rows=2, t_override=60)
+    one = bench.one_row_inputs(inp, 1)
+    a = H.oracle_reference_out_only(one, rows=[0, 1, 2, 3], heads=[1])
+    full = H.oracle_reference_out_only(inp, rows=[4, 5, 6, 7], heads=[1])
+    assert np.allclose(a[:4], full[4:8], rtol=1e-12, atol=1e-12)
+
+
+def test_step_bytes_and_layer_rotation():
+    from mla_latent_kv_12_gb300 import workloads as W
+    inp = W.make_inputs(W.DENSE_BF16)
+    byts, flops = bench.step_algorithmic(inp)
+    weights = 128 * 256 * 512 * 2
+    assert byts == 4096 * 1152 + weights + 128 * 192 * 2 + 128 * 128 * 2
+    assert flops == 4096 * 2 * 128 * 1088 + 2 * 128 * 512 * 256
+    R = bench.layers_for(inp, byts)
+    assert (R - 1) * byts >= 2 * bench.L2_BYTES            # other layers' bytes between two uses
+    assert bench.layers_for(inp, 10 ** 12) == 1
 
 
 def test_algorithmic_counts():

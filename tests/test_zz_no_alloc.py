@@ -4,14 +4,16 @@ Some callers cannot allocate device memory at decode time -- a server whose
 pool already owns the free memory, a plugin host without an allocator, a
 latency-bound loop.  For them the library keeps the split-K scratch in a
 built-in device array.  This file checks, through the C ABI, that this entry
-point gives what mla_decode_attend gives with a caller-allocated workspace, on
-two calls in a row (the shared array keeps the previous call's contents), and
-that a request too large for the array is refused without a launch.  It is
-collected last so that a failure here never hides another test's result.
+point gives what mla_decode_attend gives with a caller-allocated workspace and
+what the float64 oracle gives, on two calls in a row and on calls of
+different shapes in turn (the shared array keeps the previous call's
+contents), and that a request too large for the array is refused without a
+launch.  It is collected last so that a failure here never hides another
+test's result.
 """
-import ctypes
 import dataclasses
 
+import numpy as np
 import pytest
 import torch
 
@@ -41,6 +43,8 @@ def _no_alloc(step, ctx, lse, status):
 
 CASES = {
     "dense_t4096": lambda: W.make_inputs(W.DENSE_BF16),
+    "ragged_150_rows": lambda: W.make_inputs(dataclasses.replace(W.RAGGED_BF16, batch=150), layout="flat",
+                                             t_override=700),
     "ragged_flat": lambda: W.make_inputs(W.RAGGED_BF16, layout="flat", rows=5, t_override=1500),
     "sparse": lambda: W.make_inputs(dataclasses.replace(W.SPARSE_BF16, top_k=300), rows=3, t_override=5000),
     "verify": lambda: W.make_inputs(dataclasses.replace(W.VERIFY_BF16, top_k=0), rows=3, t_override=1100),
@@ -48,25 +52,61 @@ CASES = {
 }
 
 
-@pytest.mark.parametrize("case", sorted(CASES))
-def test_no_alloc_matches_workspace_entry_point(case):
+# query rows checked against the oracle (all rows of the small cases)
+ORACLE_ROWS = {"dense_t4096": None, "ragged_150_rows": [0, 1, 127, 128, 149], "ragged_flat": None,
+               "sparse": None, "verify": None, "tiny_f32": None}
+ORACLE_HEADS = {"dense_t4096": [0, 9, 64, 127], "ragged_150_rows": [0, 64, 127]}
+
+
+def _check_call(case, step, ref, call):
+    """One no-alloc call: against the workspace entry point's result and the oracle."""
+    w = step.w
+    ctx = torch.full_like(step.ctx, float("nan"))
+    lse = torch.full_like(step.lse, float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = _no_alloc(step, ctx, lse, status)
+    assert rc == 0, mla.lib.mla_last_error_detail().decode()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    H.assert_close(ctx, step.ctx, w.dtype, f"{case} ctx call {call} vs workspace entry point")
+    fin = torch.isfinite(step.lse)
+    assert torch.equal(torch.isfinite(lse), fin)
+    assert torch.max(torch.abs(lse[fin] - step.lse[fin])).item() <= 2e-2
+    rows, hs = ref["rows"], ref["heads"]
+    ri, hi = torch.tensor(rows), torch.tensor(hs)
+    H.assert_close(ctx.cpu()[ri][:, hi], ref["ctx"][rows], w.dtype, f"{case} ctx call {call} vs oracle")
+    l_got, l_want = H.f64(lse.cpu()[ri][:, hi]), ref["lse"][rows]
+    ok = np.isfinite(l_want)
+    assert np.array_equal(np.isfinite(l_got), ok)
+    assert np.max(np.abs(l_got[ok] - l_want[ok]), initial=0.0) <= (2e-2 if w.dtype == "bf16" else 1e-4)
+
+
+def _prepare(case):
     inp = CASES[case]()
     step = DecodeStep(inp, "cuda", fused=False)
     step.run()                                  # reference: caller-allocated workspace
     torch.cuda.synchronize()
     assert int(step.status.item()) == 0
+    ref = H.oracle_reference(inp, ORACLE_ROWS[case], ORACLE_HEADS.get(case))
+    return step, ref
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_no_alloc_matches_workspace_entry_point_and_oracle(case):
+    step, ref = _prepare(case)
     for call in range(2):                       # two calls in a row on the shared array
-        ctx = torch.full_like(step.ctx, float("nan"))
-        lse = torch.full_like(step.lse, float("nan"))
-        status = torch.zeros(1, dtype=torch.int32, device="cuda")
-        rc = _no_alloc(step, ctx, lse, status)
-        assert rc == 0, mla.lib.mla_last_error_detail().decode()
-        torch.cuda.synchronize()
-        assert int(status.item()) == 0
-        H.assert_close(ctx, step.ctx, inp.w.dtype, f"ctx call {call}")
-        fin = torch.isfinite(step.lse)
-        assert torch.equal(torch.isfinite(lse), fin)
-        assert torch.max(torch.abs(lse[fin] - step.lse[fin])).item() <= 2e-2
+        _check_call(case, step, ref, call)
+
+
+def test_no_alloc_calls_of_different_shapes_in_turn():
+    # The shared array is not cleared between calls: each call must write all
+    # it reads, whatever a larger call before it left there.
+    order = ["ragged_150_rows", "sparse", "dense_t4096", "verify", "ragged_flat", "dense_t4096",
+             "ragged_150_rows", "verify"]
+    prepared = {c: _prepare(c) for c in sorted(set(order))}
+    for k, case in enumerate(order):
+        step, ref = prepared[case]
+        _check_call(case, step, ref, k)
 
 
 def test_no_alloc_refuses_requests_beyond_its_array():
