@@ -75,6 +75,10 @@ typedef enum mla_dtype { MLA_DTYPE_F32 = 0, MLA_DTYPE_BF16 = 1 } mla_dtype;
 #define MLA_DEVICE_SCORE_RANGE (1 << 7)         /* a bf16 decode score half exceeded
                                                    MLA_FP16_SCORE_LIMIT (see
                                                    mla_decode_attend)               */
+#define MLA_DEVICE_VALUE_RANGE (1 << 8)         /* a split piece's context (an average
+                                                   of latent rows) left the fp16
+                                                   range of the bf16 decode's
+                                                   partials; saturated               */
 /* Largest |half score| (unscaled q . k over one CTA's 288 features) that the
  * bf16 decode's fp16 score exchange carries within the bf16 tolerance. */
 #define MLA_FP16_SCORE_LIMIT 256.0f
@@ -210,7 +214,7 @@ int mla_decode_attend(const void* q, int64_t q_row_stride, int64_t q_head_stride
  * that device current; make that first call before any stream capture.
  * Limit: a request whose mla_decode_workspace_size(...) exceeds
  * MLA_NO_ALLOC_SCRATCH_BYTES returns MLA_ERR_UNSUPPORTED and launches nothing
- * (at H = 128, rank 512 on a 152-SM GB300 this allows about 170 query rows).
+ * (at H = 128, rank 512 on a 152-SM GB300 this allows about 430 query rows).
  * Sharing: every call on a device uses the same array, which keeps the last
  * call's contents; nothing in it has to start at zero (each call writes what
  * it later reads).  Calls whose work overlaps on the GPU -- unordered streams,

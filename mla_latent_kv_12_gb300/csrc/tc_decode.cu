@@ -91,7 +91,7 @@ struct TcDecodeArgs {
   int32_t* status;
   int32_t* prefix;     // [n_units + 1] tile prefix over work units (planner)
   int32_t* keys;       // [n_q] visible entries per query row (planner)
-  float* ws_o;         // [slots][512][H] partial O (heads contiguous)
+  uint4* ws_o;         // [slots][RANK/8][H] partial context, 8 fp16 dims per entry (O / l of the piece)
   float* ws_ml;        // [slots][2][H] partial (m, l), log2 domain
   int32_t num_clusters;
   int32_t width;       // query rows per work unit = clusters per group
@@ -334,7 +334,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     mbar_init(&s_free, 4);      // the exchange warps have read S
     mbar_init(&p_full, 4);      // one arrival per softmax warp
     mbar_init(&pv_done, 1);
-    mbar_init(&q_full, 8);      // softmax warps (latent dims 0..127, rope) + exchange warps (128..255)
+    mbar_init(&q_full, 4);      // the exchange warps have written this segment's query into TMEM
     mbar_init(&o_free, 4);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&x_full[b], 1);   // local expect_tx arrival + the peer's remote-store bytes
@@ -617,32 +617,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     while (!aborted() && it.next(u, t0, t1, whole)) {
       if (!member_segment(a, keys_p, u, member, n, t0, t1)) continue;
       {
-        // Latent dims [dim_base+128, dim_base+256) of this head's query into
-        // TMEM columns 64..127 of Q.  Every score MMA of the previous segment
-        // has completed (its last scores were read here), so Q is free.
-        uint4 qv[16];
-        if (h < a.heads) {
-          const uint4* qlat = reinterpret_cast<const uint4*>(a.q + (int64_t)n * a.q_row_stride +
-                                                             (int64_t)h * a.q_head_stride + dim_base + 128);
+        // This head's query (this CTA's latent dims [dim_base, dim_base+256)
+        // into TMEM columns 0..127 of Q, its rope dims [32*rank, 32*rank+32)
+        // into columns 128..143).  Every score MMA of the previous segment has
+        // completed (its last scores were read here), so Q is free; the
+        // softmax warps may still be finishing that segment meanwhile.
+        const __nv_bfloat16* qrow = a.q + (int64_t)n * a.q_row_stride + (int64_t)h * a.q_head_stride;
+        const bool real = h < a.heads;   // rows past the head count stay zero
+        {
+          // all 36 loads in flight at once: 256 latent dims, then the 32 rope dims
+          uint4 qv[36];
+          const uint4* qlat = reinterpret_cast<const uint4*>(qrow + dim_base);
+          const uint4* qrope = reinterpret_cast<const uint4*>(qrow + RANK + 32 * (int)rank);
 #pragma unroll
-          for (int v = 0; v < 16; ++v) qv[v] = __ldg(qlat + v);
-        } else {
+          for (int v = 0; v < 32; ++v) qv[v] = real ? __ldg(qlat + v) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-          for (int v = 0; v < 16; ++v) qv[v] = make_uint4(0, 0, 0, 0);
-        }
+          for (int v = 0; v < 4; ++v) qv[32 + v] = real ? __ldg(qrope + v) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t r[32];
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            r[4 * v] = qv[8 * c + v].x, r[4 * v + 1] = qv[8 * c + v].y, r[4 * v + 2] = qv[8 * c + v].z,
-            r[4 * v + 3] = qv[8 * c + v].w;
-          tmem_st32(tmem + TM_Q + (2 + c) * 32 + lane_off, r);
+            for (int v = 0; v < 8; ++v)
+              r[4 * v] = qv[8 * c + v].x, r[4 * v + 1] = qv[8 * c + v].y, r[4 * v + 2] = qv[8 * c + v].z,
+              r[4 * v + 3] = qv[8 * c + v].w;
+            tmem_st32(tmem + TM_Q + c * 32 + lane_off, r);
+          }
+          uint32_t r[16];
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            r[4 * v] = qv[32 + v].x, r[4 * v + 1] = qv[32 + v].y, r[4 * v + 2] = qv[32 + v].z, r[4 * v + 3] = qv[32 + v].w;
+          tmem_st16(tmem + TM_Q + 128 + lane_off, r);
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&q_full);
+        // The next segment's query row into L2 (this head's 512 + 64 bytes),
+        // so that loading it at the next boundary is an L2 hit.
+        WorkIter peek = it;
+        int un, nn, tn0, tn1;
+        bool wn;
+        while (peek.next(un, tn0, tn1, wn)) {
+          if (!member_segment(a, keys_p, un, member, nn, tn0, tn1)) continue;
+          if (real) {
+            const __nv_bfloat16* qnext = a.q + (int64_t)nn * a.q_row_stride + (int64_t)h * a.q_head_stride;
+#pragma unroll
+            for (int l = 0; l < 4; ++l) prefetch_l2(qnext + dim_base + 64 * l);
+            prefetch_l2(qnext + RANK + 32 * (int)rank);
+          }
+          break;
+        }
       }
       for (int t = t0; t < t1; ++t) {
         const uint32_t b = tile & 1u, use = tile >> 1;
@@ -723,44 +747,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const int keys = keys_p[n];
       const int limit = a.plan_in_kernel ? row_limit_s[n] : row_limit(a, n);
       const int32_t* list = (gather && a.sel_count[n] != -1) ? a.sel + (int64_t)n * a.k_max : nullptr;
-      // ---- Q row of this head (this CTA's dims) into TMEM: latent dims
-      // [dim_base, dim_base+128) and the rope half [32*rank, 32*rank+32) here,
-      // the other 128 latent dims by the exchange warps; all loads in flight at once.
-      {
-        uint4 qv[20];
-        if (h < a.heads) {
-          const __nv_bfloat16* qrow = a.q + (int64_t)n * a.q_row_stride + (int64_t)h * a.q_head_stride;
-          const uint4* qlat = reinterpret_cast<const uint4*>(qrow + dim_base);
-          const uint4* qrope = reinterpret_cast<const uint4*>(qrow + RANK + 32 * (int)rank);
-#pragma unroll
-          for (int v = 0; v < 16; ++v) qv[v] = __ldg(qlat + v);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) qv[16 + v] = __ldg(qrope + v);
-        } else {
-#pragma unroll
-          for (int v = 0; v < 20; ++v) qv[v] = make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t r[32];
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            r[4 * v] = qv[8 * c + v].x, r[4 * v + 1] = qv[8 * c + v].y, r[4 * v + 2] = qv[8 * c + v].z,
-            r[4 * v + 3] = qv[8 * c + v].w;
-          tmem_st32(tmem + TM_Q + c * 32 + lane_off, r);
-        }
-        {
-          uint32_t r[16];
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            r[4 * v] = qv[16 + v].x, r[4 * v + 1] = qv[16 + v].y, r[4 * v + 2] = qv[16 + v].z, r[4 * v + 3] = qv[16 + v].w;
-          tmem_st16(tmem + TM_Q + 128 + lane_off, r);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&q_full);
-      }
       float m_used = -CUDART_INF_F, l = 0.f;
       bool first_tile = true;
       for (int t = t0; t < t1; ++t) {
@@ -929,18 +915,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (rank == 0 && a.lse)
           a.lse[(int64_t)n * a.heads + h] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
       } else {
-        // Partial O as [slot][RANK/8][H][8] f32: a thread stores 8 dims of its
-        // head as one 32-byte sector, a warp 1 KB contiguous.
-        float* dst = a.ws_o + ((slot * (RANK / 8) + dim_base / 8) * HEADS + h) * 8;
+        // Partial as [slot][RANK/8][H] entries of 8 fp16 dims: this piece's
+        // context normalised by its own sum (O / l, an average of latent
+        // rows, so within the range of the cache's values), with (m, l) in
+        // f32 beside it.  A thread stores 8 dims of its head as one 16-byte
+        // vector, a warp 512 B contiguous.
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint4* dst = a.ws_o + (slot * (RANK / 8) + dim_base / 8) * HEADS + h;
+        float vmax = 0.f;
         drain_o([&](int c, const uint32_t(&o)[32]) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            float v[8];
+            uint32_t w[4];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(o[8 * q + j]);
-            st_global_v8(dst + (int64_t)(4 * c + q) * HEADS * 8, v);
+            for (int j = 0; j < 4; ++j) {
+              const float x0 = __uint_as_float(o[8 * q + 2 * j]) * inv, x1 = __uint_as_float(o[8 * q + 2 * j + 1]) * inv;
+              vmax = fmaxf(vmax, fmaxf(fabsf(x0), fabsf(x1)));   // beyond 65504 the fp16 value is infinite
+              const __half2 hv = __floats2half2_rn(x0, x1);
+              w[j] = *reinterpret_cast<const uint32_t*>(&hv);
+            }
+            dst[(int64_t)(4 * c + q) * HEADS] = make_uint4(w[0], w[1], w[2], w[3]);
           }
         });
+        if (!(vmax <= 65504.f) && a.status) atomicOr(a.status, MLA_DEVICE_VALUE_RANGE);
         if (rank == 0) {
           a.ws_ml[(slot * 2) * HEADS + h] = l > 0.f ? m_used : -CUDART_INF_F;
           a.ws_ml[(slot * 2 + 1) * HEADS + h] = l;
@@ -965,9 +962,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }
 
 // ------------------------------------------------------------------ combine
+// 8 fp16 dims of a stored partial (loaded as one 16-byte vector), as f32.
+__device__ __forceinline__ uint4 ld_partial(const uint4* p) {
+  uint4 r;
+  asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p) : "memory");
+  return r;
+}
+__device__ __forceinline__ void unpack_partial(const uint4 r, float (&x)[8]) {
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+    x[2 * j] = f.x;
+    x[2 * j + 1] = f.y;
+  }
+}
+
 // grid (n_q, RANK / CDIMS); 128 threads = heads; thread h merges dims
 // [d0, d0 + CDIMS) of head h over the row's pieces.  Partials are stored as
-// [slot][RANK/8][H][8], so a warp's 32-byte loads per piece read 1 KB.
+// [slot][RANK/8][H] entries of 8 fp16 dims, so a warp's 16-byte loads per
+// piece read 512 B.
 constexpr int CDIMS = 8;
 
 __global__ void __launch_bounds__(128) tc_combine_kernel(const __grid_constant__ TcDecodeArgs a) {
@@ -995,19 +1009,23 @@ __global__ void __launch_bounds__(128) tc_combine_kernel(const __grid_constant__
       for (int c = c0; c <= c1; ++c) M = fmaxf(M, a.ws_ml[(slot_of(c) * 2) * HEADS + h]);
       for (int c = c0; c <= c1; c += 4) {
         float wc[4], x[4][CDIMS];
+        uint4 raw[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           wc[q] = 0.f;
+          raw[q] = make_uint4(0, 0, 0, 0);
           if (c + q <= c1) {
             const int64_t sl = slot_of(c + q);
             const float mc = a.ws_ml[(sl * 2) * HEADS + h];
             if (mc != -CUDART_INF_F) {
-              wc[q] = exp2f(mc - M);
-              L += wc[q] * a.ws_ml[(sl * 2 + 1) * HEADS + h];
+              wc[q] = exp2f(mc - M) * a.ws_ml[(sl * 2 + 1) * HEADS + h];   // the piece's weight e^(m-M) l
+              L += wc[q];
             }
-            ld_global_v8(a.ws_o + ((sl * (RANK / 8) + d0 / 8) * HEADS + h) * 8, x[q]);
+            raw[q] = ld_partial(a.ws_o + (sl * (RANK / 8) + d0 / 8) * HEADS + h);
           }
         }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) unpack_partial(raw[q], x[q]);
 #pragma unroll
         for (int q = 0; q < 4; ++q)
 #pragma unroll
@@ -1056,7 +1074,24 @@ constexpr int PROJ_BOX_BYTES = 128 * 128;                  // [128 v rows][64 di
 constexpr int PROJ_MERGE_BYTES = PROJ_THREADS * 10 * 4;    // per thread (M, L, acc[8])
 constexpr int PROJ_SMEM_MAX = 1024 + 8 * PROJ_BOX_BYTES + 8 * 64 * 128 + PROJ_MERGE_BYTES;
 
-// Online merge of one split piece (m, l, O[8 dims]) into a running (M, L, acc).
+// Online merge of one stored split piece (m, l, O / l [8 dims]) into a running (M, L, acc).
+__device__ __forceinline__ void merge_stored_piece(float& M, float& L, float (&acc)[8], float m, float l,
+                                                   const float (&xn)[8]) {
+  if (m == -CUDART_INF_F) return;       // an empty piece (weight 0; its context was never written)
+  if (m > M) {
+    const float f = exp2f(M - m);       // 0 while M is still -inf
+    L *= f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] *= f;
+    M = m;
+  }
+  const float w = exp2f(m - M) * l;
+  L += w;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = fmaf(w, xn[j], acc[j]);
+}
+
+// Online merge of one running state (m, l, O[8 dims], O unnormalised) into another (M, L, acc).
 __device__ __forceinline__ void merge_piece(float& M, float& L, float (&acc)[8], float m, float l,
                                             const float (&x)[8]) {
   if (m == -CUDART_INF_F) return;       // an empty piece (weight 0; its O was never written)
@@ -1131,7 +1166,7 @@ __global__ void __launch_bounds__(PROJ_THREADS) tc_combine_project_kernel(const 
       for (int c = c0 + lane; c <= c1; c += 32) {
         const int64_t sl = ((int64_t)u + c) * a.width + member;
         prefetch_l2(a.ws_ml + sl * 2 * HEADS + h);
-        prefetch_l2(a.ws_o + sl * RANK * HEADS);
+        prefetch_l2(a.ws_o + sl * (RANK / 8) * HEADS);
       }
     }
   }
@@ -1175,20 +1210,26 @@ __global__ void __launch_bounds__(PROJ_THREADS) tc_combine_project_kernel(const 
       for (int j = 0; j < 8; ++j) acc[j] = 0.f;
       if (kind == 3) {
         for (int c = c0 + rsub; c <= c1; c += PROJ_UNROLL * nsplit) {
-          float mq[PROJ_UNROLL], lq[PROJ_UNROLL], x[PROJ_UNROLL][8];
+          float mq[PROJ_UNROLL], lq[PROJ_UNROLL];
+          uint4 raw[PROJ_UNROLL];
 #pragma unroll
           for (int q = 0; q < PROJ_UNROLL; ++q) {
             mq[q] = -CUDART_INF_F;
+            raw[q] = make_uint4(0, 0, 0, 0);
             const int cq = c + q * nsplit;
             if (cq <= c1) {
               const int64_t sl = ((int64_t)u + cq) * a.width + member;
               mq[q] = a.ws_ml[(sl * 2) * HEADS + h];
               lq[q] = a.ws_ml[(sl * 2 + 1) * HEADS + h];
-              ld_global_v8(a.ws_o + ((sl * (RANK / 8) + g) * HEADS + h) * 8, x[q]);
+              raw[q] = ld_partial(a.ws_o + (sl * (RANK / 8) + g) * HEADS + h);
             }
           }
 #pragma unroll
-          for (int q = 0; q < PROJ_UNROLL; ++q) merge_piece(M, L, acc, mq[q], lq[q], x[q]);
+          for (int q = 0; q < PROJ_UNROLL; ++q) {
+            float x[8];
+            unpack_partial(raw[q], x);
+            merge_stored_piece(M, L, acc, mq[q], lq[q], x);
+          }
         }
       }
       if (nsplit > 1) {   // uniform over the block: every thread reaches both barriers
@@ -1300,7 +1341,7 @@ int tc_decode_clusters() { return device_sm_count() / 2; }
 size_t tc_decode_workspace(int32_t n_q) {
   const size_t slots = (size_t)n_q + tc_decode_clusters();
   return align256((size_t)(n_q + 1) * 4) + align256((size_t)n_q * 4) +
-         align256(slots * HEADS * RANK * 4) + align256(slots * HEADS * 2 * 4);
+         align256(slots * HEADS * RANK * 2) + align256(slots * HEADS * 2 * 4);
 }
 
 cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* workspace, size_t workspace_bytes,
@@ -1341,8 +1382,8 @@ cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* works
   a.keys = reinterpret_cast<int32_t*>(ws + off);
   off += align256((size_t)n_q * 4);
   const size_t slots = (size_t)n_q + nclusters;
-  a.ws_o = reinterpret_cast<float*>(ws + off);
-  off += align256(slots * HEADS * RANK * 4);
+  a.ws_o = reinterpret_cast<uint4*>(ws + off);
+  off += align256(slots * HEADS * RANK * 2);
   a.ws_ml = reinterpret_cast<float*>(ws + off);
   a.num_clusters = nclusters;
   // A dense multi-token verify serves each batch row's tokens with a group of

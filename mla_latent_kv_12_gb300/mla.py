@@ -21,6 +21,7 @@ DEVICE_INDEX_OUT_OF_RANGE = 1 << 4
 DEVICE_TIMEOUT = 1 << 5
 DEVICE_LAYOUT = 1 << 6
 DEVICE_SCORE_RANGE = 1 << 7
+DEVICE_VALUE_RANGE = 1 << 8
 FP16_SCORE_LIMIT = 256.0
 
 _DT = {torch.float32: F32, torch.bfloat16: BF16}
