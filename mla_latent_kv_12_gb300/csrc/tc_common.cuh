@@ -146,6 +146,45 @@ __device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t count, bool 
 
 // 2^x on the special-function unit (PTX ex2.approx; relative error ~2^-22,
 // +0 for -inf).
+// f32(h) + c for the low / high fp16 half h of `w` (the conversion is exact;
+// one f32 rounding).
+__device__ __forceinline__ float add_f16lo(uint32_t w, float c) {
+  float d;
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n add.rn.f32.f16 %0, lo, %2;\n}" : "=f"(d) : "r"(w), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float add_f16hi(uint32_t w, float c) {
+  float d;
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n add.rn.f32.f16 %0, hi, %2;\n}" : "=f"(d) : "r"(w), "f"(c));
+  return d;
+}
+// (a0 * b0, a1 * b1) as one packed f32x2 multiplication.
+__device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b) {
+  uint64_t x, y, r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(r));
+  return d;
+}
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// (a0 + b0, a1 + b1) as one packed f32x2 addition.
+__device__ __forceinline__ float2 add_f32x2(float2 a, float2 b) {
+  uint64_t x, y, r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(r));
+  return d;
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

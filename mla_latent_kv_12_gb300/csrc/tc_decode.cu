@@ -302,7 +302,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
   __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES];
   __shared__ __align__(8) uint64_t s_full, s_free, p_full, pv_done, q_full, o_free, mma_drain, pv_drain;
-  __shared__ __align__(8) uint64_t x_full[2], x_free[2], xo_full[2], xo_free[2];  // per exchange buffer
+  __shared__ __align__(8) uint64_t x_full[2], x_free[2], xo_free[2];  // per exchange buffer
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
   __shared__ int32_t plan_keys_s[kMaxRowsInKernelPlan];
@@ -337,9 +337,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     mbar_init(&q_full, 4);      // the exchange warps have written this segment's query into TMEM
     mbar_init(&o_free, 4);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&x_full[b], 1);   // local expect_tx arrival + the peer's remote-store bytes
+      mbar_init(&x_full[b], 4);   // our exchange warps have staged xout[b] (one arrival carries the
+                                  // expected bytes) + the peer's remote-store bytes into xin[b]
       mbar_init(&x_free[b], 4);   // the peer's softmax warps have read xin[b] (so our copy is done)
-      mbar_init(&xo_full[b], 4);  // our exchange warps have staged xout[b]
       mbar_init(&xo_free[b], 4);  // our softmax warps have read xout[b]
     }
     mbar_init(&mma_drain, 1);
@@ -700,19 +700,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const int k = 8 * c + 2 * q;   // scores k, k+1
             const float lo_raw = __uint_as_float(k < 32 ? sa[k] : sb[k - 32]);
             const float hi_raw = __uint_as_float(k < 32 ? sa[k + 1] : sb[k - 31]);
-            half_max = fmaxf(half_max, fmaxf(fabsf(lo_raw), fabsf(hi_raw)));
-            const float lo = fminf(fmaxf(lo_raw, -65504.f), 65504.f);
-            const float hi = fminf(fmaxf(hi_raw, -65504.f), 65504.f);
-            const __half2 hv = __floats2half2_rn(lo, hi);
+            half_max = fmax3(half_max, fabsf(lo_raw), fabsf(hi_raw));
+            // sent already scaled (log2 units): the softmax then only adds
+            const float2 sc = mul_f32x2(make_float2(lo_raw, hi_raw), make_float2(a.scale_log2, a.scale_log2));
+            const __half2 hv = __floats2half2_rn(fminf(fmaxf(sc.x, -65504.f), 65504.f), fminf(fmaxf(sc.y, -65504.f), 65504.f));
             w[q] = *reinterpret_cast<const uint32_t*>(&hv);
           }
           *reinterpret_cast<uint4*>(xo + (c * 128 + h) * 16) = make_uint4(w[0], w[1], w[2], w[3]);
           st_async_v4(xi + (uint32_t)((c * 128 + h) * 16), w[0], w[1], w[2], w[3], x_full_peer[b]);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&xo_full[b]);
-        // Our receive buffer b expects the peer's XH_BYTES for this tile.
-        if (issuer) mbar_arrive_expect_tx_u32(smem_u32(&x_full[b]), XH_BYTES);
+        // xout[b] is written by this warp; receive buffer b expects the peer's
+        // XH_BYTES for this tile (announced by one of the four arrivals).
+        if (issuer)
+          mbar_arrive_expect_tx_u32(smem_u32(&x_full[b]), XH_BYTES);
+        else if (lane == 0)
+          mbar_arrive(&x_full[b]);
         ++tile;
       }
     }
@@ -750,9 +753,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       float m_used = -CUDART_INF_F, l = 0.f;
       bool first_tile = true;
       for (int t = t0; t < t1; ++t) {
-        // ---- validity of this tile's 64 entries (lane L: entries L, L+32)
-        uint64_t valid;
-        {
+        // ---- validity of this tile's 64 entries (lane L: entries L, L+32);
+        // a whole tile of a dense row needs no check (warp-uniform test)
+        uint64_t valid = ~0ull;
+        if (list != nullptr || (t + 1) * BN > keys) {
           const int e0 = t * BN + lane, e1 = e0 + 32;
           bool v0 = e0 < keys, v1 = e1 < keys;
           if (list) {
@@ -761,15 +765,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           }
           valid = (uint64_t)__ballot_sync(0xffffffffu, v0) | ((uint64_t)__ballot_sync(0xffffffffu, v1) << 32);
         }
-        // ---- scores: own and peer fp16 partials, summed in the same order-free
-        // way in both CTAs (fp32 addition of the same two values)
+        // ---- both halves present: our own (staged by the exchange warps) and
+        // the peer's (its remote stores complete as transaction bytes on this
+        // local barrier, which makes them visible to the threads that observe
+        // the phase: a CTA-scope acquire, as for a TMA load)
         const uint32_t b = tile & 1u, use = tile >> 1;
-        if (!mbar_wait_warp(&xo_full[b], use & 1u, kWaitLimit)) { fail(); break; }
-        // The peer's bulk copy completes as transaction bytes on this local
-        // barrier, which makes the data visible to the threads that observe the
-        // phase: a CTA-scope acquire, as for a TMA load.
         if (!mbar_wait_warp(&x_full[b], use & 1u, kWaitLimit)) { fail(); break; }
-        float s[BN];
+        // ---- x = own + peer - m_ref in the log2 domain (both halves arrive
+        // already scaled), as two fp16-operand additions per score (exact
+        // conversions, f32 arithmetic), relative to the running maximum m_ref
+        // (0 before any entry was seen).
+        // The two CTAs of a pair may round x differently (they take the halves
+        // in opposite order); each normalises its own half of the context by
+        // its own sum, so the results stay consistent.
+        const float m_ref = (m_used == -CUDART_INF_F) ? 0.f : m_used;
+        float x[BN];
         {
           const uint8_t* xo = xout + b * XH_BYTES;
           const uint8_t* xi = xin + b * XH_BYTES;
@@ -780,28 +790,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w}, iw[4] = {i4.x, i4.y, i4.z, i4.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const float2 of = __half22float2(*reinterpret_cast<const __half2*>(&ow[q]));
-              const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&iw[q]));
-              s[8 * c + 2 * q] = of.x + pf.x;
-              s[8 * c + 2 * q + 1] = of.y + pf.y;
+              x[8 * c + 2 * q] = add_f16lo(iw[q], add_f16lo(ow[q], -m_ref));
+              x[8 * c + 2 * q + 1] = add_f16hi(iw[q], add_f16hi(ow[q], -m_ref));
             }
           }
         }
-        // ---- online softmax (log2 domain) with lazy rescaling.  The scale is
-        // positive, so the row maximum is taken on raw scores and scaled once;
-        // each probability is ex2(fma(s, scale, -m)).  Independent partial
-        // maxima / sums keep the dependency chains short.
         if (valid != ~0ull) {
 #pragma unroll
-          for (int k = 0; k < BN; ++k) s[k] = ((valid >> k) & 1ull) ? s[k] : -CUDART_INF_F;
+          for (int k = 0; k < BN; ++k) x[k] = ((valid >> k) & 1ull) ? x[k] : -CUDART_INF_F;
         }
-        float mx8[8];
+        // ---- tile maximum (three-input max tree), relative to m_ref
+        float mx;
+        {
+          float m21[22];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = s[k];
+          for (int k = 0; k < 21; ++k) m21[k] = fmax3(x[3 * k], x[3 * k + 1], x[3 * k + 2]);
+          m21[21] = x[63];
+          float m7[8];
 #pragma unroll
-        for (int k = 8; k < BN; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], s[k]);
-        const float mx = a.scale_log2 * fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+          for (int k = 0; k < 7; ++k) m7[k] = fmax3(m21[3 * k], m21[3 * k + 1], m21[3 * k + 2]);
+          m7[7] = m21[21];
+          mx = fmax3(fmax3(m7[0], m7[1], m7[2]), fmax3(m7[3], m7[4], m7[5]), fmaxf(m7[6], m7[7]));
+        }
         // Every score above fed mx, so the warp holds all of this tile's send
         // and receive data: free both buffers with relaxed arrives ordered by
         // that dependency (a release arrive costs a cluster-scope fence per tile).
@@ -810,32 +820,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           mbar_arrive_relaxed_dep(&xo_free[b], __float_as_uint(mx));
           mbar_arrive_remote_relaxed_dep(x_free_peer[b], __float_as_uint(mx));
         }
-        float alpha = 1.f;
+        // ---- online softmax with lazy rescaling: the reference moves only
+        // when the tile maximum exceeds it by more than the threshold (or on
+        // the first visible entry); p = 2^(x - shift).
+        float alpha = 1.f, shift = 0.f;
         bool rescale = false;
-        if (mx > m_used + kRescaleThreshold || m_used == -CUDART_INF_F) {
-          const float m_new = fmaxf(m_used, mx);
-          if (m_new != m_used) {
-            alpha = (m_used == -CUDART_INF_F) ? 0.f : ex2_approx(m_used - m_new);
-            rescale = !first_tile && m_used != -CUDART_INF_F;
-            m_used = m_new;
-          }
+        if (mx != -CUDART_INF_F && (mx > kRescaleThreshold || m_used == -CUDART_INF_F)) {
+          alpha = (m_used == -CUDART_INF_F) ? 0.f : ex2_approx(-mx);
+          rescale = !first_tile && m_used != -CUDART_INF_F;
+          m_used = m_ref + mx;
+          shift = mx;
         }
-        // With m_used finite, ex2(-inf) = +0 masks an entry; while no entry has
-        // been visible (m_used = -inf) every p is 0.
-        const float neg_m = (m_used == -CUDART_INF_F) ? -CUDART_INF_F : -m_used;
         uint32_t pk[32];
-        float ps8[8];
+        float2 ps2[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) ps8[k] = 0.f;
+        for (int k = 0; k < 8; ++k) ps2[k] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < BN; k += 2) {
-          const float p0 = ex2_approx(fmaf(s[k], a.scale_log2, neg_m));
-          const float p1 = ex2_approx(fmaf(s[k + 1], a.scale_log2, neg_m));
-          ps8[(k >> 1) & 7] += p0 + p1;
+          const float p0 = ex2_approx(x[k] - shift);
+          const float p1 = ex2_approx(x[k + 1] - shift);
+          ps2[(k >> 1) & 7] = add_f32x2(ps2[(k >> 1) & 7], make_float2(p0, p1));
           const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
           pk[k >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
         }
-        const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
+        ps2[0] = add_f32x2(add_f32x2(ps2[0], ps2[1]), add_f32x2(ps2[2], ps2[3]));
+        ps2[4] = add_f32x2(add_f32x2(ps2[4], ps2[5]), add_f32x2(ps2[6], ps2[7]));
+        ps2[0] = add_f32x2(ps2[0], ps2[4]);
+        const float psum = ps2[0].x + ps2[0].y;
         l = l * alpha + psum;
         // ---- P into TMEM once the previous P.V has consumed it (and O is stable)
         while (pv_seen < tile) {
