@@ -12,17 +12,18 @@
 //  * A cluster of two CTAs (an SM pair) owns one stream of work.  The f32
 //    context accumulator [128 x 512] would fill a whole SM's TMEM, so the pair
 //    splits the feature axis evenly: CTA r scores latent dims [256r, 256r+256)
-//    and rope dims [32r, 32r+32) (18 MMA K-steps each).  Each CTA rounds its
-//    partial scores to fp16 and stores them straight into the peer's shared
-//    memory with asynchronous remote stores (st.async, counted as
-//    transactions on the receiving barrier); both CTAs then add the same two fp16 partials in f32
-//    (commutative, so bit-identical), run the same online softmax, and each
-//    accumulates O[:, own 256 latent dims] += P . latent[:, own dims].  No MMA
-//    work is repeated and every latent byte is read by one CTA (the 128-byte
-//    rope row is read by both, from L2 the second time).
+//    and rope dims [32r, 32r+32) (18 MMA K-steps each).  Each CTA scales its
+//    partial scores to the log2 domain, rounds them to fp16 and stores them
+//    straight into the peer's shared memory with asynchronous remote stores
+//    (st.async, counted as transactions on the receiving barrier); each CTA
+//    then adds its own and the peer's halves in f32, runs the online softmax,
+//    and accumulates O[:, own 256 latent dims] += P . latent[:, own dims],
+//    normalised by its own sum.  No MMA work is repeated and every cache byte
+//    is read by exactly one CTA of the pair.
 //  * Q (the CTA's dims) and P live in TMEM as the MMA A operand; cache tiles
-//    are TMA-loaded (128-byte swizzle) into a 4-stage ring; one tile serves the
-//    score MMA (K-major B) and the P.V MMA (MN-major B) through two descriptors.
+//    are TMA-loaded into a 4-stage ring (latent dims with 128-byte swizzle,
+//    the CTA's rope dims with 64-byte swizzle); one tile serves the score MMA
+//    (K-major B) and the P.V MMA (MN-major B) through two descriptors.
 //  * Warp roles: warp 0 loads (TMA tiles, or TMA gather4 / cp.async row
 //    gathers for selected positions, plus L2 prefetch ahead); warp 1 issues the
 //    score MMAs; warps 6..9 read the scores from TMEM and run the exchange;
@@ -48,9 +49,13 @@ using namespace tc;
 
 constexpr int BN = 64;                    // keys per tile
 constexpr int STAGES = 4;
-constexpr int NCH = 5;                    // 64-dim chunks per stage: 4 latent + the rope row
-constexpr int CHUNK_BYTES = BN * 128;     // one [64 keys x 64 dims] bf16 box
-constexpr int STAGE_BYTES = NCH * CHUNK_BYTES;
+// A stage holds one tile of this CTA's features: four [64 keys x 64 latent
+// dims] boxes (128-byte rows, 128-byte swizzle) and its 32 rope dims
+// ([64 keys x 32 dims], 64-byte rows, 64-byte swizzle).
+constexpr int CHUNK_BYTES = BN * 128;
+constexpr int ROPE_BYTES = BN * 64;
+constexpr int STAGE_BYTES = 4 * CHUNK_BYTES + ROPE_BYTES;
+constexpr int STAGE_TX = STAGE_BYTES;     // bytes one tile's loads deliver into a stage
 constexpr int XH_BYTES = 128 * BN * 2;    // fp16 partial scores of one tile (one send / receive buffer)
 constexpr int HEADS = 128, RANK = 512, DV = 256;  // DV: latent dims per CTA
 constexpr int THREADS = 352;   // producer, score MMA, 4 softmax, 4 exchange, P.V MMA warps
@@ -313,7 +318,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
-  const int nch = NCH;                      // chunks this CTA loads per tile
   const int dim_base = 256 * (int)rank;     // first latent dim of this CTA
   const int cluster = blockIdx.x >> 1;
   const int group = cluster / a.width, member = cluster % a.width;
@@ -403,25 +407,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         // the segment's first tiles that the loop's look-ahead will not cover
         for (int t = t0 + STAGES; t < t0 + kPrefetchAhead && t < t1; ++t) {
           for (int c = 0; c < 4; ++c) tma_prefetch_l2_3d(&lat_map, dim_base + 64 * c, start + t * BN, zb);
-          if (rank == 0) tma_prefetch_l2_3d(&rope_map, 0, start + t * BN, zb);
+          tma_prefetch_l2_3d(&rope_map, 32 * (int)rank, start + t * BN, zb);
         }
       }
       for (int t = t0; t < t1 && !aborted(); ++t) {
         if (fills++ >= STAGES && !mbar_wait_warp(&empty_bar[stage], phase ^ 1u, kWaitLimit)) { fail(); break; }
         if (!gather) {
           if (lane == 0) {
-            mbar_arrive_expect_tx(&full_bar[stage], nch * CHUNK_BYTES);
+            mbar_arrive_expect_tx(&full_bar[stage], STAGE_TX);
             uint8_t* dst = stages + stage * STAGE_BYTES;
             const int y = start + t * BN;
             for (int c = 0; c < 4; ++c)
               tma_load_3d(dst + c * CHUNK_BYTES, &lat_map, &full_bar[stage], dim_base + 64 * c, y, zb);
-            tma_load_3d(dst + 4 * CHUNK_BYTES, &rope_map, &full_bar[stage], 0, y, zb);
+            tma_load_3d(dst + 4 * CHUNK_BYTES, &rope_map, &full_bar[stage], 32 * (int)rank, y, zb);
             // Pull a tile a few steps ahead into L2, so that refilling a stage
             // once it frees costs an L2 rather than an HBM round trip.
             if (t + kPrefetchAhead < t1) {
               const int yp = y + kPrefetchAhead * BN;
               for (int c = 0; c < 4; ++c) tma_prefetch_l2_3d(&lat_map, dim_base + 64 * c, yp, zb);
-              if (rank == 0) tma_prefetch_l2_3d(&rope_map, 0, yp, zb);
+              tma_prefetch_l2_3d(&rope_map, 32 * (int)rank, yp, zb);
             }
           }
         } else if (a.gather_tma) {
@@ -448,14 +452,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
               rr[j] = b * a.rope_rows_per_batch + w;
             }
           }
-          if (lane == 0) mbar_arrive_expect_tx(&full_bar[stage], nch * CHUNK_BYTES);
+          if (lane == 0) mbar_arrive_expect_tx(&full_bar[stage], STAGE_TX);
           __syncwarp();
           if (lane < 16) {
-            uint8_t* dst = stages + stage * STAGE_BYTES + lane * 4 * 128;
+            uint8_t* dst = stages + stage * STAGE_BYTES;
             for (int c = 0; c < 4; ++c)
-              tma_gather4(dst + c * CHUNK_BYTES, &lat_rows_map, &full_bar[stage], dim_base + 64 * c, lr[0], lr[1],
-                          lr[2], lr[3]);
-            tma_gather4(dst + 4 * CHUNK_BYTES, &rope_rows_map, &full_bar[stage], 0, rr[0], rr[1], rr[2], rr[3]);
+              tma_gather4(dst + c * CHUNK_BYTES + lane * 4 * 128, &lat_rows_map, &full_bar[stage], dim_base + 64 * c,
+                          lr[0], lr[1], lr[2], lr[3]);
+            tma_gather4(dst + 4 * CHUNK_BYTES + lane * 4 * 64, &rope_rows_map, &full_bar[stage], 32 * (int)rank,
+                        rr[0], rr[1], rr[2], rr[3]);
           }
         } else {
           // Row gather: lane L owns keys L and L+32 of the tile.
@@ -478,11 +483,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const bool vr = __shfl_sync(0xffffffffu, r < 32 ? v0 : v1, src_lane);
             const int64_t row = (int64_t)start + (vr ? pr : 0);
             const __nv_bfloat16* lrow = a.latent + lat_b + row * a.latent_row_stride + dim_base;
-            const __nv_bfloat16* rrow = a.rope + rope_b + row * a.rope_row_stride;
-            for (int q16 = lane; q16 < nch * 8; q16 += 32) {
-              const int c = q16 >> 3, uu = q16 & 7;
-              const __nv_bfloat16* src = (c < 4) ? lrow + c * 64 + uu * 8 : rrow + uu * 8;
-              const uint32_t dst = dst0 + c * CHUNK_BYTES + r * 128 + ((uu ^ (r & 7)) << 4);
+            const __nv_bfloat16* rrow = a.rope + rope_b + row * a.rope_row_stride + 32 * (int)rank;
+            // 32 16-byte pieces of the latent dims (128-byte swizzle: piece u
+            // of row r at u ^ (r % 8)), then 4 of the rope dims (64-byte
+            // swizzle: piece u of row r at u ^ ((r / 2) % 4))
+            for (int q16 = lane; q16 < 36; q16 += 32) {
+              const __nv_bfloat16* src;
+              uint32_t dst;
+              if (q16 < 32) {
+                const int c = q16 >> 3, uu = q16 & 7;
+                src = lrow + c * 64 + uu * 8;
+                dst = dst0 + c * CHUNK_BYTES + r * 128 + ((uu ^ (r & 7)) << 4);
+              } else {
+                const int uu = q16 - 32;
+                src = rrow + uu * 8;
+                dst = dst0 + 4 * CHUNK_BYTES + r * 64 + ((uu ^ ((r >> 1) & 3)) << 4);
+              }
               cp_async_16(dst, src, vr ? 16u : 0u);
             }
           }
@@ -535,7 +551,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         // offsets (a lane-0 branch with per-MMA descriptor arithmetic issues
         // the N=64 MMAs at about half the rate).
         const uint64_t d0 = smem_desc(smem_u32(stages + stage * STAGE_BYTES), 16, 1024, kSwizzle128B);
-        const uint64_t d_rope = d0 + (uint64_t)((4 * CHUNK_BYTES + 2 * (int)rank * 32) >> 4);
+        // this CTA's 32 rope dims: 64-byte rows, 8-row groups 512 bytes apart
+        const uint64_t d_rope =
+            smem_desc(smem_u32(stages + stage * STAGE_BYTES + 4 * CHUNK_BYTES), 16, 512, kSwizzle64B);
         if (elect_one()) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
@@ -1423,8 +1441,9 @@ cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* works
     const uint64_t bstride = a.batch_in_map ? (uint64_t)g.rope_batch_stride * 2
                                             : (uint64_t)g.t_max * g.rope_row_stride * 2;
     const uint64_t strides[2] = {(uint64_t)g.rope_row_stride * 2, bstride};
-    const uint32_t box[3] = {64, BN, 1};
-    if (!encode_tmap_bf16(&rope_map, g.rope, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    const uint32_t box[3] = {32, BN, 1};   // one CTA's 32 rope dims: 64-byte rows
+    if (!encode_tmap_bf16(&rope_map, g.rope, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
   }
   // Row maps for gathers: the cache as [rows, dims] with one-row boxes; a
   // batch row's rows start at b * (batch stride / row stride).
@@ -1439,9 +1458,9 @@ cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* works
     const uint64_t rrows = (uint64_t)(a.batch_in_map ? g.batch - 1 : 0) * a.rope_rows_per_batch + g.t_max;
     const uint64_t ld[2] = {(uint64_t)g.rank, lrows}, rd[2] = {(uint64_t)g.rope_dim, rrows};
     const uint64_t ls[1] = {(uint64_t)g.latent_row_stride * 2}, rs[1] = {(uint64_t)g.rope_row_stride * 2};
-    const uint32_t box[2] = {64, 1};
+    const uint32_t box[2] = {64, 1}, rbox[2] = {32, 1};
     if (lrows < (1ull << 31) && rrows < (1ull << 31) && encode_tmap_bf16(&lat_rows_map, g.latent, 2, ld, ls, box) &&
-        encode_tmap_bf16(&rope_rows_map, g.rope, 2, rd, rs, box))
+        encode_tmap_bf16(&rope_rows_map, g.rope, 2, rd, rs, rbox, CU_TENSOR_MAP_SWIZZLE_64B))
       a.gather_tma = 1;
   }
   {

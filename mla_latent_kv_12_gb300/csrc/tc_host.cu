@@ -37,7 +37,7 @@ cudaError_t set_max_dynamic_smem(const void* kernel, int bytes) {
 }
 
 bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                      const uint64_t* strides_bytes, const uint32_t* box) {
+                      const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle) {
   auto fn = encode_fn();
   if (!fn) {
     set_error_detail("cuTensorMapEncodeTiled is not available from the driver");
@@ -53,7 +53,7 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64
   }
   for (int i = 0; i + 1 < rank; ++i) gstride[i] = strides_bytes[i];
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), gdim,
-                  gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     set_error_detail("cuTensorMapEncodeTiled failed (%d)", (int)r);

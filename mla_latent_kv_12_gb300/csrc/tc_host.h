@@ -10,11 +10,13 @@
 
 namespace mla {
 
-// Encodes a bf16 tensor map of rank 2 or 3 with 128-byte swizzle.
-// dims[0] is the contiguous axis; strides_bytes[i] is the byte stride of
-// dims[i+1].  Returns false (and sets the error detail) on failure.
+// Encodes a bf16 tensor map of rank 2 or 3 with 128-byte swizzle (or the
+// given swizzle).  dims[0] is the contiguous axis; strides_bytes[i] is the
+// byte stride of dims[i+1].  Returns false (and sets the error detail) on
+// failure.
 bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                      const uint64_t* strides_bytes, const uint32_t* box);
+                      const uint64_t* strides_bytes, const uint32_t* box,
+                      CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B);
 
 // Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
 // device, once per (kernel, device); thread-safe.  Returns the CUDA error of
