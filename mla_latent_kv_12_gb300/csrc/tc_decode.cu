@@ -70,6 +70,7 @@ constexpr float kRescaleThreshold = 8.0f;    // log2 units
 // partial, worth it only against a few 72 KB tiles of cache read.
 constexpr int kMinTilesPerGroup = 4;
 constexpr int kPrefetchAhead = 6;    // tiles of the current row pulled into L2 ahead of their load
+constexpr int kQueryPrefetchTiles = 4;   // the next segment's query is pulled into L2 this many tiles before
 // Up to this many query rows, every CTA plans the split itself in its prologue
 // (no planner launch); larger batches use the planner kernel.
 constexpr int kMaxRowsInKernelPlan = 128;
@@ -670,23 +671,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&q_full);
-        // The next segment's query row into L2 (this head's 512 + 64 bytes),
-        // so that loading it at the next boundary is an L2 hit.
-        WorkIter peek = it;
-        int un, nn, tn0, tn1;
-        bool wn;
-        while (peek.next(un, tn0, tn1, wn)) {
-          if (!member_segment(a, keys_p, un, member, nn, tn0, tn1)) continue;
-          if (real) {
-            const __nv_bfloat16* qnext = a.q + (int64_t)nn * a.q_row_stride + (int64_t)h * a.q_head_stride;
-#pragma unroll
-            for (int l = 0; l < 4; ++l) prefetch_l2(qnext + dim_base + 64 * l);
-            prefetch_l2(qnext + RANK + 32 * (int)rank);
-          }
-          break;
-        }
       }
+      // A few tiles before this segment ends, the next segment's query row
+      // (this head's 512 + 64 bytes) is pulled into L2 -- and its address
+      // translation warmed -- so that loading it at the boundary is an L2 hit.
+      // Earlier would not do: the cache tiles streamed meanwhile evict it.
+      const int t_pf = t1 - kQueryPrefetchTiles > t0 ? t1 - kQueryPrefetchTiles : t0;
       for (int t = t0; t < t1; ++t) {
+        if (t == t_pf) {
+          WorkIter peek = it;
+          int un, nn, tn0, tn1;
+          bool wn;
+          while (peek.next(un, tn0, tn1, wn)) {
+            if (!member_segment(a, keys_p, un, member, nn, tn0, tn1)) continue;
+            if (h < a.heads) {
+              const __nv_bfloat16* qnext = a.q + (int64_t)nn * a.q_row_stride + (int64_t)h * a.q_head_stride;
+#pragma unroll
+              for (int l = 0; l < 4; ++l) prefetch_l2(qnext + dim_base + 64 * l);
+              prefetch_l2(qnext + RANK + 32 * (int)rank);
+            }
+            break;
+          }
+        }
         const uint32_t b = tile & 1u, use = tile >> 1;
         if (tile >= 2) {
           // the peer has read our copy of tile-2 (so xout[b] is read too), and
