@@ -109,6 +109,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_u32(uint32_t bar, uint32_t
 
 // 16-byte store into another CTA's shared memory that completes as `bytes`
 // transactions on that CTA's barrier (both addresses shared::cluster).
+// 16-bit shared-memory store (a compiler barrier: later plain loads of the
+// same bytes are not moved above it)
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
 __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w,
                                             uint32_t remote_bar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"

@@ -69,6 +69,17 @@ constexpr float kRescaleThreshold = 8.0f;    // log2 units
 // A group's tile range is at least this long: each split writes a 256 KB f32
 // partial, worth it only against a few 72 KB tiles of cache read.
 constexpr int kMinTilesPerGroup = 4;
+// Each work unit with tiles is charged this many tiles' worth of time for
+// its start: a segment boundary drains the pair's pipeline (the next query
+// enters TMEM only once the previous segment's last scores are read, then
+// its first scores and exchange run before the softmax resumes), which costs
+// several tiles of streaming.  The charge sits in the split plan ahead of the
+// unit's tiles, so a group whose range holds more unit starts gets fewer
+// tiles.  It applies when the groups stream at least kChargeMinSpan tiles
+// each: with a few tiles per group (a short or selected-position batch) every
+// group pays one start anyway, and a charge would only idle groups.
+constexpr int kUnitStartCharge = 10;
+constexpr int kChargeMinSpan = 32;
 constexpr int kPrefetchAhead = 6;    // tiles of the current row pulled into L2 ahead of their load
 constexpr int kQueryPrefetchTiles = 4;   // the next segment's query is pulled into L2 this many tiles before
 // Up to this many query rows, every CTA plans the split itself in its prologue
@@ -95,7 +106,7 @@ struct TcDecodeArgs {
   int32_t out_f32;
   float* lse;
   int32_t* status;
-  int32_t* prefix;     // [n_units + 1] tile prefix over work units (planner)
+  int32_t* prefix;     // [n_units + 2] the split plan: prefix over work units, then the start charge
   int32_t* keys;       // [n_q] visible entries per query row (planner)
   uint4* ws_o;         // [slots][RANK/8][H] partial context, 8 fp16 dims per entry (O / l of the piece)
   float* ws_ml;        // [slots][2][H] partial (m, l), log2 domain
@@ -129,17 +140,28 @@ __device__ __forceinline__ int row_limit(const TcDecodeArgs& a, int n) {
 // read each cache tile at the same time and three of four reads hit L2.
 // The units' tiles form one flattened sequence cut into equal ranges, one per
 // group (at least `min_tiles` each, so a short sequence uses fewer groups).
+// In that sequence each unit with tiles occupies charge + tiles positions,
+// its tiles at the end: prefix[0..n_units] holds these extents' exclusive
+// prefix and prefix[n_units + 1] the charge, so unit u's tile j sits at
+// position prefix[u] + charge + j.
 __device__ __forceinline__ int group_span(const TcDecodeArgs& a, int total) {
   const int ngroups = a.num_clusters / a.width;
   const int per = (total + ngroups - 1) / ngroups;
   return per > a.min_tiles ? per : a.min_tiles;
 }
 
+// The start charge of a plan whose units hold `raw` tiles in all.
+__device__ __forceinline__ int unit_start_charge(const TcDecodeArgs& a, int raw) {
+  const int ngroups = a.num_clusters / a.width;
+  return (raw + ngroups - 1) / ngroups >= kChargeMinSpan ? kUnitStartCharge : 0;
+}
+
 struct WorkIter {
   const int32_t* prefix;
-  int n, t, t_begin, t_end;
+  int n, t, t_begin, t_end, charge;
   __device__ void init(const TcDecodeArgs& a, const int32_t* unit_prefix, int group) {
     prefix = unit_prefix;
+    charge = prefix[a.n_units + 1];
     const int total = prefix[a.n_units];
     const int per = group_span(a, total);
     const int ngroups = a.num_clusters / a.width;
@@ -155,21 +177,34 @@ struct WorkIter {
     n = lo;
     t = t_begin;
   }
-  // Next segment: unit u, unit-local tiles [t0, t1); `whole` if the unit lies
-  // entirely inside this group's range.
+  // Next segment: unit u, unit-local tiles [t0, t1); `whole` if all of the
+  // unit's tiles lie inside this group's range.  A unit whose start charge
+  // alone falls in the range is no segment.
   __device__ bool next(int& u, int& t0, int& t1, bool& whole) {
-    if (t >= t_end) return false;
-    while (prefix[n + 1] <= t) ++n;
-    const int rs = prefix[n], re = prefix[n + 1];
-    const int e = min(t_end, re);
-    u = n;
-    t0 = t - rs;
-    t1 = e - rs;
-    whole = rs >= t_begin && re <= t_end;
-    t = e;
-    return true;
+    while (t < t_end) {
+      while (prefix[n + 1] <= t) ++n;
+      const int rs = prefix[n] + charge, re = prefix[n + 1];   // the unit's tiles
+      const int s = max(t, rs), e = min(t_end, re);
+      t = e;
+      if (s >= e) continue;
+      u = n;
+      t0 = s - rs;
+      t1 = e - rs;
+      whole = rs >= t_begin && re <= t_end;
+      return true;
+    }
+    return false;
   }
 };
+
+// The groups whose ranges hold unit u's tiles: [first, last] (a unit with
+// tiles; `charge` = prefix[n_units + 1]).
+__device__ __forceinline__ int first_group_of(const int32_t* prefix, int u, int per, int charge) {
+  return (prefix[u] + charge) / per;
+}
+__device__ __forceinline__ int last_group_of(const int32_t* prefix, int u, int per) {
+  return (prefix[u + 1] - 1) / per;
+}
 
 // A member's share of a unit segment: its query row n and the segment's tiles
 // clipped to that row's own tiles (a verify token sees a shorter prefix than
@@ -220,22 +255,38 @@ __device__ __forceinline__ void plan_rows(const TcDecodeArgs& a, int32_t* keys_s
   }
   __syncthreads();
   if (warp == 0) {
-    int carry = 0;
+    int tl[kMaxRowsInKernelPlan / 32];
+    int raw = 0;
+#pragma unroll
     for (int j = 0; j < kMaxRowsInKernelPlan / 32; ++j) {
       const int u = 32 * j + lane;
       int tiles = 0;
       if (u < a.n_units)
         for (int i = 0; i < a.width; ++i) tiles = max(tiles, (keys_s[u * a.width + i] + BN - 1) / BN);
-      int v = tiles;
+      tl[j] = tiles;
+      raw += tiles;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) raw += __shfl_xor_sync(0xffffffffu, raw, o);
+    const int charge = unit_start_charge(a, raw);
+    int carry = 0;
+#pragma unroll
+    for (int j = 0; j < kMaxRowsInKernelPlan / 32; ++j) {
+      const int u = 32 * j + lane;
+      const int ext = tl[j] > 0 ? tl[j] + charge : 0;   // the unit's extent in the plan
+      int v = ext;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int x = __shfl_up_sync(0xffffffffu, v, o);
         if (lane >= o) v += x;
       }
-      if (u < a.n_units) prefix_s[u] = carry + v - tiles;
+      if (u < a.n_units) prefix_s[u] = carry + v - ext;
       carry += __shfl_sync(0xffffffffu, v, 31);
     }
-    if (lane == 0) prefix_s[a.n_units] = carry;
+    if (lane == 0) {
+      prefix_s[a.n_units] = carry;
+      prefix_s[a.n_units + 1] = charge;
+    }
   }
   __syncthreads();
 }
@@ -243,23 +294,42 @@ __device__ __forceinline__ void plan_rows(const TcDecodeArgs& a, int32_t* keys_s
 __global__ void __launch_bounds__(1024) tc_plan_kernel(const __grid_constant__ TcDecodeArgs a) {
   pdl_wait();
   __shared__ int warp_sums[32];
-  __shared__ int carry_s;
-  if (threadIdx.x == 0) carry_s = 0;
+  __shared__ int carry_s, raw_s;
+  if (threadIdx.x == 0) carry_s = 0, raw_s = 0;
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // pass 1: visible entries per row (stored) and the units' tiles in all
+  int raw = 0;
+  for (int u = threadIdx.x; u < a.n_units; u += 1024) {
+    int tiles = 0;
+    for (int i = 0; i < a.width; ++i) {
+      const int n = u * a.width + i;
+      const int keys = row_keys(a, n, true);
+      a.keys[n] = keys;
+      const int t = (keys + BN - 1) / BN;
+      tiles = t > tiles ? t : tiles;
+    }
+    raw += tiles;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) raw += __shfl_xor_sync(0xffffffffu, raw, o);
+  if (lane == 0) atomicAdd(&raw_s, raw);
+  __syncthreads();
+  const int charge = unit_start_charge(a, raw_s);
+  // pass 2: the units' extents (each thread rereads the rows it stored) and
+  // their exclusive prefix
   for (int base = 0; base < a.n_units; base += 1024) {
     const int u = base + threadIdx.x;
-    int tiles = 0;
+    int ext = 0;
     if (u < a.n_units) {
+      int tiles = 0;
       for (int i = 0; i < a.width; ++i) {
-        const int n = u * a.width + i;
-        const int keys = row_keys(a, n, true);
-        a.keys[n] = keys;
-        const int t = (keys + BN - 1) / BN;
+        const int t = (a.keys[u * a.width + i] + BN - 1) / BN;
         tiles = t > tiles ? t : tiles;
       }
+      ext = tiles > 0 ? tiles + charge : 0;
     }
-    int v = tiles;
+    int v = ext;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int x = __shfl_up_sync(0xffffffffu, v, o);
@@ -277,13 +347,16 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const __grid_constant__ T
       warp_sums[lane] = w;
     }
     __syncthreads();
-    const int excl = carry_s + (warp ? warp_sums[warp - 1] : 0) + v - tiles;
+    const int excl = carry_s + (warp ? warp_sums[warp - 1] : 0) + v - ext;
     if (u < a.n_units) a.prefix[u] = excl;
     __syncthreads();
-    if (threadIdx.x == 1023) carry_s = excl + tiles;
+    if (threadIdx.x == 1023) carry_s = excl + ext;
     __syncthreads();
   }
-  if (threadIdx.x == 0) a.prefix[a.n_units] = carry_s;
+  if (threadIdx.x == 0) {
+    a.prefix[a.n_units] = carry_s;
+    a.prefix[a.n_units + 1] = charge;
+  }
   pdl_trigger();
 }
 
@@ -312,7 +385,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
   __shared__ int32_t plan_keys_s[kMaxRowsInKernelPlan];
-  __shared__ int32_t plan_prefix_s[kMaxRowsInKernelPlan + 1];
+  __shared__ int32_t plan_prefix_s[kMaxRowsInKernelPlan + 2];
   __shared__ int32_t row_start_s[kMaxRowsInKernelPlan], row_limit_s[kMaxRowsInKernelPlan];
   auto aborted = [&]() -> bool { return __any_sync(0xffffffffu, abort_s != 0); };
 
@@ -374,7 +447,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     prefix_p = plan_prefix_s;
     if (blockIdx.x == 0) {   // the combine kernel reads the plan from the workspace
       for (int i = threadIdx.x; i < a.n_q; i += THREADS) a.keys[i] = plan_keys_s[i];
-      for (int i = threadIdx.x; i <= a.n_units; i += THREADS) a.prefix[i] = plan_prefix_s[i];
+      for (int i = threadIdx.x; i <= a.n_units + 1; i += THREADS) a.prefix[i] = plan_prefix_s[i];
     }
   }
   WorkIter it;
@@ -803,6 +876,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         // in opposite order); each normalises its own half of the context by
         // its own sum, so the results stay consistent.
         const float m_ref = (m_used == -CUDART_INF_F) ? 0.f : m_used;
+        if (valid != ~0ull) {
+          // Entries past the window or out of range: this head's own half in
+          // xout[b] becomes fp16 -inf, so that x = -inf whatever the peer's
+          // (finite) half.  A rolled loop with computed addresses: it runs at a
+          // row's last tile only, where an unrolled masking pass would be
+          // fetched cold into the instruction cache.
+          const uint32_t row = smem_u32(xout + b * XH_BYTES) + (uint32_t)h * 16u;
+          uint64_t inv = ~valid;
+#pragma unroll 1
+          while (inv != 0ull) {
+            const int k = __ffsll((long long)inv) - 1;
+            inv &= inv - 1ull;
+            st_shared_u16(row + (uint32_t)((k >> 3) * 128 * 16 + (k & 7) * 2), 0xFC00u);
+          }
+        }
         float x[BN];
         {
           const uint8_t* xo = xout + b * XH_BYTES;
@@ -818,10 +906,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
               x[8 * c + 2 * q + 1] = add_f16hi(iw[q], add_f16hi(ow[q], -m_ref));
             }
           }
-        }
-        if (valid != ~0ull) {
-#pragma unroll
-          for (int k = 0; k < BN; ++k) x[k] = ((valid >> k) & 1ull) ? x[k] : -CUDART_INF_F;
         }
         // ---- tile maximum (three-input max tree), relative to m_ref
         float mx;
@@ -883,6 +967,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         // rescale pass when any of its heads needs it, the others with factor 1.
         if (__any_sync(0xffffffffu, rescale)) {
           const float f = rescale ? alpha : 1.f;
+#pragma unroll 1
           for (int c = 0; c < DV / 32; ++c) {
             uint32_t o[32];
             tmem_ld32(tmem + TM_O + c * 32 + lane_off, o);
@@ -913,7 +998,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       auto drain_o = [&](auto&& store_chunk) {
         uint32_t oa[32], ob[32];
         tmem_ld32(tmem + TM_O + lane_off, oa);
-#pragma unroll
+        // rolled: the epilogue runs once per segment, so its code is fetched
+        // cold; four copies of the chunk stores would cost more than the loop
+#pragma unroll 1
         for (int c = 0; c < DV / 32; c += 2) {
           tmem_wait_ld_regs(oa);
           tmem_ld32(tmem + TM_O + (c + 1) * 32 + lane_off, ob);
@@ -1035,8 +1122,7 @@ __global__ void __launch_bounds__(128) tc_combine_kernel(const __grid_constant__
   bool write = true;
   if (a.keys[n] != 0) {
     const int per = group_span(a, a.prefix[a.n_units]);
-    const int rs = a.prefix[u], re = a.prefix[u + 1];
-    const int c0 = rs / per, c1 = (re - 1) / per;
+    const int c0 = first_group_of(a.prefix, u, per, a.prefix[a.n_units + 1]), c1 = last_group_of(a.prefix, u, per);
     if (c0 == c1) {
       write = false;                       // finished in place by its group
     } else {
@@ -1155,7 +1241,7 @@ __global__ void __launch_bounds__(PROJ_THREADS) tc_combine_project_kernel(const 
   __shared__ uint32_t tmem_base_s;
   __shared__ int mma_ok_s;
   __shared__ int32_t keys_s[kMaxRowsInKernelPlan];
-  __shared__ int32_t prefix_s[kMaxRowsInKernelPlan + 1];
+  __shared__ int32_t prefix_s[kMaxRowsInKernelPlan + 2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x;
   const int npad = p.npad;
@@ -1196,7 +1282,7 @@ __global__ void __launch_bounds__(PROJ_THREADS) tc_combine_project_kernel(const 
     for (int n = threadIdx.x >> 5; n < a.n_q; n += PROJ_THREADS / 32) {
       if (keys_s[n] == 0) continue;
       const int u = n / a.width, member = n % a.width;
-      const int c0 = prefix_s[u] / per, c1 = (prefix_s[u + 1] - 1) / per;
+      const int c0 = first_group_of(prefix_s, u, per, prefix_s[a.n_units + 1]), c1 = last_group_of(prefix_s, u, per);
       if (c0 == c1) continue;
       for (int c = c0 + lane; c <= c1; c += 32) {
         const int64_t sl = ((int64_t)u + c) * a.width + member;
@@ -1235,8 +1321,8 @@ __global__ void __launch_bounds__(PROJ_THREADS) tc_combine_project_kernel(const 
         if (keys_s[n] != 0) {
           u = n / a.width;
           member = n % a.width;
-          c0 = prefix_s[u] / per;
-          c1 = (prefix_s[u + 1] - 1) / per;
+          c0 = first_group_of(prefix_s, u, per, prefix_s[a.n_units + 1]);
+          c1 = last_group_of(prefix_s, u, per);
           kind = c0 == c1 ? 2 : 3;
         }
       }
@@ -1375,7 +1461,7 @@ int tc_decode_clusters() { return device_sm_count() / 2; }
 // The partials are laid out for the MMA's 128 rows whatever the head count.
 size_t tc_decode_workspace(int32_t n_q) {
   const size_t slots = (size_t)n_q + tc_decode_clusters();
-  return align256((size_t)(n_q + 1) * 4) + align256((size_t)n_q * 4) +
+  return align256((size_t)(n_q + 2) * 4) + align256((size_t)n_q * 4) +
          align256(slots * HEADS * RANK * 2) + align256(slots * HEADS * 2 * 4);
 }
 
@@ -1413,7 +1499,7 @@ cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* works
   a.status = g.device_status;
   size_t off = 0;
   a.prefix = reinterpret_cast<int32_t*>(ws + off);
-  off += align256((size_t)(n_q + 1) * 4);
+  off += align256((size_t)(n_q + 2) * 4);
   a.keys = reinterpret_cast<int32_t*>(ws + off);
   off += align256((size_t)n_q * 4);
   const size_t slots = (size_t)n_q + nclusters;

@@ -4,6 +4,8 @@
 * More than 128 query rows: the decode plans its split with a separate
   planner launch instead of in its prologue, and the projections run in
   several row blocks.
+* Long rows: the split plan charges each row start, in the prologue and in
+  the planner launch.
 * A cache whose batch stride is not a whole number of rows: selected rows
   are gathered with 16-byte cp.async loads instead of TMA gather4.
 * The fp16 exchange of the two half scores of an SM pair: the range over
@@ -109,12 +111,31 @@ def test_absorb_and_project_many_row_blocks(n_q):
 PLANNER_ROWS = [0, 1, 63, 64, 127, 128, 129, 158, 159]
 
 
+def _plan_charge(step, n_units):
+    # the decode workspace starts with the split plan: the prefix over work
+    # units, then the start charge per unit
+    return int(step.workspace[: 4 * (n_units + 2)].view(torch.int32)[n_units + 1].item())
+
+
 def test_planner_path_ragged_160_rows():
     w = dataclasses.replace(W.RAGGED_BF16, batch=160)
     inp = W.make_inputs(w, layout="flat", t_override=900)
     step = _granular_and_fused(inp, rows=PLANNER_ROWS, heads=[0, 7, 64, 127], expect_fused=False)
     assert step.attend_launches() == 3          # planner + decode + combine
     assert torch.all(torch.isfinite(step.ctx.float()))
+    assert _plan_charge(step, 160) == 0         # ~15 tiles per SM pair: no start charge
+
+
+@pytest.mark.parametrize("rows,t", [(32, 12000), (160, 6000)])
+def test_charged_split_plan_every_row(rows, t):
+    # Rows long enough that every SM pair streams 32 tiles or more: the plan
+    # charges each row start (in the decode prologue for 32 rows, in the
+    # planner launch for 160), so ranges move, and a range that ends inside a
+    # row's charge holds none of that row.  Every row, three heads.
+    w = dataclasses.replace(W.RAGGED_BF16, batch=rows)
+    inp = W.make_inputs(w, layout="flat", t_override=t)
+    step = _granular_and_fused(inp, heads=[0, 77, 127], expect_fused=rows <= 64)
+    assert _plan_charge(step, rows) > 0
 
 
 @pytest.mark.parametrize("top_k", [0, 120])
