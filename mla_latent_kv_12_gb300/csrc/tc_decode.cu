@@ -380,7 +380,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   uint8_t* xout = xin + 2 * XH_BYTES;                // 2 x XH_BYTES
 
   __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES];
-  __shared__ __align__(8) uint64_t s_full, s_free, p_full, pv_done, q_full, o_free, mma_drain, pv_drain;
+  __shared__ __align__(8) uint64_t s_full, s_free, p_full, q_full, o_free, mma_drain, pv_drain;
   __shared__ __align__(8) uint64_t x_full[2], x_free[2], xo_free[2];  // per exchange buffer
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
@@ -411,7 +411,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     mbar_init(&s_full, 1);
     mbar_init(&s_free, 4);      // the exchange warps have read S
     mbar_init(&p_full, 4);      // one arrival per softmax warp
-    mbar_init(&pv_done, 1);
     mbar_init(&q_full, 4);      // the exchange warps have written this segment's query into TMEM
     mbar_init(&o_free, 4);
     for (int b = 0; b < 2; ++b) {
@@ -675,8 +674,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           for (int k = 0; k < BN / 16; ++k)
             mma_ts(tmem + TM_O, tmem + TM_P + k * 8, d0 + (uint64_t)((k * 2048) >> 4), idesc_pv,
                    k == 0 ? acc0 : 1u);
+          // one commit: the stage barrier also tells the softmax warps that
+          // this P.V has completed (a second commit costs its own latency)
           mma_commit(&empty_bar[stage]);
-          mma_commit(&pv_done);
         }
         __syncwarp();
         ++tile;
@@ -830,7 +830,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     x_free_peer[0] = mapa(smem_u32(&x_free[0]), peer);
     x_free_peer[1] = mapa(smem_u32(&x_free[1]), peer);
     uint32_t tile = 0, seg = 0;
-    uint32_t pv_seen = 0;   // P.V completions waited for
+    // P.V(k) has completed once its commit arrives on the stage barrier
+    // empty_bar[k % STAGES] (that barrier's (k / STAGES)-th completion).  P.V's
+    // complete in order, and when P.V(k) is waited for, P.V(k - STAGES) has
+    // been waited for already and P.V(k + STAGES) cannot have started, so the
+    // phase parity identifies the completion.
+    auto wait_pv = [&](uint32_t k) -> bool {
+      return mbar_wait_warp(&empty_bar[k % STAGES], (k / STAGES) & 1u, kWaitLimit);
+    };
     int u, n, t0, t1;
     bool whole;
     while (!aborted() && it.next(u, t0, t1, whole)) {
@@ -957,11 +964,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const float psum = ps2[0].x + ps2[0].y;
         l = l * alpha + psum;
         // ---- P into TMEM once the previous P.V has consumed it (and O is stable)
-        while (pv_seen < tile) {
-          if (!mbar_wait_warp(&pv_done, pv_seen & 1u, kWaitLimit)) { fail(); break; }
-          ++pv_seen;
-        }
-        if (aborted()) break;
+        if (tile > 0 && !wait_pv(tile - 1)) { fail(); break; }
         tc_fence_after();
         // tcgen05.ld / st are warp-collective: the whole warp takes the
         // rescale pass when any of its heads needs it, the others with factor 1.
@@ -987,11 +990,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
       if (aborted()) break;
       // ---- epilogue: wait for the segment's last P.V
-      while (pv_seen < tile) {
-        if (!mbar_wait_warp(&pv_done, pv_seen & 1u, kWaitLimit)) { fail(); break; }
-        ++pv_seen;
-      }
-      if (aborted()) break;
+      if (!wait_pv(tile - 1)) { fail(); break; }
       tc_fence_after();
       // O leaves TMEM 32 columns at a time, the next chunk's load in flight
       // while the current one is stored.
