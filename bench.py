@@ -33,7 +33,7 @@ METRIC = "MLA decode tokens/s and latent-cache HBM GB/s (% of GB300 roofline)"
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode +
 # combine launch pair of the current kernels, from an ncu capture of this
 # bench's workload; absent when the kernels changed after the capture.
-MEASURED_TRAFFIC: dict = {}
+MEASURED_TRAFFIC: dict = {"ragged_bf16_b32_len1k_32k_h128": 620_408_064}
 L2_BYTES = 129 * 2 ** 20
 WORKLOADS = ("tiny_f32", "dense_bf16", "ragged_bf16", "sparse_bf16", "verify_bf16", "verify_sparse_bf16")
 HEADLINE = "ragged_bf16"
@@ -51,6 +51,9 @@ def parse(argv=None):
     ap.add_argument("--no-side", action="store_true", help="skip the append / top-k / rollback / prefill objects")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="rotate exactly this many layers' buffers (0: as many as flush the L2 between uses); "
+                         "a smaller count keeps a profiler capture's device memory small")
     return ap.parse_args(argv)
 
 
@@ -340,7 +343,7 @@ def layers_for(inp, step_bytes):
     return min(16, -(-2 * L2_BYTES // max(step_bytes, 1)) + 1)
 
 
-def measure(w, steps, warmup, dev, world, peaks, e2e=False, clocks=None):
+def measure(w, steps, warmup, dev, world, peaks, e2e=False, clocks=None, layers=0):
     """Times the whole step and the decode launches of workload ``w`` on R
     rotating layers with CUDA-graph replays.  Returns a dict."""
     import torch
@@ -352,7 +355,7 @@ def measure(w, steps, warmup, dev, world, peaks, e2e=False, clocks=None):
     inp = W.make_inputs(w, layout=layout_of(w))
     byts, flops = algorithmic(inp)
     sbytes, sflops = step_algorithmic(inp)
-    R = layers_for(inp, sbytes)
+    R = layers if layers > 0 else layers_for(inp, sbytes)
     steps_l = [DecodeStep(inp, dev) for _ in range(R)]
     one = steps_l[0]
     for s in steps_l:
@@ -605,7 +608,7 @@ def ours(args):
 
     w = workload(args.workload)
     with ClockSampler(local) as clk:
-        head = measure(w, args.steps, args.warmup, dev, world, peaks, e2e=True, clocks=clk)
+        head = measure(w, args.steps, args.warmup, dev, world, peaks, e2e=True, clocks=clk, layers=args.layers)
     inp, one, cap = head["_inp"], head["_steps"][0], head["_cap"]
     side = {} if args.no_side else side_objects(w, one, inp, dev, cap, peaks)
     del head["_steps"]
@@ -615,7 +618,7 @@ def ours(args):
             if name == args.workload:
                 per_config[workload(name).name] = {k: v for k, v in public(head).items() if k not in ("e2e", "clocks")}
                 continue
-            r = measure(workload(name), max(args.steps, 20), max(args.warmup, 3), dev, world, peaks)
+            r = measure(workload(name), max(args.steps, 20), max(args.warmup, 3), dev, world, peaks, layers=args.layers)
             per_config[r["workload"]] = public(r)
             del r
             torch.cuda.empty_cache()
@@ -631,7 +634,8 @@ def ours(args):
         "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "batch": w.batch, "s_q": w.s_q, "heads": w.heads,
                    "rank": w.rank, "rope": w.rope, "cached_keys": int(inp.kv_len.sum()), "layers": 1,
-                   "l2": f"rotating {head['layers']} layers' buffers (inputs of one step x layers > 2 x L2)",
+                   "l2": (f"rotating {head['layers']} layers' buffers (inputs of one step x layers > 2 x L2)"
+                          if args.layers <= 0 else f"{head['layers']} layers fixed by --layers (L2 not flushed)"),
                    "decode_kernel": head["kind"], "parallelism": f"replicas{world}"},
         "clocks": head.get("clocks"),
         "e2e": head["e2e"],
