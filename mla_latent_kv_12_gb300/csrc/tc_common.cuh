@@ -324,6 +324,22 @@ __device__ __forceinline__ void ld_global_v8(const float* p, float (&v)[8]) {
 
 // L2 prefetch of the line holding `p` (no data returned: safe on memory that an
 // earlier grid may still be writing).
+// L2 policy that keeps lines past lines of normal priority (evicted last).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// 16-byte and 4-byte global stores with an L2 cache policy.
+__device__ __forceinline__ void st_global_v4_policy(void* ptr, uint4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void st_global_f32_policy(float* ptr, float v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(ptr), "f"(v), "l"(pol) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }

@@ -1040,8 +1040,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         // context normalised by its own sum (O / l, an average of latent
         // rows, so within the range of the cache's values), with (m, l) in
         // f32 beside it.  A thread stores 8 dims of its head as one 16-byte
-        // vector, a warp 512 B contiguous.
+        // vector, a warp 512 B contiguous.  Stored with an evict-last L2
+        // policy: the combine reads them after the whole decode, and the
+        // cache stream would otherwise push the early pieces out to DRAM.
         const float inv = l > 0.f ? 1.f / l : 0.f;
+        const uint64_t keep = l2_policy_evict_last();
         uint4* dst = a.ws_o + (slot * (RANK / 8) + dim_base / 8) * HEADS + h;
         float vmax = 0.f;
         drain_o([&](int c, const uint32_t(&o)[32]) {
@@ -1055,13 +1058,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
               const __half2 hv = __floats2half2_rn(x0, x1);
               w[j] = *reinterpret_cast<const uint32_t*>(&hv);
             }
-            dst[(int64_t)(4 * c + q) * HEADS] = make_uint4(w[0], w[1], w[2], w[3]);
+            st_global_v4_policy(dst + (int64_t)(4 * c + q) * HEADS, make_uint4(w[0], w[1], w[2], w[3]), keep);
           }
         });
         if (!(vmax <= 65504.f) && a.status) atomicOr(a.status, MLA_DEVICE_VALUE_RANGE);
         if (rank == 0) {
-          a.ws_ml[(slot * 2) * HEADS + h] = l > 0.f ? m_used : -CUDART_INF_F;
-          a.ws_ml[(slot * 2 + 1) * HEADS + h] = l;
+          st_global_f32_policy(a.ws_ml + (slot * 2) * HEADS + h, l > 0.f ? m_used : -CUDART_INF_F, keep);
+          st_global_f32_policy(a.ws_ml + (slot * 2 + 1) * HEADS + h, l, keep);
         }
       }
       tc_fence_before();
