@@ -80,7 +80,13 @@ constexpr int kMinTilesPerGroup = 4;
 // group pays one start anyway, and a charge would only idle groups.
 constexpr int kUnitStartCharge = 10;
 constexpr int kChargeMinSpan = 32;
-constexpr int kPrefetchAhead = 6;    // tiles of the current row pulled into L2 ahead of their load
+// Tiles of the current row pulled into L2 ahead of their load (the decode
+// kernel's template parameter): farther for a lockstep group (the group's
+// pairs all read each tile, three of them from L2), nearer for a single row,
+// whose early prefetches the streamed cache evicts again before use.  A
+// compile-time distance: with a run-time one the lockstep verify decode ran
+// 3 % slower.
+constexpr int kPrefetchAheadGroup = 6, kPrefetchAheadRow = 4;
 constexpr int kQueryPrefetchTiles = 4;   // the next segment's query is pulled into L2 this many tiles before
 // Up to this many query rows, every CTA plans the split itself in its prologue
 // (no planner launch); larger batches use the planner kernel.
@@ -362,6 +368,7 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const __grid_constant__ T
 
 // ------------------------------------------------------------------ decode
 
+template <int kPrefetchAhead>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc_decode_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__ CUtensorMap rope_map,
                      const __grid_constant__ CUtensorMap lat_rows_map, const __grid_constant__ CUtensorMap rope_rows_map,
@@ -1557,8 +1564,10 @@ cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* works
         encode_tmap_bf16(&rope_rows_map, g.rope, 2, rd, rs, rbox, CU_TENSOR_MAP_SWIZZLE_64B))
       a.gather_tma = 1;
   }
+  const bool lockstep = a.width > 1;
+  auto* const decode_kernel = lockstep ? tc_decode_kernel<kPrefetchAheadGroup> : tc_decode_kernel<kPrefetchAheadRow>;
   {
-    const cudaError_t ea = set_max_dynamic_smem(tc_decode_kernel, SMEM_BYTES);
+    const cudaError_t ea = set_max_dynamic_smem(decode_kernel, SMEM_BYTES);
     if (ea != cudaSuccess) return ea;
   }
   cudaError_t e = cudaSuccess;
@@ -1566,7 +1575,7 @@ cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* works
     e = launch_pdl(tc_plan_kernel, dim3(1), dim3(1024), 0, stream, a);
     if (e != cudaSuccess) return e;
   }
-  e = launch_pdl(tc_decode_kernel, dim3(2 * nclusters), dim3(THREADS), SMEM_BYTES, stream, lat_map, rope_map,
+  e = launch_pdl(decode_kernel, dim3(2 * nclusters), dim3(THREADS), SMEM_BYTES, stream, lat_map, rope_map,
                  lat_rows_map, rope_rows_map, a);
   if (e != cudaSuccess) return e;
   if (tail == nullptr) {
