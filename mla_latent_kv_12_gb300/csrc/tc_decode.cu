@@ -58,7 +58,11 @@ constexpr int STAGE_BYTES = 4 * CHUNK_BYTES + ROPE_BYTES;
 constexpr int STAGE_TX = STAGE_BYTES;     // bytes one tile's loads deliver into a stage
 constexpr int XH_BYTES = 128 * BN * 2;    // fp16 partial scores of one tile (one send / receive buffer)
 constexpr int HEADS = 128, RANK = 512, DV = 256;  // DV: latent dims per CTA
-constexpr int THREADS = 352;   // producer, score MMA, 4 softmax, 4 exchange, P.V MMA warps
+// producer, score MMA, 4 softmax, 4 exchange and P.V MMA warps; a launch that
+// gathers selected rows by TMA adds a twelfth warp issuing half of each
+// tile's gathers (an idle one costs the dense launches ~1 us)
+constexpr int THREADS = 352, THREADS_GATHER = 384;
+constexpr int kGatherWarp = 11;
 // Dynamic shared memory: the stage ring, then send[2] and receive[2].  The
 // 1024-byte alignment of the extern declaration places it on a 1024-byte
 // boundary after the static variables (checked at run time).
@@ -223,6 +227,36 @@ __device__ __forceinline__ bool member_segment(const TcDecodeArgs& a, const int3
   return t0 < t1;
 }
 
+// TMA row gather of key group g (keys 4g..4g+3) of tile t into a stage: one
+// gather4 per 64-dim latent chunk and one for this CTA's 32 rope dims.
+// Entries past the count or out of range load the window's first row
+// (finite data; the softmax gives them p = 0).
+__device__ __forceinline__ void gather_key_group(const TcDecodeArgs& a, const CUtensorMap* lat_rows_map,
+                                                 const CUtensorMap* rope_rows_map, uint8_t* dst, uint64_t* bar,
+                                                 int g, int t, int b, int start, int limit, int keys,
+                                                 const int32_t* list, uint32_t rank, int dim_base) {
+  int lr[4], rr[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = t * BN + 4 * g + j;
+    bool v = e < keys;
+    int p = e;
+    if (v && list) {
+      p = list[e];
+      if (p < 0 || p >= limit) {
+        v = false;
+        if (a.status && rank == 0) atomicOr(a.status, MLA_DEVICE_INDEX_OUT_OF_RANGE);
+      }
+    }
+    const int w = start + (v ? p : 0);
+    lr[j] = b * a.lat_rows_per_batch + w;
+    rr[j] = b * a.rope_rows_per_batch + w;
+  }
+  for (int c = 0; c < 4; ++c)
+    tma_gather4(dst + c * CHUNK_BYTES + g * 4 * 128, lat_rows_map, bar, dim_base + 64 * c, lr[0], lr[1], lr[2], lr[3]);
+  tma_gather4(dst + 4 * CHUNK_BYTES + g * 4 * 64, rope_rows_map, bar, 32 * (int)rank, rr[0], rr[1], rr[2], rr[3]);
+}
+
 // ------------------------------------------------------------------ planner
 // Per query row the number of visible entries; the planner (or the decode
 // prologue) turns them into tiles and the exclusive prefix of tiles over work
@@ -369,7 +403,7 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const __grid_constant__ T
 // ------------------------------------------------------------------ decode
 
 template <int kPrefetchAhead>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_GATHER, 1)
     tc_decode_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__ CUtensorMap rope_map,
                      const __grid_constant__ CUtensorMap lat_rows_map, const __grid_constant__ CUtensorMap rope_rows_map,
                      const __grid_constant__ TcDecodeArgs a) {
@@ -452,8 +486,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     keys_p = plan_keys_s;
     prefix_p = plan_prefix_s;
     if (blockIdx.x == 0) {   // the combine kernel reads the plan from the workspace
-      for (int i = threadIdx.x; i < a.n_q; i += THREADS) a.keys[i] = plan_keys_s[i];
-      for (int i = threadIdx.x; i <= a.n_units + 1; i += THREADS) a.prefix[i] = plan_prefix_s[i];
+      for (int i = threadIdx.x; i < a.n_q; i += blockDim.x) a.keys[i] = plan_keys_s[i];
+      for (int i = threadIdx.x; i <= a.n_units + 1; i += blockDim.x) a.prefix[i] = plan_prefix_s[i];
     }
   }
   WorkIter it;
@@ -509,39 +543,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             }
           }
         } else if (a.gather_tma) {
-          // Row gather by TMA: lane g < 16 owns keys 4g..4g+3 of the tile and
-          // issues one gather4 per 64-dim chunk.  Entries past the count or out
-          // of range load the window's first row (finite data; the softmax
-          // gives them p = 0).
-          int lr[4], rr[4];
-          if (lane < 16) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int e = t * BN + 4 * lane + j;
-              bool v = e < keys;
-              int p = e;
-              if (v && list) {
-                p = list[e];
-                if (p < 0 || p >= limit) {
-                  v = false;
-                  if (a.status && rank == 0) atomicOr(a.status, MLA_DEVICE_INDEX_OUT_OF_RANGE);
-                }
-              }
-              const int w = start + (v ? p : 0);
-              lr[j] = b * a.lat_rows_per_batch + w;
-              rr[j] = b * a.rope_rows_per_batch + w;
-            }
-          }
+          // Row gather by TMA: groups of four keys, one gather4 per 64-dim
+          // chunk; lane g < 8 issues group g, and the second gather warp groups
+          // 8..15 (a warp issues these one lane at a time, ~100 cycles each).
+          // Its copies complete on the same barrier, whose expected bytes
+          // this warp announces for the whole stage.
           if (lane == 0) mbar_arrive_expect_tx(&full_bar[stage], STAGE_TX);
           __syncwarp();
-          if (lane < 16) {
-            uint8_t* dst = stages + stage * STAGE_BYTES;
-            for (int c = 0; c < 4; ++c)
-              tma_gather4(dst + c * CHUNK_BYTES + lane * 4 * 128, &lat_rows_map, &full_bar[stage], dim_base + 64 * c,
-                          lr[0], lr[1], lr[2], lr[3]);
-            tma_gather4(dst + 4 * CHUNK_BYTES + lane * 4 * 64, &rope_rows_map, &full_bar[stage], 32 * (int)rank,
-                        rr[0], rr[1], rr[2], rr[3]);
-          }
+          if (lane < 8)
+            gather_key_group(a, &lat_rows_map, &rope_rows_map, stages + stage * STAGE_BYTES, &full_bar[stage], lane,
+                             t, b, start, limit, keys, list, rank, dim_base);
         } else {
           // Row gather: lane L owns keys L and L+32 of the tile.
           const int e0 = t * BN + lane, e1 = e0 + 32;
@@ -695,6 +706,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (lane == 0) mma_commit(&pv_drain);
     __syncwarp();
     mbar_wait_warp(&pv_drain, 0, kWaitLimit);
+  } else if (warp == kGatherWarp) {
+    // ============================================================ second gather warp
+    // TMA row gathers of key groups 8..15 of every tile (selected positions
+    // only), following the producer's tiles, stages and stage waits.
+    if (gather && a.gather_tma) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int fills = 0;
+      int u, n, t0, t1;
+      bool whole;
+      while (!aborted() && it.next(u, t0, t1, whole)) {
+        if (!member_segment(a, keys_p, u, member, n, t0, t1)) continue;
+        const int b = n / a.s_q;
+        const int start = a.plan_in_kernel ? row_start_s[n] : (a.kv_start ? a.kv_start[b] : 0);
+        const int limit = a.plan_in_kernel ? row_limit_s[n] : row_limit(a, n);
+        const int keys = keys_p[n];
+        const int32_t* list = a.sel_count[n] != -1 ? a.sel + (int64_t)n * a.k_max : nullptr;
+        for (int t = t0; t < t1 && !aborted(); ++t) {
+          if (fills++ >= STAGES && !mbar_wait_warp(&empty_bar[stage], phase ^ 1u, kWaitLimit)) { fail(); break; }
+          if (lane < 8)
+            gather_key_group(a, &lat_rows_map, &rope_rows_map, stages + stage * STAGE_BYTES, &full_bar[stage],
+                             8 + lane, t, b, start, limit, keys, list, rank, dim_base);
+          if (++stage == STAGES) stage = 0, phase ^= 1u;
+        }
+      }
+    }
   } else if (warp >= 6 && warp < 10) {
     // ============================================================ exchange warps
     // Read this CTA's partial scores from TMEM, round them to fp16 (saturating)
@@ -1575,8 +1612,8 @@ cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* works
     e = launch_pdl(tc_plan_kernel, dim3(1), dim3(1024), 0, stream, a);
     if (e != cudaSuccess) return e;
   }
-  e = launch_pdl(decode_kernel, dim3(2 * nclusters), dim3(THREADS), SMEM_BYTES, stream, lat_map, rope_map,
-                 lat_rows_map, rope_rows_map, a);
+  e = launch_pdl(decode_kernel, dim3(2 * nclusters), dim3(a.gather_tma ? THREADS_GATHER : THREADS), SMEM_BYTES, stream,
+                 lat_map, rope_map, lat_rows_map, rope_rows_map, a);
   if (e != cudaSuccess) return e;
   if (tail == nullptr) {
     e = launch_pdl(tc_combine_kernel, dim3(n_q, RANK / CDIMS), dim3(g.heads), 0, stream, a);
