@@ -58,11 +58,12 @@ constexpr int STAGE_BYTES = 4 * CHUNK_BYTES + ROPE_BYTES;
 constexpr int STAGE_TX = STAGE_BYTES;     // bytes one tile's loads deliver into a stage
 constexpr int XH_BYTES = 128 * BN * 2;    // fp16 partial scores of one tile (one send / receive buffer)
 constexpr int HEADS = 128, RANK = 512, DV = 256;  // DV: latent dims per CTA
-// producer, score MMA, 4 softmax, 4 exchange and P.V MMA warps; a launch that
-// gathers selected rows by TMA adds a twelfth warp issuing half of each
-// tile's gathers (an idle one costs the dense launches ~1 us)
-constexpr int THREADS = 352, THREADS_GATHER = 384;
-constexpr int kGatherWarp = 11;
+// producer, score MMA, 4 softmax, 4 exchange and P.V MMA warps; the kernel
+// instance for TMA row gathers of selected positions adds two warps that share
+// each tile's gathers with the producer (its own instance: compiled for more
+// threads the dense kernel gets fewer registers and ran 3 % slower)
+constexpr int THREADS = 352, THREADS_GATHER = THREADS + 64;
+constexpr int kGatherWarp = 11;   // first extra gather warp
 // Dynamic shared memory: the stage ring, then send[2] and receive[2].  The
 // 1024-byte alignment of the extern declaration places it on a 1024-byte
 // boundary after the static variables (checked at run time).
@@ -402,8 +403,8 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const __grid_constant__ T
 
 // ------------------------------------------------------------------ decode
 
-template <int kPrefetchAhead>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_GATHER, 1)
+template <int kPrefetchAhead, int kThreads>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_decode_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__ CUtensorMap rope_map,
                      const __grid_constant__ CUtensorMap lat_rows_map, const __grid_constant__ CUtensorMap rope_rows_map,
                      const __grid_constant__ TcDecodeArgs a) {
@@ -543,16 +544,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_GATHER, 1)
             }
           }
         } else if (a.gather_tma) {
-          // Row gather by TMA: groups of four keys, one gather4 per 64-dim
-          // chunk; lane g < 8 issues group g, and the second gather warp groups
-          // 8..15 (a warp issues these one lane at a time, ~100 cycles each).
-          // Its copies complete on the same barrier, whose expected bytes
-          // this warp announces for the whole stage.
+          // Row gather by TMA: 16 groups of four keys, one gather4 per 64-dim
+          // chunk, shared by this warp and the extra gather warps (a warp
+          // issues them one lane at a time, ~100 cycles each): issuer i takes
+          // groups i, i + issuers, ...  The other issuers' copies complete on
+          // the same barrier, whose expected bytes this warp announces for
+          // the whole stage.
           if (lane == 0) mbar_arrive_expect_tx(&full_bar[stage], STAGE_TX);
           __syncwarp();
-          if (lane < 8)
-            gather_key_group(a, &lat_rows_map, &rope_rows_map, stages + stage * STAGE_BYTES, &full_bar[stage], lane,
-                             t, b, start, limit, keys, list, rank, dim_base);
+          constexpr int kIssuers = 1 + (kThreads - THREADS) / 32;
+          if (kIssuers * lane < BN / 4)
+            gather_key_group(a, &lat_rows_map, &rope_rows_map, stages + stage * STAGE_BYTES, &full_bar[stage],
+                             kIssuers * lane, t, b, start, limit, keys, list, rank, dim_base);
         } else {
           // Row gather: lane L owns keys L and L+32 of the tile.
           const int e0 = t * BN + lane, e1 = e0 + 32;
@@ -706,10 +709,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_GATHER, 1)
     if (lane == 0) mma_commit(&pv_drain);
     __syncwarp();
     mbar_wait_warp(&pv_drain, 0, kWaitLimit);
-  } else if (warp == kGatherWarp) {
-    // ============================================================ second gather warp
-    // TMA row gathers of key groups 8..15 of every tile (selected positions
+  } else if (kThreads > THREADS && warp >= kGatherWarp) {
+    // ============================================================ extra gather warps
+    // Their share of the TMA row gathers of every tile (selected positions
     // only), following the producer's tiles, stages and stage waits.
+    constexpr int kIssuers = 1 + (kThreads - THREADS) / 32;
+    const int issuer = 1 + (warp - kGatherWarp);
     if (gather && a.gather_tma) {
       int stage = 0;
       uint32_t phase = 0;
@@ -725,9 +730,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS_GATHER, 1)
         const int32_t* list = a.sel_count[n] != -1 ? a.sel + (int64_t)n * a.k_max : nullptr;
         for (int t = t0; t < t1 && !aborted(); ++t) {
           if (fills++ >= STAGES && !mbar_wait_warp(&empty_bar[stage], phase ^ 1u, kWaitLimit)) { fail(); break; }
-          if (lane < 8)
-            gather_key_group(a, &lat_rows_map, &rope_rows_map, stages + stage * STAGE_BYTES, &full_bar[stage],
-                             8 + lane, t, b, start, limit, keys, list, rank, dim_base);
+          const int g = issuer + kIssuers * lane;
+          if (g < BN / 4)
+            gather_key_group(a, &lat_rows_map, &rope_rows_map, stages + stage * STAGE_BYTES, &full_bar[stage], g, t,
+                             b, start, limit, keys, list, rank, dim_base);
           if (++stage == STAGES) stage = 0, phase ^= 1u;
         }
       }
@@ -1602,7 +1608,11 @@ cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* works
       a.gather_tma = 1;
   }
   const bool lockstep = a.width > 1;
-  auto* const decode_kernel = lockstep ? tc_decode_kernel<kPrefetchAheadGroup> : tc_decode_kernel<kPrefetchAheadRow>;
+  // (the prefetch distance only serves the dense path; gathers take the
+  // instance with the extra gather warps)
+  auto* const decode_kernel = a.gather_tma ? tc_decode_kernel<kPrefetchAheadRow, THREADS_GATHER>
+                              : lockstep   ? tc_decode_kernel<kPrefetchAheadGroup, THREADS>
+                                           : tc_decode_kernel<kPrefetchAheadRow, THREADS>;
   {
     const cudaError_t ea = set_max_dynamic_smem(decode_kernel, SMEM_BYTES);
     if (ea != cudaSuccess) return ea;
