@@ -59,10 +59,10 @@ constexpr int STAGE_TX = STAGE_BYTES;     // bytes one tile's loads deliver into
 constexpr int XH_BYTES = 128 * BN * 2;    // fp16 partial scores of one tile (one send / receive buffer)
 constexpr int HEADS = 128, RANK = 512, DV = 256;  // DV: latent dims per CTA
 // producer, score MMA, 4 softmax, 4 exchange and P.V MMA warps; the kernel
-// instance for TMA row gathers of selected positions adds two warps that share
-// each tile's gathers with the producer (its own instance: compiled for more
-// threads the dense kernel gets fewer registers and ran 3 % slower)
-constexpr int THREADS = 352, THREADS_GATHER = THREADS + 64;
+// instance for TMA row gathers of selected positions adds three warps that
+// share each tile's gathers with the producer (its own instance: compiled for
+// more threads the dense kernel gets fewer registers and ran 3 % slower)
+constexpr int THREADS = 352, THREADS_GATHER = THREADS + 96;
 constexpr int kGatherWarp = 11;   // first extra gather warp
 // Dynamic shared memory: the stage ring, then send[2] and receive[2].  The
 // 1024-byte alignment of the extern declaration places it on a 1024-byte
