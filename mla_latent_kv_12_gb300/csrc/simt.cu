@@ -68,7 +68,6 @@ __device__ __forceinline__ RowKeys row_keys(const DecodeGeometry& g, int n) {
 
 constexpr int kDecodeWarps = 4;
 constexpr int kMaxD = 1280;            // rank + rope
-constexpr int kMaxPerLane = kMaxD / 32;  // 40
 constexpr int kMaxRank = 1024;
 constexpr int kMaxRankPerLane = kMaxRank / 32;
 
