@@ -13,7 +13,6 @@ namespace mla {
 namespace {
 
 __device__ __forceinline__ float to_f(float x) { return x; }
-__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 template <typename T>
 __device__ __forceinline__ T cvt(float x);
 template <>
