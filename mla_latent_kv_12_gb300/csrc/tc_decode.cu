@@ -906,6 +906,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int32_t* list = (gather && a.sel_count[n] != -1) ? a.sel + (int64_t)n * a.k_max : nullptr;
       float m_used = -CUDART_INF_F, l = 0.f;
       bool first_tile = true;
+      // Selected positions of the lane's two entries of the next tile, read a
+      // tile ahead so that their load is not on the path of the tile's scores.
+      int pos0 = 0, pos1 = 0;
+      if (list) {
+        const int e0 = t0 * BN + lane, e1 = e0 + 32;
+        if (e0 < keys) pos0 = __ldg(list + e0);
+        if (e1 < keys) pos1 = __ldg(list + e1);
+      }
       for (int t = t0; t < t1; ++t) {
         // ---- validity of this tile's 64 entries (lane L: entries L, L+32);
         // a whole tile of a dense row needs no check (warp-uniform test)
@@ -914,8 +922,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int e0 = t * BN + lane, e1 = e0 + 32;
           bool v0 = e0 < keys, v1 = e1 < keys;
           if (list) {
-            if (v0) { const int p = list[e0]; v0 = p >= 0 && p < limit; }
-            if (v1) { const int p = list[e1]; v1 = p >= 0 && p < limit; }
+            v0 = v0 && pos0 >= 0 && pos0 < limit;
+            v1 = v1 && pos1 >= 0 && pos1 < limit;
+            if (t + 1 < t1) {
+              if (e0 + BN < keys) pos0 = __ldg(list + e0 + BN);
+              if (e1 + BN < keys) pos1 = __ldg(list + e1 + BN);
+            }
           }
           valid = (uint64_t)__ballot_sync(0xffffffffu, v0) | ((uint64_t)__ballot_sync(0xffffffffu, v1) << 32);
         }
