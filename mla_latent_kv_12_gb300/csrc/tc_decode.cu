@@ -236,14 +236,20 @@ __device__ __forceinline__ void gather_key_group(const TcDecodeArgs& a, const CU
                                                  const CUtensorMap* rope_rows_map, uint8_t* dst, uint64_t* bar,
                                                  int g, int t, int b, int start, int limit, int keys,
                                                  const int32_t* list, uint32_t rank, int dim_base) {
-  int lr[4], rr[4];
+  int lr[4], rr[4], pos[4];
+  // the four positions are read before any is checked: one round trip (a
+  // status update between reads would order them)
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = t * BN + 4 * g + j;
+    pos[j] = (list && e < keys) ? __ldg(list + e) : e;
+  }
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int e = t * BN + 4 * g + j;
     bool v = e < keys;
-    int p = e;
+    int p = pos[j];
     if (v && list) {
-      p = list[e];
       if (p < 0 || p >= limit) {
         v = false;
         if (a.status && rank == 0) atomicOr(a.status, MLA_DEVICE_INDEX_OUT_OF_RANGE);
