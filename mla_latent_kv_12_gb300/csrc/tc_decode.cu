@@ -1170,19 +1170,49 @@ __device__ __forceinline__ void unpack_partial(const uint4 r, float (&x)[8]) {
   }
 }
 
-// grid (n_q, RANK / CDIMS); 128 threads = heads; thread h merges dims
+// grid (n_q, RANK / CDIMS); 128 threads, thread h < heads merges dims
 // [d0, d0 + CDIMS) of head h over the row's pieces.  Partials are stored as
 // [slot][RANK/8][H] entries of 8 fp16 dims, so a warp's 16-byte loads per
-// piece read 512 B.
+// piece read 512 B.  The loads of up to kCombineBatch pieces are issued
+// together, and batches are merged online.  Few rows have many pieces each
+// (one row of 4096 keys: 16) and a small grid, many rows a few pieces each and
+// a grid of several thousand CTAs: the batch is chosen per launch, since its
+// registers bound the CTAs resident per SM.
 constexpr int CDIMS = 8;
+constexpr int kCombineWideRows = 8;   // rows up to which the combine loads 16 pieces at once
 
+template <int kCombineBatch>
 __global__ void __launch_bounds__(128) tc_combine_kernel(const __grid_constant__ TcDecodeArgs a) {
-  pdl_wait();
+  __shared__ int32_t keys_s[kMaxRowsInKernelPlan];
+  __shared__ int32_t prefix_s[kMaxRowsInKernelPlan + 2];
   const int n = blockIdx.x;
   const int d0 = blockIdx.y * CDIMS;
   const int h = threadIdx.x;
-  if (h >= a.heads) return;
   const int u = n / a.width, member = n % a.width;
+  // The row's pieces, before the wait.  The plan depends only on the call's
+  // inputs and, above kMaxRowsInKernelPlan rows, on the planner launch: every
+  // decode CTA passes its own dependency wait before it lets this grid start,
+  // so all of those launches have completed.  (The copy of an in-kernel plan
+  // that the decode kernel stores is not read: it is visible only after the
+  // wait.)
+  int keys;
+  const int32_t* prefix;
+  if (a.plan_in_kernel) {
+    plan_rows(a, keys_s, prefix_s, false);   // 128 threads >= n_q
+    keys = keys_s[n];
+    prefix = prefix_s;
+  } else {
+    keys = a.keys[n];
+    prefix = a.prefix;
+  }
+  int c0 = 0, c1 = 0;
+  if (keys != 0) {
+    const int per = group_span(a, prefix[a.n_units]);
+    c0 = first_group_of(prefix, u, per, prefix[a.n_units + 1]);
+    c1 = last_group_of(prefix, u, per);
+  }
+  pdl_wait();
+  if (h >= a.heads) return;
   const int64_t orow = (int64_t)n * a.ctx_row_stride + (int64_t)h * a.ctx_head_stride + d0;
   float acc[CDIMS];
 #pragma unroll
@@ -1190,37 +1220,46 @@ __global__ void __launch_bounds__(128) tc_combine_kernel(const __grid_constant__
   float M = -CUDART_INF_F, L = 0.f;
   static_assert(CDIMS == 8, "one 8-dim group of the partial layout per thread");
   bool write = true;
-  if (a.keys[n] != 0) {
-    const int per = group_span(a, a.prefix[a.n_units]);
-    const int c0 = first_group_of(a.prefix, u, per, a.prefix[a.n_units + 1]), c1 = last_group_of(a.prefix, u, per);
+  if (keys != 0) {
     if (c0 == c1) {
       write = false;                       // finished in place by its group
     } else {
       auto slot_of = [&](int g) -> int64_t { return ((int64_t)u + g) * a.width + member; };
-      for (int c = c0; c <= c1; ++c) M = fmaxf(M, a.ws_ml[(slot_of(c) * 2) * HEADS + h]);
-      for (int c = c0; c <= c1; c += 4) {
-        float wc[4], x[4][CDIMS];
-        uint4 raw[4];
+      for (int cb = c0; cb <= c1; cb += kCombineBatch) {
+        float mq[kCombineBatch], lq[kCombineBatch];
+        uint4 raw[kCombineBatch];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          wc[q] = 0.f;
+        for (int q = 0; q < kCombineBatch; ++q) {
+          mq[q] = -CUDART_INF_F;
+          lq[q] = 0.f;
           raw[q] = make_uint4(0, 0, 0, 0);
-          if (c + q <= c1) {
-            const int64_t sl = slot_of(c + q);
-            const float mc = a.ws_ml[(sl * 2) * HEADS + h];
-            if (mc != -CUDART_INF_F) {
-              wc[q] = exp2f(mc - M) * a.ws_ml[(sl * 2 + 1) * HEADS + h];   // the piece's weight e^(m-M) l
-              L += wc[q];
-            }
+          if (cb + q <= c1) {
+            const int64_t sl = slot_of(cb + q);
+            mq[q] = a.ws_ml[(sl * 2) * HEADS + h];
+            lq[q] = a.ws_ml[(sl * 2 + 1) * HEADS + h];
             raw[q] = ld_partial(a.ws_o + (sl * (RANK / 8) + d0 / 8) * HEADS + h);
           }
         }
+        float mb = M;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) unpack_partial(raw[q], x[q]);
+        for (int q = 0; q < kCombineBatch; ++q) mb = fmaxf(mb, mq[q]);
+        if (mb == -CUDART_INF_F) continue;   // every piece so far is empty
+        const float f = exp2f(M - mb);       // 0 while M is still -inf
+        L *= f;
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int j = 0; j < CDIMS; ++j) acc[j] *= f;
+        M = mb;
 #pragma unroll
-          for (int j = 0; j < CDIMS; ++j) acc[j] = (wc[q] != 0.f) ? fmaf(wc[q], x[q][j], acc[j]) : acc[j];
+        for (int q = 0; q < kCombineBatch; ++q) {
+          // the piece's weight e^(m - M) l; an empty piece (m = -inf) has weight
+          // 0 and its context, never written, is not read into the sum
+          const float w = mq[q] != -CUDART_INF_F ? exp2f(mq[q] - M) * lq[q] : 0.f;
+          L += w;
+          float x[CDIMS];
+          unpack_partial(raw[q], x);
+#pragma unroll
+          for (int j = 0; j < CDIMS; ++j) acc[j] = (w != 0.f) ? fmaf(w, x[j], acc[j]) : acc[j];
+        }
       }
       const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
@@ -1644,7 +1683,10 @@ cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* works
                  lat_map, rope_map, lat_rows_map, rope_rows_map, a);
   if (e != cudaSuccess) return e;
   if (tail == nullptr) {
-    e = launch_pdl(tc_combine_kernel, dim3(n_q, RANK / CDIMS), dim3(g.heads), 0, stream, a);
+    // batch 16 (128 registers, 4 CTAs per SM) while the grid fits one wave
+    // at that occupancy, else 4
+    auto* const combine = n_q <= kCombineWideRows ? tc_combine_kernel<16> : tc_combine_kernel<4>;
+    e = launch_pdl(combine, dim3(n_q, RANK / CDIMS), dim3(HEADS), 0, stream, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
