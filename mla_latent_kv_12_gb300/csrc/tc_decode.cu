@@ -409,7 +409,13 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const __grid_constant__ T
 
 // ------------------------------------------------------------------ decode
 
-template <int kPrefetchAhead, int kThreads>
+// kLateP: a tile's P is announced to the P.V issuer only once the next tile's
+// score halves have arrived (for the lockstep verify groups, whose tensor work
+// per tile is four tokens' worth: each P.V then follows the next tile's score
+// MMAs instead of delaying them; single rows lose by the added P.V latency).
+// Without deadlock: the next tile's scores wait on the P.V STAGES tiles back
+// (its stage) and on the exchange of this tile's, in both CTAs, never on this P.V.
+template <int kPrefetchAhead, int kThreads, bool kLateP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_decode_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__ CUtensorMap rope_map,
                      const __grid_constant__ CUtensorMap lat_rows_map, const __grid_constant__ CUtensorMap rope_rows_map,
@@ -912,6 +918,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int32_t* list = (gather && a.sel_count[n] != -1) ? a.sel + (int64_t)n * a.k_max : nullptr;
       float m_used = -CUDART_INF_F, l = 0.f;
       bool first_tile = true;
+      bool p_pending = false;   // kLateP: the previous tile's P is not yet announced
       // Selected positions of the lane's two entries of the next tile, read a
       // tile ahead so that their load is not on the path of the tile's scores.
       int pos0 = 0, pos1 = 0;
@@ -943,6 +950,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // the phase: a CTA-scope acquire, as for a TMA load)
         const uint32_t b = tile & 1u, use = tile >> 1;
         if (!mbar_wait_warp(&x_full[b], use & 1u, kWaitLimit)) { fail(); break; }
+        if (kLateP && p_pending) {
+          if (lane == 0) mbar_arrive(&p_full);
+          p_pending = false;
+        }
         // ---- x = own + peer - m_ref in the log2 domain (both halves arrive
         // already scaled), as two fp16-operand additions per score (exact
         // conversions, f32 arithmetic), relative to the running maximum m_ref
@@ -1052,7 +1063,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full);
+        if (kLateP && t + 1 < t1)
+          p_pending = true;
+        else if (lane == 0)
+          mbar_arrive(&p_full);
         first_tile = false;
         ++tile;
       }
@@ -1667,9 +1681,9 @@ cudaError_t launch_tc_decode(const DecodeGeometry& g, int out_dtype, void* works
   const bool lockstep = a.width > 1;
   // (the prefetch distance only serves the dense path; gathers take the
   // instance with the extra gather warps)
-  auto* const decode_kernel = a.gather_tma ? tc_decode_kernel<kPrefetchAheadRow, THREADS_GATHER>
-                              : lockstep   ? tc_decode_kernel<kPrefetchAheadGroup, THREADS>
-                                           : tc_decode_kernel<kPrefetchAheadRow, THREADS>;
+  auto* const decode_kernel = a.gather_tma ? tc_decode_kernel<kPrefetchAheadRow, THREADS_GATHER, false>
+                              : lockstep   ? tc_decode_kernel<kPrefetchAheadGroup, THREADS, true>
+                                           : tc_decode_kernel<kPrefetchAheadRow, THREADS, false>;
   {
     const cudaError_t ea = set_max_dynamic_smem(decode_kernel, SMEM_BYTES);
     if (ea != cudaSuccess) return ea;
