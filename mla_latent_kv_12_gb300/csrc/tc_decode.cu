@@ -28,12 +28,16 @@
 //    gathers for selected positions, plus L2 prefetch ahead); warp 1 issues the
 //    score MMAs; warps 6..9 read the scores from TMEM and run the exchange;
 //    warps 2..5 (one thread per head) run the online softmax (log2 domain,
-//    lazy rescale) and the epilogue; warp 10 issues the P.V MMAs.
+//    lazy rescale) and the epilogue; warp 10 issues the P.V MMAs.  The
+//    instance for TMA row gathers adds warps 11..13, which issue their share
+//    of each tile's gather4 copies.
 //  * Split-K: each query row's tiles are counted (by every CTA in its prologue
 //    for up to 128 rows, else by a planner kernel); the flattened tile
-//    sequence is cut into equal ranges, one per cluster group.  A row wholly
-//    inside one range is finished in place; otherwise each piece writes an f32
-//    partial (O, m, l) and a combine kernel merges them.
+//    sequence, in which each row start is charged a few tiles when the ranges
+//    are long, is cut into equal ranges, one per cluster group.  A row wholly
+//    inside one range is finished in place; otherwise each piece writes its
+//    normalised context O / l in fp16 with (m, l) in f32, and a combine kernel
+//    merges them.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math_constants.h>
