@@ -95,7 +95,7 @@ constexpr int kChargeMinSpan = 32;
 // whose early prefetches the streamed cache evicts again before use.  A
 // compile-time distance: with a run-time one the lockstep verify decode ran
 // 3 % slower.
-constexpr int kPrefetchAheadGroup = 8, kPrefetchAheadRow = 4;
+constexpr int kPrefetchAheadGroup = 8, kPrefetchAheadRow = 3;
 constexpr int kQueryPrefetchTiles = 4;   // the next segment's query is pulled into L2 this many tiles before
 // Up to this many query rows, every CTA plans the split itself in its prologue
 // (no planner launch); larger batches use the planner kernel.
