@@ -502,7 +502,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     plan_rows(a, plan_keys_s, plan_prefix_s, blockIdx.x == 0, row_start_s, row_limit_s);
     keys_p = plan_keys_s;
     prefix_p = plan_prefix_s;
-    if (blockIdx.x == 0) {   // the combine kernel reads the plan from the workspace
+    if (blockIdx.x == 0) {   // a copy in the workspace, where the planner launch puts it above 128 rows
       for (int i = threadIdx.x; i < a.n_q; i += blockDim.x) a.keys[i] = plan_keys_s[i];
       for (int i = threadIdx.x; i <= a.n_units + 1; i += blockDim.x) a.prefix[i] = plan_prefix_s[i];
     }
