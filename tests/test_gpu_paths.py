@@ -6,6 +6,9 @@
   several row blocks.
 * Long rows: the split plan charges each row start, in the prologue and in
   the planner launch.
+* Many split pieces per row: the combine loads a batch of pieces at once and
+  merges the batches online (a rescale when a later batch holds a larger
+  maximum); the fused tail's thread groups share a row's pieces.
 * A cache whose batch stride is not a whole number of rows: selected rows
   are gathered with 16-byte cp.async loads instead of TMA gather4.
 * The fp16 exchange of the two half scores of an SM pair: the range over
@@ -136,6 +139,18 @@ def test_charged_split_plan_every_row(rows, t):
     inp = W.make_inputs(w, layout="flat", t_override=t)
     step = _granular_and_fused(inp, heads=[0, 77, 127], expect_fused=rows <= 64)
     assert _plan_charge(step, rows) > 0
+
+
+@pytest.mark.parametrize("batch,t", [(1, 40000), (3, 20000)])
+def test_combine_merges_many_pieces_per_row(batch, t):
+    # One row of 40,000 keys is 625 tiles; the 76 SM pairs of a GB300 take
+    # ranges of 9 (no row-start charge at this length), so the row has 70
+    # pieces: five batches of the combine's 16, and nine pieces for each of the
+    # fused tail's eight thread groups.  Three rows of 20,000 keys: ~24 pieces
+    # each.
+    w = dataclasses.replace(W.DENSE_BF16, batch=batch, t=t)
+    inp = W.make_inputs(w)
+    _granular_and_fused(inp, heads=[0, 127] if batch == 1 else [9, 64])
 
 
 @pytest.mark.parametrize("top_k", [0, 120])
