@@ -150,8 +150,6 @@ __device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t count, bool 
   return r != 0;
 }
 
-// 2^x on the special-function unit (PTX ex2.approx; relative error ~2^-22,
-// +0 for -inf).
 // f32(h) + c for the low / high fp16 half h of `w` (the conversion is exact;
 // one f32 rounding).
 __device__ __forceinline__ float add_f16lo(uint32_t w, float c) {
@@ -191,6 +189,8 @@ __device__ __forceinline__ float2 add_f32x2(float2 a, float2 b) {
   return d;
 }
 
+// 2^x on the special-function unit (PTX ex2.approx; relative error ~2^-22,
+// +0 for -inf).
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

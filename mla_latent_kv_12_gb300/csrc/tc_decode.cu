@@ -1035,8 +1035,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 8; ++k) ps2[k] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < BN; k += 2) {
-          const float p0 = ex2_approx(x[k] - shift);
-          const float p1 = ex2_approx(x[k + 1] - shift);
+          const float2 xs = add_f32x2(make_float2(x[k], x[k + 1]), make_float2(-shift, -shift));
+          const float p0 = ex2_approx(xs.x);
+          const float p1 = ex2_approx(xs.y);
           ps2[(k >> 1) & 7] = add_f32x2(ps2[(k >> 1) & 7], make_float2(p0, p1));
           const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
           pk[k >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
