@@ -33,7 +33,7 @@ METRIC = "MLA decode tokens/s and latent-cache HBM GB/s (% of GB300 roofline)"
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode +
 # combine launch pair of the current kernels, from an ncu capture of this
 # bench's workload; absent when the kernels changed after the capture.
-MEASURED_TRAFFIC: dict = {}
+MEASURED_TRAFFIC: dict = {"ragged_bf16_b32_len1k_32k_h128": 601_256_192}
 L2_BYTES = 129 * 2 ** 20
 WORKLOADS = ("tiny_f32", "dense_bf16", "ragged_bf16", "sparse_bf16", "verify_bf16", "verify_sparse_bf16")
 HEADLINE = "ragged_bf16"
