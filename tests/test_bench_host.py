@@ -1,5 +1,6 @@
 """Host-side logic of bench.py: max-over-ranks timing with two gloo ranks on CPU,
-the reference arm's rank rule, and the algorithmic byte / flop counts."""
+the reference arm's rank rule, the algorithmic byte / flop counts, the
+roofline's bound and fraction, and the clock record's summary."""
 import json
 import os
 import socket
@@ -116,3 +117,31 @@ def test_algorithmic_counts():
     byts, flops = bench.algorithmic(inp)
     assert byts == 2 * 100 * 1152                 # each row's window read once
     assert flops == 2 * (97 + 98 + 99 + 100) * 2 * 128 * 1088
+
+
+def test_roofline_takes_the_slower_bound():
+    # The ragged pair: 573.8 MB of cache and 138.7 GFLOP in 130.4 us -> HBM-bound.
+    r = bench.roofline(573_754_752, 138_721_148_928, 130.4e-6, 6687.1, 1935.2, "measured")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 6687.1
+    assert r["achieved"] == pytest.approx(573_754_752 / 130.4e-6 / 1e9)
+    assert r["frac"] == pytest.approx(r["achieved"] / 6687.1)
+    assert 0.65 < r["frac"] < 0.67
+    # The verify pair: 604 MB and 584 GFLOP (967 flop/B, above the ridge) -> tensor-bound.
+    v = bench.roofline(603_979_776, 584_102_182_912, 433.4e-6, 6687.1, 1935.2, "measured")
+    assert v["bound"] == "tensor" and v["unit"] == "TFLOP/s"
+    assert v["frac"] == pytest.approx(584_102_182_912 / 433.4e-6 / 1e12 / 1935.2)
+    # exactly at the ridge the bytes decide
+    ridge = bench.roofline(6687.1e9, 1935.2e12, 1.0, 6687.1, 1935.2, "measured")
+    assert ridge["bound"] == "hbm" and ridge["frac"] == pytest.approx(1.0)
+
+
+def test_clock_summary_reasons():
+    cs = bench.ClockSampler(0)
+    assert cs.summary()["reasons"] == ["unavailable"] and cs.summary()["samples"] == 0
+    row = lambda sm, cap: [sm, "2070", "1100.5", "0x0", "Not Active", "Not Active", "Not Active", cap]
+    cs.samples = [(1.0, row("2070", "Not Active")), (2.0, row("2040", "Active")), (3.0, row("2070", "Not Active"))]
+    s = cs.summary()
+    assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0 and s["samples"] == 3
+    assert s["reasons"] == ["sw_power_cap"]
+    # samples before the timed region are left out
+    assert cs.summary(since=2.5)["reasons"] == [] and cs.summary(since=2.5)["samples"] == 1
